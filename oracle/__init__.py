@@ -1,0 +1,198 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention (test infrastructure).
+
+This package is the oracle that the CUDA kernels are checked against.  Only the
+test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import it; the product path never does.  It shares no code with the CUDA
+library: the arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over
+rows), and this module only marshals numpy arrays into it.
+
+Functions and the passages they follow:
+
+* ``attention_fwd`` -- the direct two-pass softmax(scale * Q K^T) V with the
+  per-row log-sum-exp ("Pourquoi l'attention est liée à la mémoire",
+  marketmaker.cc; "Problema e motivação", FlashAttention reading guide).
+* ``attention_fwd_blockwise`` -- the tiled online-softmax recurrence in the
+  pages' order ("L'algorithme Flash Attention", marketmaker.cc; "Método" and
+  "Rastreamento Incremental do Softmax", reading guide), with the output either
+  renormalised per step or divided by the running sum at the end (the deferred
+  form of "FA2 : parallélisme" and of the loop on the Ultralytics page).
+* ``attention_bwd`` / ``attention_bwd_rows`` -- gradients from the derivative of
+  the definition ("Passe arrière : recalculer au lieu de stocker" only says that
+  P is recomputed from the saved statistics; the formulas are calculus).
+
+Masks: ``mask`` is a uint8 array of shape [T, T] (shared by every batch and
+head) or [B, H, T, T], with T = ceil(N / mask_block); entry [i // mb, j // mb]
+keeps (1) or hides (0) the pair (query i, key j) ("Extensão: Block-Sparse
+FlashAttention", reading guide).  Causal hides keys j > i.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_SO = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``liboracle.so`` next to it (gcc, OpenMP)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=gnu11", "-fopenmp", "-fPIC", "-shared",
+               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_SO)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    LL = ctypes.c_longlong
+    Dd = ctypes.c_double
+    F = ctypes.c_float
+    lib.orc_num_threads.restype = I
+    lib.orc_fwd.argtypes = [I, I, I, I, P, P, P, Dd, I, P, I, LL, LL, P, P]
+    lib.orc_fwd_rows.argtypes = [I, I, P, P, P, Dd, I, P, I, I, P, P, P]
+    lib.orc_fwd_blockwise_f64.argtypes = [I, I, I, I, P, P, P, Dd, I, P, I, LL, LL,
+                                          I, I, I, P, P]
+    lib.orc_fwd_blockwise_f32.argtypes = [I, I, I, I, P, P, P, F, I, P, I, LL, LL,
+                                          I, I, I, P, P]
+    lib.orc_bwd.argtypes = [I, I, I, I, P, P, P, P, Dd, I, P, I, LL, LL, P, P, P]
+    lib.orc_bwd_rows.argtypes = [I, I, P, P, P, P, Dd, I, P, I, I, P, P, I, P, P, P]
+    for f in ("orc_fwd", "orc_fwd_rows", "orc_fwd_blockwise_f64",
+              "orc_fwd_blockwise_f32", "orc_bwd", "orc_bwd_rows"):
+        getattr(lib, f).restype = None
+    _lib = lib
+    return lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on."""
+    return int(_load().orc_num_threads())
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _mask_args(mask, B, H, N, mask_block):
+    """(pointer, kept array, batch stride, head stride) for the C side."""
+    if mask is None:
+        return None, None, 0, 0
+    m = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
+    T = (N + mask_block - 1) // mask_block
+    if m.ndim == 2:
+        if m.shape != (T, T):
+            raise ValueError(f"mask shape {m.shape} != {(T, T)}")
+        return _ptr(m), m, 0, 0
+    if m.ndim == 4 and m.shape[2:] == (T, T):
+        if m.shape[0] not in (1, B) or m.shape[1] not in (1, H):
+            raise ValueError(f"mask shape {m.shape} does not broadcast to B={B}, H={H}")
+        sh = T * T if m.shape[1] > 1 else 0
+        sb = m.shape[1] * T * T if m.shape[0] > 1 else 0
+        return _ptr(m), m, sb, sh
+    raise ValueError(f"mask shape {m.shape} is neither [T,T] nor [B,H,T,T] with T={T}")
+
+
+def _head_mask(mask, b, h, N, mask_block):
+    if mask is None:
+        return None
+    m = np.asarray(mask, dtype=np.uint8)
+    if m.ndim == 4:
+        m = m[b if m.shape[0] > 1 else 0, h if m.shape[1] > 1 else 0]
+    return np.ascontiguousarray(m)
+
+
+def attention_fwd(q, k, v, scale, causal=False, mask=None, mask_block=128):
+    """Direct forward over whole [B,H,N,d] tensors -> (O [B,H,N,d], LSE [B,H,N]), fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = q.shape
+    O = np.zeros_like(q)
+    LSE = np.zeros((B, H, N), dtype=np.float64)
+    mp, keep, sb, sh = _mask_args(mask, B, H, N, mask_block)
+    _load().orc_fwd(B, H, N, d, _ptr(q), _ptr(k), _ptr(v), float(scale), int(bool(causal)),
+                    mp, int(mask_block), sb, sh, _ptr(O), _ptr(LSE))
+    return O, LSE
+
+
+def attention_fwd_rows(qh, kh, vh, rows, scale, causal=False, mask_h=None, mask_block=128):
+    """Direct forward of selected query rows of one head ([N,d] tensors).
+
+    Returns (O_rows [len(rows), d], LSE_rows [len(rows)]).
+    """
+    qh, kh, vh = _f64(qh), _f64(kh), _f64(vh)
+    N, d = qh.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    O = np.zeros((len(rows), d), dtype=np.float64)
+    L = np.zeros(len(rows), dtype=np.float64)
+    m = None if mask_h is None else np.ascontiguousarray(np.asarray(mask_h, dtype=np.uint8))
+    _load().orc_fwd_rows(N, d, _ptr(qh), _ptr(kh), _ptr(vh), float(scale), int(bool(causal)),
+                         None if m is None else _ptr(m), int(mask_block), len(rows),
+                         _ptr(rows), _ptr(O), _ptr(L))
+    return O, L
+
+
+def attention_fwd_blockwise(q, k, v, scale, Br, Bc, causal=False, mask=None, mask_block=128,
+                            precision="f64", norm_at_end=False):
+    """Blockwise online-softmax forward -> (O, LSE) in the requested precision."""
+    dt = np.float64 if precision == "f64" else np.float32
+    q = np.ascontiguousarray(np.asarray(q, dtype=dt))
+    k = np.ascontiguousarray(np.asarray(k, dtype=dt))
+    v = np.ascontiguousarray(np.asarray(v, dtype=dt))
+    B, H, N, d = q.shape
+    O = np.zeros_like(q)
+    LSE = np.zeros((B, H, N), dtype=dt)
+    mp, keep, sb, sh = _mask_args(mask, B, H, N, mask_block)
+    fn = _load().orc_fwd_blockwise_f64 if precision == "f64" else _load().orc_fwd_blockwise_f32
+    fn(B, H, N, d, _ptr(q), _ptr(k), _ptr(v), float(scale), int(bool(causal)), mp,
+       int(mask_block), sb, sh, int(Br), int(Bc), int(bool(norm_at_end)), _ptr(O), _ptr(LSE))
+    return O, LSE
+
+
+def attention_bwd(q, k, v, do, scale, causal=False, mask=None, mask_block=128):
+    """Gradients (dQ, dK, dV) of sum(dO * O) over whole [B,H,N,d] tensors, fp64."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, N, d = q.shape
+    dQ, dK, dV = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
+    mp, keep, sb, sh = _mask_args(mask, B, H, N, mask_block)
+    _load().orc_bwd(B, H, N, d, _ptr(q), _ptr(k), _ptr(v), _ptr(do), float(scale),
+                    int(bool(causal)), mp, int(mask_block), sb, sh,
+                    _ptr(dQ), _ptr(dK), _ptr(dV))
+    return dQ, dK, dV
+
+
+def attention_bwd_rows(qh, kh, vh, doh, qrows, krows, scale, causal=False, mask_h=None,
+                       mask_block=128):
+    """Gradients of selected rows of one head: dQ[qrows], dK[krows], dV[krows]."""
+    qh, kh, vh, doh = _f64(qh), _f64(kh), _f64(vh), _f64(doh)
+    N, d = qh.shape
+    qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32))
+    kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32))
+    dQ = np.zeros((len(qr), d))
+    dK = np.zeros((len(kr), d))
+    dV = np.zeros((len(kr), d))
+    m = None if mask_h is None else np.ascontiguousarray(np.asarray(mask_h, dtype=np.uint8))
+    _load().orc_bwd_rows(N, d, _ptr(qh), _ptr(kh), _ptr(vh), _ptr(doh), float(scale),
+                         int(bool(causal)), None if m is None else _ptr(m), int(mask_block),
+                         len(qr), _ptr(qr), _ptr(dQ), len(kr), _ptr(kr), _ptr(dK), _ptr(dV))
+    return dQ, dK, dV
+
+
+def head_mask(mask, b, h, N, mask_block=128):
+    """The [T,T] mask matrix that applies to head (b, h), or None."""
+    return _head_mask(mask, b, h, N, mask_block)
