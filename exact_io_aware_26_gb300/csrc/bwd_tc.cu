@@ -1,0 +1,410 @@
+// bwd_tc.cu -- attention backward main kernel on the 5th-generation tensor cores.
+//
+// The backward pass keeps only O and the per-row statistic from the forward
+// pass and recomputes the scores and probabilities tile by tile ("Passe
+// arrière : recalculer au lieu de stocker", marketmaker.cc; "Recomputação no
+// Backward Pass", FlashAttention reading guide).  One CTA owns one 128-key
+// tile (K_j, V_j) of one (batch, head), keeps it in shared memory, accumulates
+// dK_j and dV_j in TMEM, and walks the 128-query tiles i that the causal rule
+// and the block mask leave:
+//   S^T  = K_j Q_i^T                    (tcgen05, TMEM)
+//   P^T  = exp(scale * S^T - LSE_i)      (CUDA cores; thread = key row)
+//   dP^T = V_j dO_i^T                    (tcgen05, TMEM)
+//   dV  += P^T dO_i                      (tcgen05, P^T from shared memory)
+//   dS^T = P^T * (dP^T - D_i)            (CUDA cores)
+//   dK  += dS^T Q_i                      (tcgen05)
+//   dQ_i = dS K_j                        (tcgen05, read back and added to the
+//                                         fp32 accumulator with vector atomics)
+// The score scale is applied once at the end: dK = scale * sum dS^T Q here,
+// dQ = scale * accumulator in the finalize kernel.
+//
+// Warp roles (320 threads): warps 0-3 and 4-7 are two compute warpgroups that
+// split the 128 query columns of every tile (TMEM lane = key row); warp 8 is
+// the TMA producer (K_j, V_j once; Q_i, dO_i through a ring); warp 9 owns TMEM
+// and issues the MMAs.
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kTile = 128;
+
+template <int D>
+struct BwdLayout {
+  static constexpr uint32_t TILE = kTile * D * 2;
+  static constexpr int NS = (D == 64) ? 2 : 1;        // Q/dO ring depth
+  static constexpr uint32_t K = 0;
+  static constexpr uint32_t V = TILE;
+  static constexpr uint32_t QS = 2 * TILE;            // stage s: Q at QS + 2s TILE, dO after it
+  static constexpr uint32_t PT = QS + NS * 2 * TILE;  // P^T, 128 x 128 16-bit
+  static constexpr uint32_t DST = PT + kTile * kTile * 2;  // dS^T
+  static constexpr uint32_t STAT = DST + kTile * kTile * 2;  // [2][256] fp32: LSE*log2e, D
+  static constexpr uint32_t BAR = STAT + 2 * 256 * 4;
+  // barriers: 0 kv_full, 1 s_full, 2 s_free, 3 dp_full, 4 dp_free, 5 p_full, 6 p_free,
+  //           7 ds_full, 8 ds_free, 9 dq_full, 10 dq_free, 11 done, 12-13 stat[2],
+  //           14.. q_full[NS], 14+NS.. q_empty[NS]
+  static constexpr uint32_t NBAR = 14 + 2 * NS;
+  static constexpr uint32_t TSLOT = BAR + NBAR * 8;
+  static constexpr uint32_t ABORT = TSLOT + 4;
+  static constexpr uint32_t BYTES = ABORT + 4;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM columns
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  static constexpr bool ALIAS_DQ = (D == 128);  // dQ reuses the S^T columns
+  static constexpr uint32_t T_DQ = ALIAS_DQ ? T_S : 256 + 2 * D;
+};
+
+__device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
+  if (m.causal && kt > qt) return false;
+  if (m.mask) {
+    const long long at = (long long)b * m.mask_sb + (long long)h * m.mask_sh +
+                         (long long)((qt * kTile) / m.mask_block) * m.mask_cols +
+                         (kt * kTile) / m.mask_block;
+    return m.mask[at] != 0;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(320, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdArgs a) {
+  using L = BwdLayout<D>;
+  constexpr int NS = L::NS;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int BH = a.B * a.H;
+  const int n_tiles = (a.N + kTile - 1) / kTile;
+  const int kt = (int)(blockIdx.x / BH);  // causal: low key tiles see the most queries
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / a.H, h = bh % a.H;
+  const int qt_begin = a.m.causal ? kt : 0;
+
+  auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
+  const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_s_free = bar(2), bar_dp_full = bar(3),
+                 bar_dp_free = bar(4), bar_p_full = bar(5), bar_p_free = bar(6),
+                 bar_ds_full = bar(7), bar_ds_free = bar(8), bar_dq_full = bar(9),
+                 bar_dq_free = bar(10), bar_done = bar(11);
+  auto bar_stat = [&](int s) { return bar(12 + s); };
+  auto bar_qf = [&](int s) { return bar(14 + s); };
+  auto bar_qe = [&](int s) { return bar(14 + NS + s); };
+  volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
+  const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
+
+  if ((sb & 1023u) != 0) {
+    if (threadIdx.x == 0) raise_error(w, FA_ERR_CUDA);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_s_free, 8);
+    mbar_init(bar_dp_full, 1);
+    mbar_init(bar_dp_free, 8);
+    mbar_init(bar_p_full, 8);
+    mbar_init(bar_p_free, 1);
+    mbar_init(bar_ds_full, 8);
+    mbar_init(bar_ds_free, 1);
+    mbar_init(bar_dq_full, 1);
+    mbar_init(bar_dq_free, 8);
+    mbar_init(bar_done, 1);
+    mbar_init(bar_stat(0), 256);
+    mbar_init(bar_stat(1), 256);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_qf(s), 1);
+      mbar_init(bar_qe(s), 1);
+    }
+    *abort_cta = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmdO);
+      mbar_arrive_expect_tx(bar_kv, 2 * L::TILE);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sb + L::K + c * (kTile * 128), &tmK, bar_kv, c * 64, kt * kTile, bh);
+        tma_load_3d(sb + L::V + c * (kTile * 128), &tmV, bar_kv, c * 64, kt * kTile, bh);
+      }
+      int it = 0;
+      for (int qt = qt_begin; qt < n_tiles; ++qt) {
+        if (!tile_kept(a.m, b, h, qt, kt)) continue;
+        const int s = it % NS;
+        if (it >= NS && !mbar_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
+        const uint32_t dst = sb + L::QS + (uint32_t)s * 2u * L::TILE;
+        mbar_arrive_expect_tx(bar_qf(s), 2 * L::TILE);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(dst + c * (kTile * 128), &tmQ, bar_qf(s), c * 64, qt * kTile, bh);
+          tma_load_3d(dst + L::TILE + c * (kTile * 128), &tmdO, bar_qf(s), c * 64, qt * kTile, bh);
+        }
+        ++it;
+      }
+      mbar_drain(w, bar_kv, 0);
+      for (int s = 0; s < NS; ++s) {
+        const int n = (it - s + NS - 1) / NS;  // loads issued into stage s
+        if (n > 0) mbar_drain(w, bar_qf(s), (n - 1) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);  // K-major x K-major
+      constexpr uint32_t idKV = idesc_f16(F16, kTile, D, false, true);      // K-major x MN-major
+      constexpr uint32_t idQ = idesc_f16(F16, kTile, D, true, true);        // MN-major x MN-major
+      const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
+                     tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
+      bool ok = mbar_wait(w, bar_kv, 0);
+      int it = 0;
+      for (int qt = qt_begin; ok && qt < n_tiles; ++qt) {
+        if (!tile_kept(a.m, b, h, qt, kt)) continue;
+        const int s = it % NS;
+        const uint32_t sQ = sb + L::QS + (uint32_t)s * 2u * L::TILE, sdO = sQ + L::TILE;
+        if (!(ok = mbar_wait(w, bar_qf(s), (it / NS) & 1))) break;
+        if (it > 0) {
+          if (!(ok = mbar_wait(w, bar_s_free, (it - 1) & 1))) break;
+          if (L::ALIAS_DQ && !(ok = mbar_wait(w, bar_dq_free, (it - 1) & 1))) break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss(tS, desc_kmajor(sb + L::K, kk, kTile), desc_kmajor(sQ, kk, kTile), idS,
+                    kk > 0 ? 1u : 0u);
+        tc_commit(bar_s_full);
+        if (it > 0 && !(ok = mbar_wait(w, bar_dp_free, (it - 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss(tDP, desc_kmajor(sb + L::V, kk, kTile), desc_kmajor(sdO, kk, kTile), idS,
+                    kk > 0 ? 1u : 0u);
+        tc_commit(bar_dp_full);
+        // dV += P^T dO_i
+        if (!(ok = mbar_wait(w, bar_p_full, it & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma_ss(tDV, desc_kmajor(sb + L::PT, kk, kTile), desc_mnmajor(sdO, kk, kTile), idKV,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar_p_free);
+        // dK += dS^T Q_i ; dQ_i = dS K_j
+        if (!(ok = mbar_wait(w, bar_ds_full, it & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma_ss(tDK, desc_kmajor(sb + L::DST, kk, kTile), desc_mnmajor(sQ, kk, kTile), idKV,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        if (!L::ALIAS_DQ && it > 0 && !(ok = mbar_wait(w, bar_dq_free, (it - 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma_ss(tDQ, desc_mnmajor(sb + L::DST, kk, kTile), desc_mnmajor(sb + L::K, kk, kTile),
+                    idQ, kk > 0 ? 1u : 0u);
+        tc_commit(bar_ds_free);
+        tc_commit(bar_dq_full);
+        tc_commit(bar_qe(s));
+        ++it;
+      }
+      tc_commit(bar_done);
+      mbar_drain(w, bar_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warpgroups
+    const int g = warp >> 2;                 // 0: query columns 0-63, 1: 64-127
+    const int r = (warp & 3) * 32 + lane;    // key row in the tile = TMEM lane
+    const int key = kt * kTile + r;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float c2 = a.scale_log2;
+    const float* stat = reinterpret_cast<const float*>(smem + L::STAT);
+    float* stat_w = reinterpret_cast<float*>(smem + L::STAT);
+    const int t = threadIdx.x;  // 0..255
+    bool ok = true;
+    int it = 0;
+    for (int qt = qt_begin; qt < n_tiles; ++qt) {
+      if (!tile_kept(a.m, b, h, qt, kt)) continue;
+      // row statistics of the query tile: LSE in log2 units (+inf hides the row:
+      // past the end, or a row that saw no key) and D
+      {
+        const int q = qt * kTile + (t & 127);
+        float v;
+        if (t < 128) {
+          const float lse = q < a.N ? a.LSE[(size_t)bh * a.N + q] : -INFINITY;
+          v = (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
+        } else {
+          v = q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
+        }
+        stat_w[(it & 1) * 256 + t] = v;
+        mbar_arrive(bar_stat(it & 1));
+        // buffer it&1 was last read in iteration it-2, which every thread
+        // finished before arriving for iteration it-1
+        if (!(ok = warp_wait(w, bar_stat(it & 1), (it >> 1) & 1))) break;
+      }
+      const float* lse2 = stat + (it & 1) * 256 + 64 * g;
+      const float* Dq = stat + (it & 1) * 256 + 128 + 64 * g;
+
+      if (!(ok = warp_wait(w, bar_s_full, it & 1))) break;
+      tc_fence_after();
+      float p[64];
+      {
+        uint32_t u[64];
+        tmem_ld64(tmem + L::T_S + lane_off + 64 * g, u);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(u[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_s_free);
+      const int q0 = qt * kTile + 64 * g;
+      const bool row_out = key >= a.N;
+      const bool diag = a.m.causal && qt == kt;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float pv = ex2(fmaf(p[c], c2, -lse2[c]));
+        if (row_out || (diag && q0 + c < key)) pv = 0.f;
+        p[c] = pv;
+      }
+      if (it > 0 && !(ok = warp_wait(w, bar_p_free, (it - 1) & 1))) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        st_shared_v4(sb + L::PT + sw128_chunk_offset(r, 8 * g + ch, kTile),
+                     pack2<F16>(p[ch * 8 + 0], p[ch * 8 + 1]), pack2<F16>(p[ch * 8 + 2], p[ch * 8 + 3]),
+                     pack2<F16>(p[ch * 8 + 4], p[ch * 8 + 5]), pack2<F16>(p[ch * 8 + 6], p[ch * 8 + 7]));
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_full);
+
+      if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
+      tc_fence_after();
+      float ds[64];
+      {
+        uint32_t u[64];
+        tmem_ld64(tmem + L::T_DP + lane_off + 64 * g, u);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) ds[c] = __uint_as_float(u[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dp_free);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) ds[c] = p[c] * (ds[c] - Dq[c]);
+      if (it > 0 && !(ok = warp_wait(w, bar_ds_free, (it - 1) & 1))) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        st_shared_v4(sb + L::DST + sw128_chunk_offset(r, 8 * g + ch, kTile),
+                     pack2<F16>(ds[ch * 8 + 0], ds[ch * 8 + 1]), pack2<F16>(ds[ch * 8 + 2], ds[ch * 8 + 3]),
+                     pack2<F16>(ds[ch * 8 + 4], ds[ch * 8 + 5]), pack2<F16>(ds[ch * 8 + 6], ds[ch * 8 + 7]));
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds_full);
+
+      // dQ_i (TMEM lane = query row) -> fp32 accumulator
+      if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
+      tc_fence_after();
+      {
+        const int qrow = qt * kTile + r;
+        float* dst = a.dQacc + ((size_t)bh * a.N + qrow) * D + g * (D / 2);
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t u[32];
+          tmem_ld32(tmem + L::T_DQ + lane_off + g * (D / 2) + c0, u);
+          if (qrow < a.N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              red_add_v4(dst + c0 + 4 * v, __uint_as_float(u[4 * v]), __uint_as_float(u[4 * v + 1]),
+                         __uint_as_float(u[4 * v + 2]), __uint_as_float(u[4 * v + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_free);
+      ++it;
+    }
+    // ------------------------------------------------------------ dK, dV epilogue
+    bool have = false;
+    if (ok) {
+      ok = warp_wait(w, bar_done, 0);
+      tc_fence_after();
+      have = ok && it > 0;
+    }
+    if (ok && key < a.N) {
+      typedef uint16_t elem_t;
+      elem_t* dVrow = reinterpret_cast<elem_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * (D / 2);
+      elem_t* dKrow = reinterpret_cast<elem_t*>(a.dK) + ((size_t)bh * a.N + key) * D + g * (D / 2);
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = (which == 0 ? L::T_DV : L::T_DK) + g * (D / 2);
+        const float mul = which == 0 ? 1.f : a.scale;
+        elem_t* dst = which == 0 ? dVrow : dKrow;
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t u[32];
+          if (have) {
+            tmem_ld32(tmem + col + lane_off + c0, u);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = 0u;
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 pk;
+            pk.x = pack2<F16>(__uint_as_float(u[v * 8 + 0]) * mul, __uint_as_float(u[v * 8 + 1]) * mul);
+            pk.y = pack2<F16>(__uint_as_float(u[v * 8 + 2]) * mul, __uint_as_float(u[v * 8 + 3]) * mul);
+            pk.z = pack2<F16>(__uint_as_float(u[v * 8 + 4]) * mul, __uint_as_float(u[v * 8 + 5]) * mul);
+            pk.w = pack2<F16>(__uint_as_float(u[v * 8 + 6]) * mul, __uint_as_float(u[v * 8 + 7]) * mul);
+            *reinterpret_cast<uint4*>(dst + c0 + v * 8) = pk;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int D, bool F16>
+cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
+  using L = BwdLayout<D>;
+  auto kern = bwd_tc_kernel<D, F16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (a.N + kTile - 1) / kTile;
+  kern<<<(unsigned)(n_tiles * a.B * a.H), 320, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* tm, cudaStream_t s) {
+  if (d == 64) return f16 ? launch_t<64, true>(a, tm, s) : launch_t<64, false>(a, tm, s);
+  return f16 ? launch_t<128, true>(a, tm, s) : launch_t<128, false>(a, tm, s);
+}
+
+}  // namespace fa

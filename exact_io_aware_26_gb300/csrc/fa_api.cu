@@ -1,0 +1,406 @@
+// fa_api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument
+// validation, TMA tensor-map encoding, the device status word, and the kernel
+// launches.  Everything here is host code except the status word.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+using namespace fa;
+
+namespace {
+
+__device__ DevStatus g_status;  // per device: first error code + abort epoch
+
+thread_local char g_err[512] = "";
+
+void set_err(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+  set_err("%s: %s", what, cudaGetErrorString(e));
+  return FA_ERR_CUDA;
+}
+
+std::atomic<uint32_t> g_epoch{0};
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+
+constexpr int kMaxDev = 64;
+struct DevState {
+  bool checked = false;
+  bool supported = false;
+  DevStatus* st = nullptr;
+};
+DevState g_dev[kMaxDev];
+std::mutex g_mu;
+
+// The current device must be sm_103; resolves the status word's address once.
+fa_status device_ready(DevStatus** st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDev) {
+    set_err("device ordinal %d out of range", dev);
+    return FA_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_status)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(status)");
+      d.st = static_cast<DevStatus*>(p);
+    }
+    d.checked = true;
+    if (!d.supported) {
+      set_err("device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
+    }
+  }
+  if (!d.supported) return FA_ERR_DEVICE;
+  *st = d.st;
+  return FA_OK;
+}
+
+Report make_report(DevStatus* st) {
+  Report r;
+  r.st = st;
+  r.epoch = g_epoch.fetch_add(1) + 1;
+  r.wait_ns = g_wait_ns.load();
+  return r;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- TMA maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A [B*H][N][d] 16-bit tensor as a 3-D TMA map {d, N, B*H}; box {64, 128, 1},
+// 128-byte swizzle; rows past N read as zero.
+fa_status encode_bhnd(CUtensorMap* m, const void* ptr, const fa_params* p) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_err("cuTensorMapEncodeTiled is not available from the driver");
+    return FA_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)p->d, (cuuint64_t)p->N, (cuuint64_t)p->B * p->H};
+  const cuuint64_t strides[2] = {(cuuint64_t)p->d * 2, (cuuint64_t)p->N * p->d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      p->dtype == FA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_err("cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+MaskArgs mask_args(const fa_params* p) {
+  MaskArgs m;
+  m.causal = p->causal ? 1 : 0;
+  m.mask = p->block_mask;
+  m.mask_block = p->block_mask ? p->mask_block : 128;
+  m.mask_cols = (p->N + m.mask_block - 1) / m.mask_block;
+  m.mask_sb = p->mask_stride_b;
+  m.mask_sh = p->mask_stride_h;
+  return m;
+}
+
+BwdArgs bwd_args(const fa_params* p, void* ws) {
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = p->B;
+  a.H = p->H;
+  a.N = p->N;
+  a.scale = p->scale;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.m = mask_args(p);
+  const size_t rows = (size_t)p->B * p->H * p->N;
+  a.Dsum = static_cast<float*>(ws);
+  a.dQacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * 4));
+  return a;
+}
+
+fa_status check_ws(const fa_params* p, const void* ws, size_t bytes) {
+  const size_t need = fa_bwd_workspace_size(p);
+  if (!ws || bytes < need || !aligned(ws, 256)) {
+    set_err("workspace %p of %zu bytes; need %zu bytes, 256-byte aligned", ws, bytes, need);
+    return FA_ERR_WORKSPACE;
+  }
+  return FA_OK;
+}
+
+fa_status need16(const void* ptr, const char* name) {
+  if (!ptr) {
+    set_err("%s is NULL", name);
+    return FA_ERR_INVALID;
+  }
+  if (!aligned(ptr, 16)) {
+    set_err("%s is not 16-byte aligned", name);
+    return FA_ERR_INVALID;
+  }
+  return FA_OK;
+}
+
+#define FA_TRY(x)                    \
+  do {                               \
+    fa_status _s = (x);              \
+    if (_s != FA_OK) return _s;      \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_last_error(void) { return g_err; }
+
+const char* fa_status_string(int s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_DEVICE: return "device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+fa_status fa_check(const fa_params* p, int for_backward) {
+  if (!p) {
+    set_err("params is NULL");
+    return FA_ERR_INVALID;
+  }
+  if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) {
+    set_err("B, H, N, d must be >= 1 (got %d, %d, %d, %d)", p->B, p->H, p->N, p->d);
+    return FA_ERR_INVALID;
+  }
+  if (p->dtype != FA_F32 && p->dtype != FA_F16 && p->dtype != FA_BF16) {
+    set_err("dtype %d is not an fa_dtype", p->dtype);
+    return FA_ERR_INVALID;
+  }
+  if (!(std::isfinite(p->scale) && p->scale > 0.f)) {
+    set_err("scale must be positive and finite");
+    return FA_ERR_INVALID;
+  }
+  if (p->d != 64 && p->d != 128) {
+    set_err("head size %d is not supported (64 or 128)", p->d);
+    return FA_ERR_UNSUPPORTED;
+  }
+  const long long elems = (long long)p->B * p->H * p->N * p->d;
+  if (elems >= (1ll << 31)) {
+    set_err("B*H*N*d = %lld exceeds 2^31 - 1", elems);
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (p->block_mask) {
+    if (p->mask_block <= 0 || p->mask_stride_b < 0 || p->mask_stride_h < 0) {
+      set_err("mask_block must be positive and mask strides non-negative");
+      return FA_ERR_INVALID;
+    }
+    if (p->mask_block % 128 != 0) {
+      set_err("mask_block %d is not a multiple of the 128-token tile", p->mask_block);
+      return FA_ERR_UNSUPPORTED;
+    }
+  }
+  if (for_backward && p->dtype == FA_F32) {
+    set_err("the backward pass takes fp16 or bf16 tensors");
+    return FA_ERR_UNSUPPORTED;
+  }
+  return FA_OK;
+}
+
+unsigned long long fa_set_wait_limit_ns(unsigned long long ns) {
+  if (ns == 0) ns = 1;
+  return g_wait_ns.exchange(ns);
+}
+
+fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
+                 float* LSE, void* stream) {
+  FA_TRY(fa_check(p, 0));
+  FA_TRY(need16(Q, "Q"));
+  FA_TRY(need16(K, "K"));
+  FA_TRY(need16(V, "V"));
+  FA_TRY(need16(O, "O"));
+  if (!LSE || !aligned(LSE, 4)) {
+    set_err("LSE is NULL or misaligned");
+    return FA_ERR_INVALID;
+  }
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = p->B;
+  a.H = p->H;
+  a.N = p->N;
+  a.scale = p->scale;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.m = mask_args(p);
+  a.O = O;
+  a.LSE = LSE;
+  a.rep = make_report(st);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (p->dtype == FA_F32) {
+    e = launch_fwd_f32(a, p->d, static_cast<const float*>(Q), static_cast<const float*>(K),
+                       static_cast<const float*>(V), s);
+  } else {
+    CUtensorMap tm[3];
+    FA_TRY(encode_bhnd(&tm[0], Q, p));
+    FA_TRY(encode_bhnd(&tm[1], K, p));
+    FA_TRY(encode_bhnd(&tm[2], V, p));
+    e = launch_fwd_tc(a, p->d, p->dtype == FA_F16, tm, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(const fa_params* p) {
+  if (fa_check(p, 0) != FA_OK) return 0;
+  const size_t rows = (size_t)p->B * p->H * p->N;
+  return align256(rows * 4) + align256(rows * (size_t)p->d * 4);
+}
+
+fa_status fa_bwd_preprocess(const fa_params* p, const void* O, const void* dO, void* ws,
+                            size_t ws_bytes, void* stream) {
+  FA_TRY(fa_check(p, 1));
+  FA_TRY(need16(O, "O"));
+  FA_TRY(need16(dO, "dO"));
+  FA_TRY(check_ws(p, ws, ws_bytes));
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  BwdArgs a = bwd_args(p, ws);
+  a.O = O;
+  a.dO = dO;
+  a.rep = make_report(st);
+  cudaError_t e = launch_bwd_preprocess(a, p->d, p->dtype == FA_F16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  return FA_OK;
+}
+
+fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const void* V,
+                      const void* dO, const float* LSE, void* dK, void* dV, void* ws,
+                      size_t ws_bytes, void* stream) {
+  FA_TRY(fa_check(p, 1));
+  FA_TRY(need16(Q, "Q"));
+  FA_TRY(need16(K, "K"));
+  FA_TRY(need16(V, "V"));
+  FA_TRY(need16(dO, "dO"));
+  FA_TRY(need16(dK, "dK"));
+  FA_TRY(need16(dV, "dV"));
+  if (!LSE || !aligned(LSE, 4)) {
+    set_err("LSE is NULL or misaligned");
+    return FA_ERR_INVALID;
+  }
+  FA_TRY(check_ws(p, ws, ws_bytes));
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  BwdArgs a = bwd_args(p, ws);
+  a.dO = dO;
+  a.LSE = LSE;
+  a.dK = dK;
+  a.dV = dV;
+  a.rep = make_report(st);
+  CUtensorMap tm[4];
+  FA_TRY(encode_bhnd(&tm[0], Q, p));
+  FA_TRY(encode_bhnd(&tm[1], K, p));
+  FA_TRY(encode_bhnd(&tm[2], V, p));
+  FA_TRY(encode_bhnd(&tm[3], dO, p));
+  cudaError_t e = launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) {
+    set_err("backward main kernel not available in this build");
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "backward main launch");
+  return FA_OK;
+}
+
+fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* ws, size_t ws_bytes, void* stream) {
+  FA_TRY(fa_check(p, 1));
+  FA_TRY(need16(dQ, "dQ"));
+  FA_TRY(check_ws(p, ws, ws_bytes));
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  BwdArgs a = bwd_args(p, ws);
+  a.dQ = dQ;
+  a.rep = make_report(st);
+  cudaError_t e = launch_bwd_finalize(a, p->d, p->dtype == FA_F16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward finalize launch");
+  return FA_OK;
+}
+
+fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V, const void* O,
+                 const void* dO, const float* LSE, void* dQ, void* dK, void* dV, void* ws,
+                 size_t ws_bytes, void* stream) {
+  FA_TRY(fa_check(p, 1));
+  FA_TRY(need16(dQ, "dQ"));
+  FA_TRY(fa_bwd_preprocess(p, O, dO, ws, ws_bytes, stream));
+  FA_TRY(fa_bwd_main(p, Q, K, V, dO, LSE, dK, dV, ws, ws_bytes, stream));
+  return fa_bwd_finalize(p, dQ, ws, ws_bytes, stream);
+}
+
+fa_status fa_get_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  int code = 0;
+  if ((e = cudaMemcpy(&code, &st->code, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "reading the status word");
+  if (code != 0) {
+    if ((e = cudaMemset(&st->code, 0, sizeof(int))) != cudaSuccess)
+      return cuda_fail(e, "clearing the status word");
+    set_err("device reported: %s", fa_status_string(code));
+  }
+  return static_cast<fa_status>(code);
+}
+
+fa_status fa_selftest_timeout(void* stream) {
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  cudaError_t e = launch_wait_selftest(make_report(st), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// internal.h -- declarations shared by the C-ABI front end (fa_api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Library status word in device memory (one per device).  `code` is the first
+// device-side error since the last fa_get_status(); `abort_epoch` is the
+// highest launch epoch in which some CTA gave up, so that the other CTAs of
+// the same launch stop waiting too.
+struct DevStatus {
+  int code;
+  unsigned int abort_epoch;
+};
+
+// Where a launch reports to and how long its waits may last.
+struct Report {
+  DevStatus* st;
+  uint32_t epoch;
+  uint64_t wait_ns;
+};
+
+// Which (query tile, key tile) pairs are visited: causal skips tiles whose
+// keys all lie after their queries, and the block mask skips hidden tiles.
+struct MaskArgs {
+  int causal;
+  const uint8_t* mask;  // device, or nullptr
+  int mask_block;       // tokens per mask entry (a multiple of the kernel tile)
+  int mask_cols;        // ceil(N / mask_block)
+  long long mask_sb, mask_sh;
+};
+
+struct FwdArgs {
+  int B, H, N;
+  float scale;       // natural-units score scale
+  float scale_log2;  // scale * log2(e)
+  MaskArgs m;
+  void* O;
+  float* LSE;
+  Report rep;
+};
+
+struct BwdArgs {
+  int B, H, N;
+  float scale;
+  float scale_log2;
+  MaskArgs m;
+  const void* O;
+  const void* dO;
+  const float* LSE;
+  void* dK;
+  void* dV;
+  void* dQ;
+  float* Dsum;   // [B*H*N]  rowsum(dO * O)
+  float* dQacc;  // [B*H*N*d] fp32 accumulator of dQ / scale
+  Report rep;
+};
+
+// Kernel launchers (one per translation unit).
+cudaError_t launch_fwd_f32(const FwdArgs& a, int d, const float* Q, const float* K,
+                           const float* V, cudaStream_t s);
+cudaError_t launch_fwd_tc(const FwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
+                          cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_t s);
+cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
+                          cudaStream_t s);
+cudaError_t launch_bwd_finalize(const BwdArgs& a, int d, bool f16, cudaStream_t s);
+cudaError_t launch_wait_selftest(const Report& rep, cudaStream_t s);
+
+}  // namespace fa

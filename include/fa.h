@@ -1,0 +1,159 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact tiled scaled-dot-product attention on one
+ * GB300 GPU (sm_103a), forward and backward.
+ *
+ * The operation is O = softmax(scale * Q K^T) V for every batch b and head h,
+ * as stated in "Pourquoi l'attention est liée à la mémoire" (marketmaker.cc,
+ * "Un contexte d'une journée complète bat-il un contexte de dix minutes ?")
+ * and in "Problema e motivação" of the FlashAttention reading guide
+ * (xyznot.com, arXiv 2205.14135).  The score matrix is never written to
+ * device memory: the forward pass streams key/value tiles through on-chip
+ * memory with the running-max / running-sum recurrence ("La récurrence
+ * softmax en ligne"; "Rastreamento Incremental do Softmax"), and the backward
+ * pass recomputes the scores and probabilities tile by tile from Q, K, V and
+ * the saved per-row statistic ("Passe arrière : recalculer au lieu de
+ * stocker").
+ *
+ * Conventions shared by every call:
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are device buffers of shape
+ *     [B][H][N][d], contiguous, in the element type `dtype`; their base
+ *     addresses must be 16-byte aligned.  LSE is a device fp32 buffer [B][H][N].
+ *   - The caller owns every buffer.  The library allocates no device memory of
+ *     its own apart from one small status word per device.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, or NULL for the
+ *     legacy default stream).  Argument errors are returned before anything is
+ *     launched; a failed launch returns FA_ERR_CUDA; a kernel that gives up
+ *     waiting on an on-chip barrier records FA_ERR_TIMEOUT in the status word,
+ *     which fa_get_status() returns.
+ *   - Only the current CUDA device is used; it must be compute capability 10.3.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = -1,     /* null pointer, size out of range, misaligned buffer, bad scale */
+  FA_ERR_UNSUPPORTED = -2, /* well-formed request this library does not implement */
+  FA_ERR_CUDA = -3,        /* a CUDA runtime or driver call failed */
+  FA_ERR_TIMEOUT = -4,     /* a kernel gave up waiting on a barrier (via fa_get_status) */
+  FA_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required */
+  FA_ERR_DEVICE = -6       /* the current device is not compute capability 10.3 */
+} fa_status;
+
+typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+/*
+ * Problem description.
+ *   B, H, N, d  batch, heads, sequence length (queries = keys), head size.
+ *               N >= 1 (any value: tails that are not a multiple of the tile
+ *               are masked); d in {64, 128}; B*H*N*d < 2^31.
+ *   dtype       element type of Q, K, V, O, dO, dQ, dK, dV (fa_dtype).
+ *               FA_F32 runs the fp32 forward only.
+ *   scale       positive finite factor applied to Q K^T before the softmax
+ *               (1/sqrt(d) for standard attention).
+ *   causal      nonzero: query i only sees keys j <= i ("Le masquage causal
+ *               est l'endroit où le trading bénéficie d'une remise").
+ *   block_mask  device uint8 matrix or NULL ("Extensão: Block-Sparse
+ *               FlashAttention"): entry [i / mask_block][j / mask_block]
+ *               keeps (nonzero) or hides (0) the pair (query i, key j).  Each
+ *               (b, h) uses the T x T row-major matrix at
+ *               block_mask + b * mask_stride_b + h * mask_stride_h, with
+ *               T = ceil(N / mask_block); strides in elements, 0 broadcasts.
+ *               Combined with `causal` by AND.  Hidden tiles are never loaded.
+ *   mask_block  tokens per mask entry; a positive multiple of 128 when
+ *               block_mask is set (ignored otherwise).
+ * A query row whose allowed key set is empty gets O = 0 and LSE = -inf, and
+ * contributes nothing to the gradients.
+ */
+typedef struct {
+  int B, H, N, d;
+  int dtype;
+  float scale;
+  int causal;
+  const uint8_t* block_mask;
+  int mask_block;
+  long long mask_stride_b, mask_stride_h;
+} fa_params;
+
+/* Host-only validation of `p` (no CUDA call).  for_backward selects the
+ * backward's extra limits.  Returns FA_OK, FA_ERR_INVALID or
+ * FA_ERR_UNSUPPORTED. */
+fa_status fa_check(const fa_params* p, int for_backward);
+
+/*
+ * Forward: O = softmax(scale * Q K^T [masked]) V and
+ * LSE[b,h,i] = m_i + ln(l_i), the natural-log log-sum-exp of row i of the
+ * scaled, masked scores (the running max m and running sum l of "L'algorithme
+ * Flash Attention", folded into one number).  O is written in `dtype`; LSE in
+ * fp32.  fp16/bf16 run on the tensor cores (tcgen05, fp32 accumulation);
+ * fp32 runs a SIMT kernel in fp32 arithmetic.
+ */
+fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
+                 float* LSE, void* stream);
+
+/* Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * O) [B*H*N] and
+ * the fp32 dQ accumulator [B*H*N*d], each 256-byte aligned.  0 on invalid p. */
+size_t fa_bwd_workspace_size(const fa_params* p);
+
+/*
+ * Backward of the forward above for the loss whose gradient at O is dO:
+ *   P = exp(scale * S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+ *   dS = P * (dP - D), dQ = scale * dS K, dK = scale * dS^T Q.
+ * Q, K, V, O, LSE must be those of the forward call (same params).  dQ, dK, dV
+ * are written in `dtype`.  `workspace` is a device buffer of at least
+ * fa_bwd_workspace_size(p) bytes, 256-byte aligned, owned by the caller; its
+ * contents on entry do not matter.  fp16/bf16 only (FA_F32 -> UNSUPPORTED).
+ * Runs fa_bwd_preprocess, fa_bwd_main and fa_bwd_finalize in that order.
+ */
+fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V, const void* O,
+                 const void* dO, const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* The three stages of fa_bwd, exported so that each can be timed on its own.
+ * preprocess: D = rowsum(dO * O) into the workspace, dQ accumulator zeroed.
+ * main: recompute P tile by tile, accumulate dK, dV per key tile (written to
+ *       dK, dV) and add scale-free dQ contributions into the accumulator.
+ * finalize: dQ = scale * accumulator, converted to `dtype`. */
+fa_status fa_bwd_preprocess(const fa_params* p, const void* O, const void* dO, void* workspace,
+                            size_t workspace_bytes, void* stream);
+fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const void* V,
+                      const void* dO, const float* LSE, void* dK, void* dV, void* workspace,
+                      size_t workspace_bytes, void* stream);
+fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Synchronises `stream`, returns the device-side status recorded since the
+ * previous call (FA_OK or FA_ERR_TIMEOUT) and clears it; FA_ERR_CUDA if the
+ * synchronisation itself fails. */
+fa_status fa_get_status(void* stream);
+
+/* Upper bound, in nanoseconds, on any single barrier wait inside the kernels
+ * launched after this call (default 2e9).  Returns the previous value. */
+unsigned long long fa_set_wait_limit_ns(unsigned long long ns);
+
+/* Launches one CTA that waits on a barrier nothing will complete, so that the
+ * wait limit runs out and FA_ERR_TIMEOUT is recorded; used to test the
+ * failure path without faulting the GPU.  Returns the launch status. */
+fa_status fa_selftest_timeout(void* stream);
+
+/* Static description of a status code. */
+const char* fa_status_string(int status);
+
+/* Text of the last CUDA or validation failure seen by this thread. */
+const char* fa_last_error(void);
+
+/* Library interface version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,100 @@
+"""Host-only checks of libfa.so: it builds, loads without a GPU, exports every
+function include/fa.h declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+
+import pytest
+
+import exact_io_aware_26_gb300 as fa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.load()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = fa.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.fa_status_string(code)
+
+
+def _p(**kw):
+    base = dict(B=1, H=1, N=128, d=64, dtype=fa.FA_BF16, scale=0.125, causal=0,
+                block_mask=None, mask_block=128, mask_stride_b=0, mask_stride_h=0)
+    base.update(kw)
+    return fa.FaParams(**base)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({}, fa.FA_OK),
+    ({"dtype": fa.FA_F32}, fa.FA_OK),
+    ({"N": 1}, fa.FA_OK),
+    ({"N": 23400, "H": 12}, fa.FA_OK),
+    ({"d": 128}, fa.FA_OK),
+    ({"B": 0}, fa.FA_ERR_INVALID),
+    ({"N": 0}, fa.FA_ERR_INVALID),
+    ({"d": 32}, fa.FA_ERR_UNSUPPORTED),
+    ({"d": 96}, fa.FA_ERR_UNSUPPORTED),
+    ({"dtype": 7}, fa.FA_ERR_INVALID),
+    ({"scale": 0.0}, fa.FA_ERR_INVALID),
+    ({"scale": -1.0}, fa.FA_ERR_INVALID),
+    ({"scale": float("inf")}, fa.FA_ERR_INVALID),
+    ({"scale": float("nan")}, fa.FA_ERR_INVALID),
+    ({"B": 64, "H": 64, "N": 65536}, fa.FA_ERR_UNSUPPORTED),
+    ({"block_mask": 4096, "mask_block": 64}, fa.FA_ERR_UNSUPPORTED),
+    ({"block_mask": 4096, "mask_block": 0}, fa.FA_ERR_INVALID),
+    ({"block_mask": 4096, "mask_block": 256}, fa.FA_OK),
+    ({"block_mask": 4096, "mask_stride_h": -1}, fa.FA_ERR_INVALID),
+])
+def test_check_params(lib, kw, expect):
+    assert fa.check_params(_p(**kw)) == expect
+
+
+def test_backward_limits(lib):
+    assert fa.check_params(_p(dtype=fa.FA_F32), for_backward=True) == fa.FA_ERR_UNSUPPORTED
+    assert fa.check_params(_p(dtype=fa.FA_F16), for_backward=True) == fa.FA_OK
+    assert lib.fa_check(None, 0) == fa.FA_ERR_INVALID
+
+
+def test_workspace_size(lib):
+    p = _p(B=4, H=12, N=2048, d=64)
+    rows = 4 * 12 * 2048
+    up = lambda x: (x + 255) // 256 * 256
+    assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4)
+    p = _p(N=23400, H=12, d=64)
+    rows = 12 * 23400
+    assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4)
+    assert lib.fa_bwd_workspace_size(ctypes.byref(_p(d=32))) == 0
+
+
+def test_invalid_calls_return_before_any_launch(lib):
+    """Null or misaligned pointers and a short workspace fail on the host."""
+    p = _p()
+    ok_ptr = 1 << 20  # never dereferenced: every call below fails validation first
+    assert lib.fa_fwd(ctypes.byref(p), None, ok_ptr, ok_ptr, ok_ptr, ok_ptr, None) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd(ctypes.byref(p), ok_ptr + 2, ok_ptr, ok_ptr, ok_ptr, ok_ptr, None) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd(ctypes.byref(p), ok_ptr, ok_ptr, ok_ptr, ok_ptr, None, None) == fa.FA_ERR_INVALID
+    assert lib.fa_fwd(ctypes.byref(_p(d=32)), ok_ptr, ok_ptr, ok_ptr, ok_ptr, ok_ptr, None) == fa.FA_ERR_UNSUPPORTED
+    need = lib.fa_bwd_workspace_size(ctypes.byref(p))
+    args = [ok_ptr] * 9
+    assert lib.fa_bwd(ctypes.byref(p), *args, ok_ptr, need - 1, None) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd(ctypes.byref(p), *args, None, need, None) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd(ctypes.byref(p), *args, ok_ptr + 16, need, None) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd(ctypes.byref(_p(dtype=fa.FA_F32)), *args, ok_ptr, need, None) == fa.FA_ERR_UNSUPPORTED
+    assert b"workspace" in lib.fa_last_error() or b"fp16" in lib.fa_last_error()
+
+
+def test_library_links_no_cuda_driver_at_load_time():
+    """libfa.so must load on a machine without the driver: no libcuda dependency."""
+    import subprocess
+    out = subprocess.run(["ldd", fa.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
