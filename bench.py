@@ -1,0 +1,427 @@
+"""Benchmark of exact tiled attention (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole path over one batch of the workload: for every
+causal setting the workload runs, fa_fwd then the three fa_bwd stages
+(preprocess, main, finalize), all through the C ABI of libfa.so.  Inputs are
+resident in device memory; L2 is flushed (a 256 MiB write) between steps,
+outside the timed events.  Each step is bracketed by CUDA events on the
+launching stream, and so is every launch of the dominant kernel (the backward
+main kernel), which gives the roofline figure.  FLOPs follow the usual
+convention: forward 4 B H N^2 d, backward 2.5 x forward, halved for causal,
+scaled by the kept-tile fraction for a block mask.
+
+`e2e` is the same metric measured end to end: per step the inputs are copied
+from pinned host memory, the path runs, and every output is copied back to
+pinned host memory, all inside the timed events.
+
+`cpu_baseline` times the fp64 CPU oracle on the host cores on a bounded sample
+of the same workload (a subset of heads), scaled to the same unit.
+
+With --impl reference the oracle itself is the timed arm (each step one bounded
+sample of the workload on the host cores).
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own copy of the
+workload (independent batches: weak scaling, no collective on the data path);
+the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("attention fwd/bwd TFLOP/s at N=2k–23.4k, d=64/128; "
+          "% of GB300 BF16 tensor peak")
+DEFAULT_WORKLOAD = "bf16_b4h12_n2048"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def kept_fraction(mask, causal: bool) -> float:
+    """Visited (query, key) pairs relative to N^2 under the FLOP convention."""
+    if mask is None:
+        return 0.5 if causal else 1.0
+    import numpy as np
+    m = np.asarray(mask, dtype=bool)
+    if causal:
+        m = np.tril(m)
+    return float(m.mean())
+
+
+def workload_flops(w, mask) -> dict:
+    dense = 4.0 * w.B * w.H * w.N * w.N * w.d
+    out = {}
+    for c in w.causal:
+        f = dense * kept_fraction(mask, c)
+        out[c] = {"fwd": f, "bwd": 2.5 * f}
+    return out
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms in the background."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == 0:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        inside = [s for (t, s) in self.samples if self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        if not inside:
+            inside = [s for (_, s) in self.samples]
+        sm, mx, power, reasons = [], [], [], set()
+        for s in inside:
+            f = [x.strip() for x in s.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(self.NAMES, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def oracle_sample(w, inp, heads: int):
+    """fp64 oracle forward + backward on the first `heads` heads; returns (flops, s, threads)."""
+    import oracle
+    B, H = w.B, w.H
+    sel = [(b, h) for b in range(B) for h in range(H)][:heads]
+    x = {n: inp[n].double().numpy() for n in ("q", "k", "v", "do")}
+    flops = workload_flops(w, inp["mask"])
+    total = 0.0
+    t = time.perf_counter()
+    for (b, h) in sel:
+        sl = lambda n: x[n][b:b + 1, h:h + 1]
+        mh = oracle.head_mask(inp["mask"], b, h, w.N, w.mask_block)
+        for c in w.causal:
+            oracle.attention_fwd(sl("q"), sl("k"), sl("v"), w.scale, causal=c, mask=mh,
+                                 mask_block=w.mask_block)
+            oracle.attention_bwd(sl("q"), sl("k"), sl("v"), sl("do"), w.scale, causal=c, mask=mh,
+                                 mask_block=w.mask_block)
+            total += (flops[c]["fwd"] + flops[c]["bwd"]) / (B * H)
+    return total, time.perf_counter() - t, oracle.num_threads()
+
+
+def heads_for_seconds(w, target_s: float) -> int:
+    """Heads that keep the oracle near target_s (it runs at roughly 1 GFLOP/s per core
+    on this convention's FLOPs)."""
+    cores = os.cpu_count() or 8
+    f = workload_flops(w, None)
+    per_head = sum(v["fwd"] + v["bwd"] for v in f.values()) / (w.B * w.H)
+    n = int(target_s * cores * 1.0e9 / max(per_head, 1.0))
+    return max(1, min(n, w.B * w.H))
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+            "causal": list(w.causal), "block_mask_p": w.mask_p,
+            "passes": "fwd+bwd per causal setting",
+            "l2": "flushed between steps (256 MiB write outside the timed events)"}
+
+
+def run_reference(args, w, rank):
+    import synth
+    if rank != 0:
+        return
+    inp = synth.workload_inputs(w)
+    # the whole reference run stays within a few minutes whatever K is
+    heads = heads_for_seconds(w, min(1.5, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, max(1, heads // 4))
+    tot_f, tot_s, cores = 0.0, 0.0, 1
+    for _ in range(args.steps):
+        f, s, cores = oracle_sample(w, inp, heads)
+        tot_f += f
+        tot_s += s
+    value = tot_f / tot_s / 1e12
+    sample = (f"fp64 oracle, forward + backward of {heads} of {w.B * w.H} heads per step "
+              f"({w.name}, causal settings {list(w.causal)})")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def kernel_source_digest() -> str:
+    """Digest of the sources the backward main kernel is built from."""
+    h = hashlib.sha256()
+    for f in ("bwd_tc.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "exact_io_aware_26_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) recorded in
+    profiles/traffic.json for this workload and this exact kernel source; None otherwise."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[workload][kernel]
+        if t.get("source_digest") != kernel_source_digest():
+            return None
+        return t["bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def run_e2e(fa, inp, runs, flops, steps, dev, stream):
+    """Same metric with host buffers: H2D inputs, the path, D2H of every output, per step."""
+    import torch
+    host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    dev_in = {n: torch.empty_like(inp[n], device=dev) for n in host_in}
+    host_out = [{n: torch.empty(r[n].shape, dtype=r[n].dtype).pin_memory()
+                 for n in ("o", "lse", "dq", "dk", "dv")} for r in runs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for ho in host_out for t in ho.values())
+
+    def one():
+        for n in host_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        for r, ho in zip(runs, host_out):
+            fa.fwd_raw(r["p"], dev_in["q"], dev_in["k"], dev_in["v"], r["o"], r["lse"], stream)
+            fa.bwd_preprocess(r["p"], r["o"], dev_in["do"], r["ws"], stream)
+            fa.bwd_main(r["p"], dev_in["q"], dev_in["k"], dev_in["v"], dev_in["do"], r["lse"],
+                        r["dk"], r["dv"], r["ws"], stream)
+            fa.bwd_finalize(r["p"], r["dq"], r["ws"], stream)
+            for n in ho:
+                ho[n].copy_(r[n], non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    s = a.elapsed_time(b) / 1000.0
+    step_flops = sum(f["fwd"] + f["bwd"] for f in flops.values())
+    return {"value": step_flops * steps / s / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = parse()
+    import torch
+    import synth
+
+    w = synth.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    import exact_io_aware_26_gb300 as fa
+    lib = fa.load()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    inp = synth.workload_inputs(w)
+    dev = torch.device("cuda", local)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    mask = None if inp["mask"] is None else torch.as_tensor(inp["mask"]).to(dev)
+    flops = workload_flops(w, inp["mask"])
+    step_flops = sum(f["fwd"] + f["bwd"] for f in flops.values())
+
+    runs = []
+    for c in w.causal:
+        p, keep = fa.make_params(q, w.scale, c, mask, w.mask_block)
+        ws = torch.empty(int(lib.fa_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8,
+                         device=dev)
+        runs.append(dict(causal=c, p=p, keep=keep, o=torch.empty_like(q),
+                         lse=torch.empty(q.shape[:3], dtype=torch.float32, device=dev),
+                         dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
+                         ws=ws))
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev_main=None, ev_fwd=None):
+        for i, r in enumerate(runs):
+            if ev_fwd is not None:
+                ev_fwd[i][0].record(stream)
+            fa.fwd_raw(r["p"], q, k, v, r["o"], r["lse"], stream)
+            if ev_fwd is not None:
+                ev_fwd[i][1].record(stream)
+            fa.bwd_preprocess(r["p"], r["o"], do, r["ws"], stream)
+            if ev_main is not None:
+                ev_main[i][0].record(stream)
+            fa.bwd_main(r["p"], q, k, v, do, r["lse"], r["dk"], r["dv"], r["ws"], stream)
+            if ev_main is not None:
+                ev_main[i][1].record(stream)
+            fa.bwd_finalize(r["p"], r["dq"], r["ws"], stream)
+
+    W = max(args.warmup, 3)
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    if fa.get_status() != fa.FA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    K = args.steps
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    ev_step = [(E(), E()) for _ in range(K)]
+    ev_main = [[(E(), E()) for _ in runs] for _ in range(K)]
+    ev_fwd = [[(E(), E()) for _ in runs] for _ in range(K)]
+    uuid = getattr(torch.cuda.get_device_properties(local), "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(0)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev_step[i][0].record(stream)
+        step(ev_main[i], ev_fwd[i])
+        ev_step[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks.mark(1)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    status = fa.get_status()
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    total_s = sum(a.elapsed_time(b) for a, b in ev_step) / 1000.0
+    main_s = sum(a.elapsed_time(b) for row in ev_main for a, b in row) / 1000.0
+    fwd_s = sum(a.elapsed_time(b) for row in ev_fwd for a, b in row) / 1000.0
+    if dist:
+        t = torch.tensor([total_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+
+    peak, peak_src = read_peaks()
+    launches = K * len(runs)
+    bwd_flops = sum(flops[r["causal"]]["bwd"] for r in runs) * K
+    fwd_flops = sum(flops[r["causal"]]["fwd"] for r in runs) * K
+    achieved = bwd_flops / main_s / 1e12
+    fwd_tflops = fwd_flops / fwd_s / 1e12
+    value = step_flops * K * world / total_s / 1e12
+
+    e2e = run_e2e(fa, inp, runs, flops, args.e2e_steps, dev, stream)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        heads = heads_for_seconds(w, 15.0)
+        f, s, cores = oracle_sample(w, inp, heads)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"fp64 oracle forward + backward of {heads} of {w.B * w.H} heads "
+                         f"(causal settings {list(w.causal)}), {s:.1f} s"}
+
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": 1000.0 * total_s / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic", "config": config_of(w),
+            "breakdown": {
+                "fwd_tflops": fwd_tflops, "bwd_main_tflops": achieved,
+                "fwd_frac_of_bf16_peak": fwd_tflops / peak,
+                "bwd_main_frac_of_bf16_peak": achieved / peak,
+                "step_frac_of_bf16_peak": value / world / peak,
+                "wall_s_timed_region": wall},
+            "roofline": {"kernel": "bwd_tc_kernel (backward main)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "peak_source": ("measured bf16 burst, MEASURED_PEAKS.json"
+                                         if peak_src == "measured" else "fallback bf16 burst"),
+                         "traffic": measured_traffic(w.name, "bwd_main"),
+                         "algorithmic_flops_per_launch": bwd_flops / launches},
+            "clocks": clk, "e2e": e2e, "gpu_launches": launches * 4,
+            "cpu_baseline": cpu}), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
