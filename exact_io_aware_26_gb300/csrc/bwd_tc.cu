@@ -350,7 +350,10 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       have = ok && it > 0;
     }
-    if (ok && key < a.N) {
+    // tcgen05.ld is .sync.aligned: every lane of the warp loads (the condition
+    // `ok`/`have` is warp-uniform); only the stores are predicated on the row
+    if (ok) {
+      const bool store = key < a.N;
       typedef uint16_t elem_t;
       elem_t* dVrow = reinterpret_cast<elem_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * (D / 2);
       elem_t* dKrow = reinterpret_cast<elem_t*>(a.dK) + ((size_t)bh * a.N + key) * D + g * (D / 2);
@@ -374,7 +377,7 @@ __global__ void __launch_bounds__(320, 1)
             pk.y = pack2<F16>(__uint_as_float(u[v * 8 + 2]) * mul, __uint_as_float(u[v * 8 + 3]) * mul);
             pk.z = pack2<F16>(__uint_as_float(u[v * 8 + 4]) * mul, __uint_as_float(u[v * 8 + 5]) * mul);
             pk.w = pack2<F16>(__uint_as_float(u[v * 8 + 6]) * mul, __uint_as_float(u[v * 8 + 7]) * mul);
-            *reinterpret_cast<uint4*>(dst + c0 + v * 8) = pk;
+            if (store) *reinterpret_cast<uint4*>(dst + c0 + v * 8) = pk;
           }
         }
       }

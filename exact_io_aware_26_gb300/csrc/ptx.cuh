@@ -237,6 +237,10 @@ __device__ __forceinline__ uint32_t sw128_chunk_offset(int r, int ch, int rows) 
 #define FA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
                  "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 
+// TMEM loads and stores are .sync.aligned: all 32 lanes of the warp must execute
+// them together, so they may only sit under warp-uniform conditions (predicate
+// the global stores that follow, never the TMEM access itself).
+//
 // 32 consecutive TMEM columns of this thread's lane -> 32 registers, and wait
 // for the load in the same asm statement so that no use can be scheduled
 // before the data has arrived.
