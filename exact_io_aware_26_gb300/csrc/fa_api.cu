@@ -13,6 +13,12 @@
 using namespace fa;
 
 namespace {
+void set_err(const char* fmt, ...);
+}
+
+void fa::set_error_text(const char* text) { set_err("%s", text); }
+
+namespace {
 
 __device__ DevStatus g_status;  // per device: first error code + abort epoch
 

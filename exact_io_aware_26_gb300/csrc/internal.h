@@ -72,4 +72,7 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* 
 cudaError_t launch_bwd_finalize(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_wait_selftest(const Report& rep, cudaStream_t s);
 
+// Records the text fa_last_error() returns on this thread.
+void set_error_text(const char* text);
+
 }  // namespace fa

@@ -129,6 +129,38 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
 fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/*
+ * Maximum workspace, in bytes, that fa_bwd_noalloc can serve (64 MiB): enough for
+ * B*H*N*(d+1) <= 16 Mi fp32 values, e.g. B=4, H=12, N=2048, d=64.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+
+/*
+ * The backward pass for callers that cannot allocate device memory where they
+ * run it -- a plugin handed a fixed memory budget by its host application, an
+ * engine that plans every buffer ahead of time and forbids allocation on its
+ * execution path, or code that must not enter the CUDA allocator while other
+ * work holds it.  The pages have no counterpart of this call; it exists for
+ * those callers only.
+ *
+ * Same arguments and results as fa_bwd without the workspace: the fp32 scratch
+ * (D and the dQ accumulator) comes from a FA_NOALLOC_SCRATCH_BYTES array that
+ * is part of the library image, so every GPU that loads libfa.so holds that
+ * memory until the process exits.  No call here allocates or frees device
+ * memory.  A problem whose workspace (fa_bwd_workspace_size) exceeds the array
+ * is rejected with FA_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  Every call, on every stream, shares the one array: calls that can
+ * overlap on the GPU race on it and must be serialised by the caller.  Each
+ * call rewrites all the scratch it reads (D, and the dQ accumulator, which it
+ * zeroes first), so nothing left by an earlier call affects its results.
+ */
+fa_status fa_bwd_noalloc(const fa_params* p, const void* Q, const void* K, const void* V,
+                         const void* O, const void* dO, const float* LSE, void* dQ, void* dK,
+                         void* dV, void* stream);
+
 /* Synchronises `stream`, returns the device-side status recorded since the
  * previous call (FA_OK or FA_ERR_TIMEOUT) and clears it; FA_ERR_CUDA if the
  * synchronisation itself fails. */
