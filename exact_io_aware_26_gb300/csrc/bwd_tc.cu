@@ -10,7 +10,7 @@
 //   S^T  = K_j Q_i^T                    (tcgen05, TMEM)
 //   P^T  = exp(scale * S^T - LSE_i)      (CUDA cores; thread = key row)
 //   dP^T = V_j dO_i^T                    (tcgen05, TMEM)
-//   dV  += P^T dO_i                      (tcgen05, P^T from shared memory)
+//   dV  += P^T dO_i                      (tcgen05, P^T read from TMEM)
 //   dS^T = P^T * (dP^T - D_i)            (CUDA cores)
 //   dK  += dS^T Q_i                      (tcgen05)
 //   dQ_i = dS K_j                        (tcgen05, read back and added to the
@@ -32,26 +32,26 @@ constexpr int kTile = 128;
 template <int D>
 struct BwdLayout {
   static constexpr uint32_t TILE = kTile * D * 2;
-  static constexpr int NS = (D == 64) ? 2 : 1;        // Q/dO ring depth
+  static constexpr int NS = 2;                         // Q/dO ring depth
   static constexpr uint32_t K = 0;
   static constexpr uint32_t V = TILE;
-  static constexpr uint32_t QS = 2 * TILE;            // stage s: Q at QS + 2s TILE, dO after it
-  static constexpr uint32_t PT = QS + NS * 2 * TILE;  // P^T, 128 x 128 16-bit
-  static constexpr uint32_t DST = PT + kTile * kTile * 2;  // dS^T
+  static constexpr uint32_t QS = 2 * TILE;             // stage s: Q at QS + 2s TILE, dO after it
+  static constexpr uint32_t DST = QS + NS * 2 * TILE;  // dS^T, 128 x 128 16-bit
   static constexpr uint32_t STAT = DST + kTile * kTile * 2;  // [2][256] fp32: LSE*log2e, D
   static constexpr uint32_t BAR = STAT + 2 * 256 * 4;
-  // barriers: 0 kv_full, 1 s_full, 2 s_free, 3 dp_full, 4 dp_free, 5 p_full, 6 p_free,
-  //           7 ds_full, 8 ds_free, 9 dq_full, 10 dq_free, 11 done, 12-13 stat[2],
-  //           14.. q_full[NS], 14+NS.. q_empty[NS]
-  static constexpr uint32_t NBAR = 14 + 2 * NS;
+  // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
+  //           7 dq_full, 8 dq_free, 9 done, 10-11 stat[2], 12.. q_full[NS], 12+NS.. q_empty[NS]
+  static constexpr uint32_t NBAR = 12 + 2 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns
+  // TMEM columns.  S^T [0,128): warpgroup g reads columns [64g, 64g+64) and then
+  // writes its 16-bit P^T over [64g, 64g+32).  dP^T [128,256), dV and dK d columns
+  // each, dQ d columns of its own at d = 64 and over dP^T at d = 128.
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
-  static constexpr bool ALIAS_DQ = (D == 128);  // dQ reuses the S^T columns
-  static constexpr uint32_t T_DQ = ALIAS_DQ ? T_S : 256 + 2 * D;
+  static constexpr bool ALIAS_DQ = (D == 128);
+  static constexpr uint32_t T_DQ = ALIAS_DQ ? T_DP : 256 + 2 * D;
 };
 
 __device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
@@ -65,10 +65,28 @@ __device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int q
   return true;
 }
 
+// First query tile at or after qt that sees key tile kt, or n_tiles.
+__device__ __forceinline__ int next_q(const MaskArgs& m, int b, int h, int qt, int kt, int n_tiles) {
+  while (qt < n_tiles && !tile_kept(m, b, h, qt, kt)) ++qt;
+  return qt;
+}
+
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
                "f"(d)
                : "memory");
+}
+
+// Row statistic t of query tile qt, as the compute warps keep it: threads 0-127
+// hold LSE * log2(e) (+inf hides the row: past the end, or a row that saw no key),
+// threads 128-255 hold D.
+__device__ __forceinline__ float load_stat(const BwdArgs& a, int bh, int qt, int t) {
+  const int q = qt * kTile + (t & 127);
+  if (t < 128) {
+    const float lse = q < a.N ? a.LSE[(size_t)bh * a.N + q] : -INFINITY;
+    return (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
+  }
+  return q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
 }
 
 template <int D, bool F16>
@@ -90,13 +108,12 @@ __global__ void __launch_bounds__(320, 1)
   const int qt_begin = a.m.causal ? kt : 0;
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
-  const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_s_free = bar(2), bar_dp_full = bar(3),
-                 bar_dp_free = bar(4), bar_p_full = bar(5), bar_p_free = bar(6),
-                 bar_ds_full = bar(7), bar_ds_free = bar(8), bar_dq_full = bar(9),
-                 bar_dq_free = bar(10), bar_done = bar(11);
-  auto bar_stat = [&](int s) { return bar(12 + s); };
-  auto bar_qf = [&](int s) { return bar(14 + s); };
-  auto bar_qe = [&](int s) { return bar(14 + NS + s); };
+  const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_dp_full = bar(2), bar_dp_free = bar(3),
+                 bar_p_full = bar(4), bar_ds_full = bar(5), bar_ds_free = bar(6),
+                 bar_dq_full = bar(7), bar_dq_free = bar(8), bar_done = bar(9);
+  auto bar_stat = [&](int s) { return bar(10 + s); };
+  auto bar_qf = [&](int s) { return bar(12 + s); };
+  auto bar_qe = [&](int s) { return bar(12 + NS + s); };
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -107,11 +124,9 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
     mbar_init(bar_s_full, 1);
-    mbar_init(bar_s_free, 8);
     mbar_init(bar_dp_full, 1);
     mbar_init(bar_dp_free, 8);
     mbar_init(bar_p_full, 8);
-    mbar_init(bar_p_free, 1);
     mbar_init(bar_ds_full, 8);
     mbar_init(bar_ds_free, 1);
     mbar_init(bar_dq_full, 1);
@@ -148,8 +163,8 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sb + L::V + c * (kTile * 128), &tmV, bar_kv, c * 64, kt * kTile, bh);
       }
       int it = 0;
-      for (int qt = qt_begin; qt < n_tiles; ++qt) {
-        if (!tile_kept(a.m, b, h, qt, kt)) continue;
+      for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles;
+           qt = next_q(a.m, b, h, qt + 1, kt, n_tiles)) {
         const int s = it % NS;
         if (it >= NS && !mbar_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
         const uint32_t dst = sb + L::QS + (uint32_t)s * 2u * L::TILE;
@@ -168,44 +183,49 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Order per query tile i (the next tile's Q/dO sit in the other ring stage):
+    //   dV += P^T dO_i | S^T_{i+1} | dK += dS^T Q_i, dQ_i = dS K | dP^T_{i+1}
+    // so the next score tile is computed while the compute warps form dS_i, and
+    // the next dP^T while they read dQ_i out.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);  // K-major x K-major
       constexpr uint32_t idKV = idesc_f16(F16, kTile, D, false, true);      // K-major x MN-major
       constexpr uint32_t idQ = idesc_f16(F16, kTile, D, true, true);        // MN-major x MN-major
       const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
-      bool ok = mbar_wait(w, bar_kv, 0);
-      int it = 0;
-      for (int qt = qt_begin; ok && qt < n_tiles; ++qt) {
-        if (!tile_kept(a.m, b, h, qt, kt)) continue;
-        const int s = it % NS;
-        const uint32_t sQ = sb + L::QS + (uint32_t)s * 2u * L::TILE, sdO = sQ + L::TILE;
-        if (!(ok = mbar_wait(w, bar_qf(s), (it / NS) & 1))) break;
-        if (it > 0) {
-          if (!(ok = mbar_wait(w, bar_s_free, (it - 1) & 1))) break;
-          if (L::ALIAS_DQ && !(ok = mbar_wait(w, bar_dq_free, (it - 1) & 1))) break;
-        }
+      auto stage_q = [&](int it) { return sb + L::QS + (uint32_t)(it % NS) * 2u * L::TILE; };
+      auto issue_s = [&](int it) -> bool {
+        if (!mbar_wait(w, bar_qf(it % NS), (it / NS) & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tS, desc_kmajor(sb + L::K, kk, kTile), desc_kmajor(sQ, kk, kTile), idS,
+          tc_mma_ss(tS, desc_kmajor(sb + L::K, kk, kTile), desc_kmajor(stage_q(it), kk, kTile), idS,
                     kk > 0 ? 1u : 0u);
         tc_commit(bar_s_full);
-        if (it > 0 && !(ok = mbar_wait(w, bar_dp_free, (it - 1) & 1))) break;
-        tc_fence_after();
+        return true;
+      };
+      auto issue_dp = [&](int it) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tDP, desc_kmajor(sb + L::V, kk, kTile), desc_kmajor(sdO, kk, kTile), idS,
-                    kk > 0 ? 1u : 0u);
+          tc_mma_ss(tDP, desc_kmajor(sb + L::V, kk, kTile),
+                    desc_kmajor(stage_q(it) + L::TILE, kk, kTile), idS, kk > 0 ? 1u : 0u);
         tc_commit(bar_dp_full);
-        // dV += P^T dO_i
+      };
+      bool ok = mbar_wait(w, bar_kv, 0);
+      int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
+      if (ok && qt < n_tiles && (ok = issue_s(0))) issue_dp(0);
+      for (int it = 0; ok && qt < n_tiles; ++it) {
+        const uint32_t sQ = stage_q(it), sdO = sQ + L::TILE;
+        // dV += P^T dO_i, P^T read from TMEM (warpgroup g's half at columns 64g..64g+31)
         if (!(ok = mbar_wait(w, bar_p_full, it & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ss(tDV, desc_kmajor(sb + L::PT, kk, kTile), desc_mnmajor(sdO, kk, kTile), idKV,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar_p_free);
+          tc_mma_ts(tDV, tS + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+                    desc_mnmajor(sdO, kk, kTile), idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
+        // S^T_{i+1} lands in the same columns after dV has read P^T (issue order)
+        if (qn < n_tiles && !(ok = issue_s(it + 1))) break;
         // dK += dS^T Q_i ; dQ_i = dS K_j
         if (!(ok = mbar_wait(w, bar_ds_full, it & 1))) break;
         tc_fence_after();
@@ -221,8 +241,15 @@ __global__ void __launch_bounds__(320, 1)
                     idQ, kk > 0 ? 1u : 0u);
         tc_commit(bar_ds_free);
         tc_commit(bar_dq_full);
-        tc_commit(bar_qe(s));
-        ++it;
+        tc_commit(bar_qe(it % NS));
+        if (qn < n_tiles) {
+          // dP^T_{i+1}: dP^T_i has been read; at d = 128 dQ_i (over dP^T) too
+          if (!(ok = mbar_wait(w, bar_dp_free, it & 1))) break;
+          if (L::ALIAS_DQ && !(ok = mbar_wait(w, bar_dq_free, it & 1))) break;
+          tc_fence_after();
+          issue_dp(it + 1);
+        }
+        qt = qn;
       }
       tc_commit(bar_done);
       mbar_drain(w, bar_done, 0);
@@ -233,31 +260,23 @@ __global__ void __launch_bounds__(320, 1)
     const int r = (warp & 3) * 32 + lane;    // key row in the tile = TMEM lane
     const int key = kt * kTile + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float c2 = a.scale_log2;
+    const uint64_t c2p = f2pack(a.scale_log2, a.scale_log2);
     const float* stat = reinterpret_cast<const float*>(smem + L::STAT);
     float* stat_w = reinterpret_cast<float*>(smem + L::STAT);
     const int t = threadIdx.x;  // 0..255
     bool ok = true;
     int it = 0;
-    for (int qt = qt_begin; qt < n_tiles; ++qt) {
-      if (!tile_kept(a.m, b, h, qt, kt)) continue;
-      // row statistics of the query tile: LSE in log2 units (+inf hides the row:
-      // past the end, or a row that saw no key) and D
-      {
-        const int q = qt * kTile + (t & 127);
-        float v;
-        if (t < 128) {
-          const float lse = q < a.N ? a.LSE[(size_t)bh * a.N + q] : -INFINITY;
-          v = (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
-        } else {
-          v = q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
-        }
-        stat_w[(it & 1) * 256 + t] = v;
-        mbar_arrive(bar_stat(it & 1));
-        // buffer it&1 was last read in iteration it-2, which every thread
-        // finished before arriving for iteration it-1
-        if (!(ok = warp_wait(w, bar_stat(it & 1), (it >> 1) & 1))) break;
-      }
+    int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
+    float pre = qt < n_tiles ? load_stat(a, bh, qt, t) : 0.f;
+    for (; qt < n_tiles; ++it) {
+      const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
+      // publish this tile's row statistics and fetch the next tile's early
+      stat_w[(it & 1) * 256 + t] = pre;
+      mbar_arrive(bar_stat(it & 1));
+      if (qn < n_tiles) pre = load_stat(a, bh, qn, t);
+      // buffer it&1 was last read in iteration it-2, which every thread
+      // finished before arriving for iteration it-1
+      if (!(ok = warp_wait(w, bar_stat(it & 1), (it >> 1) & 1))) break;
       const float* lse2 = stat + (it & 1) * 256 + 64 * g;
       const float* Dq = stat + (it & 1) * 256 + 128 + 64 * g;
 
@@ -270,26 +289,24 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(u[c]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s_free);
       const int q0 = qt * kTile + 64 * g;
       const bool row_out = key >= a.N;
       const bool diag = a.m.causal && qt == kt;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float pv = ex2(fmaf(p[c], c2, -lse2[c]));
-        if (row_out || (diag && q0 + c < key)) pv = 0.f;
-        p[c] = pv;
+      for (int c = 0; c < 64; c += 2) {
+        float x0, x1;
+        f2unpack(ffma2(f2pack(p[c], p[c + 1]), c2p, f2pack(-lse2[c], -lse2[c + 1])), x0, x1);
+        float p0 = ex2(x0), p1 = ex2(x1);
+        if (row_out || (diag && q0 + c < key)) p0 = 0.f;
+        if (row_out || (diag && q0 + c + 1 < key)) p1 = 0.f;
+        p[c] = p0;
+        p[c + 1] = p1;
+        pk[c / 2] = pack2<F16>(p0, p1);
       }
-      if (it > 0 && !(ok = warp_wait(w, bar_p_free, (it - 1) & 1))) break;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        st_shared_v4(sb + L::PT + sw128_chunk_offset(r, 8 * g + ch, kTile),
-                     pack2<F16>(p[ch * 8 + 0], p[ch * 8 + 1]), pack2<F16>(p[ch * 8 + 2], p[ch * 8 + 3]),
-                     pack2<F16>(p[ch * 8 + 4], p[ch * 8 + 5]), pack2<F16>(p[ch * 8 + 6], p[ch * 8 + 7]));
-      }
-      fence_async_smem();
+      // P^T over the first half of this warpgroup's S^T columns
+      tmem_st32(tmem + L::T_S + lane_off + 64 * g, pk);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_full);
@@ -307,14 +324,18 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dp_free);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) ds[c] = p[c] * (ds[c] - Dq[c]);
+      for (int c = 0; c < 64; c += 2) {
+        float y0, y1;
+        f2unpack(fmul2(f2pack(p[c], p[c + 1]),
+                       fadd2(f2pack(ds[c], ds[c + 1]), f2pack(-Dq[c], -Dq[c + 1]))),
+                 y0, y1);
+        pk[c / 2] = pack2<F16>(y0, y1);
+      }
       if (it > 0 && !(ok = warp_wait(w, bar_ds_free, (it - 1) & 1))) break;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        st_shared_v4(sb + L::DST + sw128_chunk_offset(r, 8 * g + ch, kTile),
-                     pack2<F16>(ds[ch * 8 + 0], ds[ch * 8 + 1]), pack2<F16>(ds[ch * 8 + 2], ds[ch * 8 + 3]),
-                     pack2<F16>(ds[ch * 8 + 4], ds[ch * 8 + 5]), pack2<F16>(ds[ch * 8 + 6], ds[ch * 8 + 7]));
-      }
+      for (int ch = 0; ch < 8; ++ch)
+        st_shared_v4(sb + L::DST + sw128_chunk_offset(r, 8 * g + ch, kTile), pk[ch * 4 + 0],
+                     pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -341,7 +362,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_free);
-      ++it;
+      qt = qn;
     }
     // ------------------------------------------------------------ dK, dV epilogue
     bool have = false;
@@ -354,13 +375,12 @@ __global__ void __launch_bounds__(320, 1)
     // `ok`/`have` is warp-uniform); only the stores are predicated on the row
     if (ok) {
       const bool store = key < a.N;
-      typedef uint16_t elem_t;
-      elem_t* dVrow = reinterpret_cast<elem_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * (D / 2);
-      elem_t* dKrow = reinterpret_cast<elem_t*>(a.dK) + ((size_t)bh * a.N + key) * D + g * (D / 2);
+      uint16_t* dVrow = reinterpret_cast<uint16_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * (D / 2);
+      uint16_t* dKrow = reinterpret_cast<uint16_t*>(a.dK) + ((size_t)bh * a.N + key) * D + g * (D / 2);
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = (which == 0 ? L::T_DV : L::T_DK) + g * (D / 2);
         const float mul = which == 0 ? 1.f : a.scale;
-        elem_t* dst = which == 0 ? dVrow : dKrow;
+        uint16_t* dst = which == 0 ? dVrow : dKrow;
 #pragma unroll
         for (int c0 = 0; c0 < D / 2; c0 += 32) {
           uint32_t u[32];
@@ -372,12 +392,12 @@ __global__ void __launch_bounds__(320, 1)
           }
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            uint4 pk;
-            pk.x = pack2<F16>(__uint_as_float(u[v * 8 + 0]) * mul, __uint_as_float(u[v * 8 + 1]) * mul);
-            pk.y = pack2<F16>(__uint_as_float(u[v * 8 + 2]) * mul, __uint_as_float(u[v * 8 + 3]) * mul);
-            pk.z = pack2<F16>(__uint_as_float(u[v * 8 + 4]) * mul, __uint_as_float(u[v * 8 + 5]) * mul);
-            pk.w = pack2<F16>(__uint_as_float(u[v * 8 + 6]) * mul, __uint_as_float(u[v * 8 + 7]) * mul);
-            if (store) *reinterpret_cast<uint4*>(dst + c0 + v * 8) = pk;
+            uint4 pq;
+            pq.x = pack2<F16>(__uint_as_float(u[v * 8 + 0]) * mul, __uint_as_float(u[v * 8 + 1]) * mul);
+            pq.y = pack2<F16>(__uint_as_float(u[v * 8 + 2]) * mul, __uint_as_float(u[v * 8 + 3]) * mul);
+            pq.z = pack2<F16>(__uint_as_float(u[v * 8 + 4]) * mul, __uint_as_float(u[v * 8 + 5]) * mul);
+            pq.w = pack2<F16>(__uint_as_float(u[v * 8 + 6]) * mul, __uint_as_float(u[v * 8 + 7]) * mul);
+            if (store) *reinterpret_cast<uint4*>(dst + c0 + v * 8) = pq;
           }
         }
       }

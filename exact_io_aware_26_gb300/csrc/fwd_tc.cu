@@ -9,41 +9,52 @@
 //   m'  = max(m, rowmax(scale * S))      one thread per row (TMEM lane)
 //   P~  = exp(scale * S - m')            exp2 with log2(e) folded into scale
 //   l   = l * e^(m - m') + rowsum(P~)
-//   O   = O * e^(m - m') + P~ V_j        rescale in TMEM, then tcgen05.mma
+//   O   = O * e^(m - m') + P~ V_j        P~ written to TMEM as 16-bit, then
+//                                        tcgen05.mma with A read from TMEM
 // and at the end O / l and LSE = m + ln l are written out.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t = TMEM lane t;
-//   warp 4     TMA producer: Q once, then K_j / V_j through a 2-stage ring;
-//   warp 5     TMEM allocator and MMA issuer (one thread).
-// The MMA thread issues S_{j+1} as soon as the softmax warps have copied S_j
-// into registers, so the tensor core computes the next score tile while the
-// exponentials of the current one run on the CUDA cores ("FA3 : Mécanique de
-// la trémie", point 2).  Tiles hidden by the causal rule or the block mask
-// are never loaded ("Le masquage causal ...": "jamais chargée et jamais
-// calculée").
+// The running max is only moved when a row's new maximum exceeds the one in
+// use by more than 2^8 (in the exp2 domain): until then P~ <= 2^8, which fp32
+// sums and the 16-bit P~ hold exactly as well, and O and l keep sharing the
+// same stale max, so the result is unchanged while most tiles skip the O
+// rescale.
+//
+// Per CTA the schedule is serial -- S_j, softmax, P~V_j, S_{j+1} -- because
+// P~ overwrites S in TMEM; two CTAs share each SM (256 TMEM columns and at
+// most 97 KiB of shared memory each), so one CTA's exponentials run on the
+// CUDA cores while the other's MMAs run on the tensor core ("FA3 : Mécanique
+// de la trémie", point 2, realised across CTAs).
+//
+// Warp roles (192 threads): warps 0-3 softmax (thread t owns query row t =
+// TMEM lane t); warp 4 TMA producer (Q once, K_j and V_j through a ring of
+// NS stages with separate K and V barriers); warp 5 TMEM owner and MMA
+// issuer.  Tiles hidden by the causal rule or the block mask are never
+// loaded ("Le masquage causal ...": "jamais chargée et jamais calculée").
 #include "ptx.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kTile = 128;  // query rows per CTA = keys per K/V tile
+constexpr int kTile = 128;        // query rows per CTA = keys per K/V tile
+constexpr float kRescaleThr = 8.f;  // move the running max only past 2^8
 
 template <int D>
 struct FwdLayout {
-  static constexpr uint32_t TILE = kTile * D * 2;     // one 128-row 16-bit tile
+  static constexpr uint32_t TILE = kTile * D * 2;  // one 128-row 16-bit tile
+  static constexpr int NS = (D == 64) ? 2 : 1;     // K/V ring depth
   static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K0 = Q + TILE;            // K stage s at K0 + s * TILE
-  static constexpr uint32_t V0 = K0 + 2 * TILE;       // V stage s at V0 + s * TILE
-  static constexpr uint32_t P = V0 + 2 * TILE;        // 128 x 128 16-bit probabilities
-  static constexpr uint32_t BAR = P + kTile * kTile * 2;
-  // barriers: 0 q_full, 1-2 k_full, 3-4 v_full, 5-6 kv_empty, 7 s_full,
-  //           8 s_free, 9 p_full, 10 o_done, 11 fin
-  static constexpr uint32_t NBAR = 12;
+  static constexpr uint32_t K0 = Q + TILE;          // K stage s at K0 + s * TILE
+  static constexpr uint32_t V0 = K0 + NS * TILE;    // V stage s at V0 + s * TILE
+  static constexpr uint32_t BAR = V0 + NS * TILE;
+  // barriers: 0 q_full, 1 s_full, 2 p_full, 3 o_done, 4 fin,
+  //           5.. k_full[NS], v_full[NS], k_empty[NS], v_empty[NS]
+  static constexpr uint32_t NBAR = 5 + 4 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
-  static constexpr uint32_t TMEM_COLS = 256;          // S: 128 columns, O: D columns
+  // TMEM: S at [0, 128) with P~ (16-bit pairs) over its first 64 columns; O at [128, 128 + D)
+  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr uint32_t T_S = 0, T_O = 128;
 };
 
 __device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
@@ -57,11 +68,19 @@ __device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int q
   return true;
 }
 
+// First kept key tile at or after kt, or kt_end when there is none.
+__device__ __forceinline__ int next_kept(const MaskArgs& m, int b, int h, int qt, int kt,
+                                         int kt_end) {
+  while (kt < kt_end && !tile_kept(m, b, h, qt, kt)) ++kt;
+  return kt;
+}
+
 template <int D, bool F16>
-__global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
+__global__ void __launch_bounds__(192, 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
   using L = FwdLayout<D>;
+  constexpr int NS = L::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -73,15 +92,12 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
   const int b = bh / a.H, h = bh % a.H;
   const int kt_end = a.m.causal ? min(qt + 1, n_tiles) : n_tiles;
 
-  const uint32_t bar_q = sb + L::BAR;
-  auto bar_k = [&](int s) { return sb + L::BAR + 8u * (1 + s); };
-  auto bar_v = [&](int s) { return sb + L::BAR + 8u * (3 + s); };
-  auto bar_e = [&](int s) { return sb + L::BAR + 8u * (5 + s); };
-  const uint32_t bar_s_full = sb + L::BAR + 8u * 7;
-  const uint32_t bar_s_free = sb + L::BAR + 8u * 8;
-  const uint32_t bar_p = sb + L::BAR + 8u * 9;
-  const uint32_t bar_o = sb + L::BAR + 8u * 10;
-  const uint32_t bar_fin = sb + L::BAR + 8u * 11;
+  auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
+  const uint32_t bar_q = bar(0), bar_s = bar(1), bar_p = bar(2), bar_o = bar(3), bar_fin = bar(4);
+  auto bar_kf = [&](int s) { return bar(5 + s); };
+  auto bar_vf = [&](int s) { return bar(5 + NS + s); };
+  auto bar_ke = [&](int s) { return bar(5 + 2 * NS + s); };
+  auto bar_ve = [&](int s) { return bar(5 + 3 * NS + s); };
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -91,16 +107,16 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
   }
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_k(s), 1);
-      mbar_init(bar_v(s), 1);
-      mbar_init(bar_e(s), 1);
-    }
-    mbar_init(bar_s_full, 1);
-    mbar_init(bar_s_free, 4);
+    mbar_init(bar_s, 1);
     mbar_init(bar_p, 4);
     mbar_init(bar_o, 1);
     mbar_init(bar_fin, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_kf(s), 1);
+      mbar_init(bar_vf(s), 1);
+      mbar_init(bar_ke(s), 1);
+      mbar_init(bar_ve(s), 1);
+    }
     *abort_cta = 0;
     fence_barrier_init();
   }
@@ -112,8 +128,6 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
-  const uint32_t tS = tmem;          // columns [0, 128)
-  const uint32_t tO = tmem + kTile;  // columns [128, 128 + D)
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -124,29 +138,30 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
       mbar_arrive_expect_tx(bar_q, L::TILE);
       for (int c = 0; c < D / 64; ++c)
         tma_load_3d(sb + L::Q + c * (kTile * 128), &tmQ, bar_q, c * 64, qt * kTile, bh);
-      int it = 0;
-      for (int kt = 0; kt < kt_end; ++kt) {
-        if (!tile_kept(a.m, b, h, qt, kt)) continue;
-        const int s = it & 1;
-        if (it >= 2 && !mbar_wait(w, bar_e(s), ((it >> 1) - 1) & 1)) break;
-        mbar_arrive_expect_tx(bar_k(s), L::TILE);
+      int nk = 0, nv = 0;  // K and V copies issued
+      for (int kt = next_kept(a.m, b, h, qt, 0, kt_end); kt < kt_end;
+           kt = next_kept(a.m, b, h, qt, kt + 1, kt_end)) {
+        const int s = nk % NS;
+        const uint32_t ph = ((nk / NS) - 1) & 1;
+        if (nk >= NS && !mbar_wait(w, bar_ke(s), ph)) break;
+        mbar_arrive_expect_tx(bar_kf(s), L::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sb + L::K0 + s * L::TILE + c * (kTile * 128), &tmK, bar_k(s), c * 64,
+          tma_load_3d(sb + L::K0 + s * L::TILE + c * (kTile * 128), &tmK, bar_kf(s), c * 64,
                       kt * kTile, bh);
-        mbar_arrive_expect_tx(bar_v(s), L::TILE);
+        ++nk;
+        if (nv >= NS && !mbar_wait(w, bar_ve(s), ph)) break;
+        mbar_arrive_expect_tx(bar_vf(s), L::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sb + L::V0 + s * L::TILE + c * (kTile * 128), &tmV, bar_v(s), c * 64,
+          tma_load_3d(sb + L::V0 + s * L::TILE + c * (kTile * 128), &tmV, bar_vf(s), c * 64,
                       kt * kTile, bh);
-        ++it;
+        ++nv;
       }
       // every copy issued must have landed before the CTA may exit
       mbar_drain(w, bar_q, 0);
-      for (int s = 0; s < 2; ++s) {
-        const int n = (it + 1 - s) / 2;  // loads issued into stage s
-        if (n > 0) {
-          mbar_drain(w, bar_k(s), (n - 1) & 1);
-          mbar_drain(w, bar_v(s), (n - 1) & 1);
-        }
+      for (int s = 0; s < NS; ++s) {
+        const int ck = (nk - s + NS - 1) / NS, cv = (nv - s + NS - 1) / NS;  // copies into stage s
+        if (ck > 0) mbar_drain(w, bar_kf(s), (ck - 1) & 1);
+        if (cv > 0) mbar_drain(w, bar_vf(s), (cv - 1) & 1);
       }
     }
   } else if (warp == 5) {
@@ -154,37 +169,39 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);
       constexpr uint32_t idO = idesc_f16(F16, kTile, D, false, true);
-      auto issue_pv = [&](int t) -> bool {
-        const int s = t & 1;
-        if (!mbar_wait(w, bar_p, t & 1)) return false;
-        if (!mbar_wait(w, bar_v(s), (t >> 1) & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ss(tO, desc_kmajor(sb + L::P, kk, kTile),
-                    desc_mnmajor(sb + L::V0 + s * L::TILE, kk, kTile), idO,
-                    (t > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar_o);
-        tc_commit(bar_e(s));
-        return true;
-      };
-      bool ok = mbar_wait(w, bar_q, 0);
-      int it = 0;
-      for (int kt = 0; ok && kt < kt_end; ++kt) {
-        if (!tile_kept(a.m, b, h, qt, kt)) continue;
-        const int s = it & 1;
-        if (!(ok = mbar_wait(w, bar_k(s), (it >> 1) & 1))) break;
-        if (it > 0 && !(ok = mbar_wait(w, bar_s_free, (it - 1) & 1))) break;
+      const uint32_t tS = tmem + L::T_S, tO = tmem + L::T_O;
+      auto issue_s = [&](int it) -> bool {
+        const int s = it % NS;
+        if (!mbar_wait(w, bar_kf(s), (it / NS) & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           tc_mma_ss(tS, desc_kmajor(sb + L::Q, kk, kTile),
                     desc_kmajor(sb + L::K0 + s * L::TILE, kk, kTile), idS, kk > 0 ? 1u : 0u);
-        tc_commit(bar_s_full);
-        if (it > 0 && !(ok = issue_pv(it - 1))) break;
-        ++it;
+        tc_commit(bar_s);
+        tc_commit(bar_ke(s));
+        return true;
+      };
+      bool ok = mbar_wait(w, bar_q, 0);
+      int kt = next_kept(a.m, b, h, qt, 0, kt_end);
+      if (ok && kt < kt_end) ok = issue_s(0);
+      for (int it = 0; ok && kt < kt_end; ++it) {
+        const int s = it % NS;
+        // P~ V_j, with P~ read from TMEM (it overwrote the first half of S)
+        if (!(ok = mbar_wait(w, bar_p, it & 1))) break;
+        if (!(ok = mbar_wait(w, bar_vf(s), (it / NS) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma_ts(tO, tS + (uint32_t)kk * 8u, desc_mnmajor(sb + L::V0 + s * L::TILE, kk, kTile),
+                    idO, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar_o);
+        tc_commit(bar_ve(s));
+        // the next score tile goes into the same TMEM columns: MMAs of one
+        // thread execute in issue order, so it lands after P~ V_j has read P~
+        kt = next_kept(a.m, b, h, qt, kt + 1, kt_end);
+        if (kt < kt_end) ok = issue_s(it + 1);
       }
-      if (ok && it > 0) issue_pv(it - 1);
       // every MMA issued must have completed before TMEM is released
       tc_commit(bar_fin);
       mbar_drain(w, bar_fin, 0);
@@ -194,29 +211,28 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
     const int r = threadIdx.x;  // query row in the tile = TMEM lane
     const int row = qt * kTile + r;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tS = tmem + L::T_S + lane_off, tO = tmem + L::T_O + lane_off;
     const float c2 = a.scale_log2;
-    float m2 = -INFINITY;  // running max of scale*log2(e)*S, log2 units
-    float l = 0.f;         // running sum of exp2(...) in fp32
+    float m_use = -INFINITY;  // running max in use (exp2 domain)
+    float l = 0.f;            // running sum of P~ (fp32)
     bool ok = true;
     int it = 0;
-    for (int kt = 0; kt < kt_end; ++kt) {
-      if (!tile_kept(a.m, b, h, qt, kt)) continue;
-      if (!(ok = warp_wait(w, bar_s_full, it & 1))) break;
+    for (int kt = next_kept(a.m, b, h, qt, 0, kt_end); kt < kt_end;
+         kt = next_kept(a.m, b, h, qt, kt + 1, kt_end), ++it) {
+      // S_j is complete, and so is every earlier MMA (P~ V_{j-1} included):
+      // O is stable and P~_{j-1} has been consumed
+      if (!(ok = warp_wait(w, bar_s, it & 1))) break;
       tc_fence_after();
       float s[kTile];
       {
         uint32_t u[64];
-        tmem_ld64(tS + lane_off, u);
+        tmem_ld64(tS, u);
 #pragma unroll
         for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
-        tmem_ld64(tS + lane_off + 64, u);
+        tmem_ld64(tS + 64, u);
 #pragma unroll
         for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(u[c]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s_free);
-
       // hide keys past the end of the sequence and, on the diagonal tile,
       // keys after the query ("Le masquage causal")
       const int k0 = kt * kTile;
@@ -227,56 +243,63 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
         for (int c = 0; c < kTile; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx = -INFINITY;
+      float mx = fmax3(s[0], s[1], s[2]);
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m2, mx * c2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m2 - m_use);
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        s[c] = ex2(fmaf(s[c], c2, -m_use));
-        sum += s[c];
+      for (int c = 3; c + 1 < kTile; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
+      mx = fmaxf(mx, s[kTile - 1]);
+      const float m_tile = mx * c2;
+      float alpha = 1.f;
+      if (m_tile > m_use + kRescaleThr) {
+        alpha = ex2(m_use - m_tile);  // 0 on the first tile that sees a key
+        m_use = m_tile;
       }
-      l = l * alpha + sum;
-
-      if (it > 0) {
-        // P~ V of the previous tile must be done: it read the P buffer and
-        // wrote the O accumulator that is rescaled now
-        if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      const float mneg = (m_use == -INFINITY) ? 0.f : -m_use;
+      const uint64_t c2p = f2pack(c2, c2), mp = f2pack(mneg, mneg);
+      uint64_t acc = f2pack(0.f, 0.f);
+      uint32_t plo[32], phi[32];  // P~ as 16-bit pairs: keys [0, 64) and [64, 128)
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + c0, o);
+      for (int c = 0; c < kTile; c += 2) {
+        float x0, x1;
+        f2unpack(ffma2(f2pack(s[c], s[c + 1]), c2p, mp), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        acc = fadd2(acc, f2pack(p0, p1));
+        if (c < 64)
+          plo[c / 2] = pack2<F16>(p0, p1);
+        else
+          phi[(c - 64) / 2] = pack2<F16>(p0, p1);
+      }
+      float sum0, sum1;
+      f2unpack(acc, sum0, sum1);
+      l = l * alpha + (sum0 + sum1);
+      // P~ over the first 64 columns of S (all of S is already in registers)
+      tmem_st32(tS, plo);
+      tmem_st32(tS + 32, phi);
+      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint64_t ap = f2pack(alpha, alpha);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + lane_off + c0, o);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float y0, y1;
+            f2unpack(fmul2(f2pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ap), y0, y1);
+            o[i] = __float_as_uint(y0);
+            o[i + 1] = __float_as_uint(y1);
           }
-          tmem_st_wait();
+          tmem_st32(tO + c0, o);
         }
       }
-      // P~ (16-bit) -> shared memory, K-major 128-byte-swizzled, row r
-#pragma unroll
-      for (int ch = 0; ch < kTile / 8; ++ch) {
-        st_shared_v4(sb + L::P + sw128_chunk_offset(r, ch, kTile),
-                     pack2<F16>(s[ch * 8 + 0], s[ch * 8 + 1]),
-                     pack2<F16>(s[ch * 8 + 2], s[ch * 8 + 3]),
-                     pack2<F16>(s[ch * 8 + 4], s[ch * 8 + 5]),
-                     pack2<F16>(s[ch * 8 + 6], s[ch * 8 + 7]));
-      }
-      fence_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
-      m2 = m_new;
-      ++it;
     }
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
     if (ok && it > 0) {
+      // every P~ V up to the (it-2)-th completed before S_{it-1} did, so the
+      // o_done barrier is at most one phase behind the last one
       ok = warp_wait(w, bar_o, (it - 1) & 1);
       tc_fence_after();
       have_o = ok;
@@ -284,15 +307,14 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     if (row < a.N && ok) {
       a.LSE[(size_t)bh * a.N + row] =
-          (l > 0.f) ? (m2 + __log2f(l)) * 0.693147180559945309f : -INFINITY;
+          (l > 0.f) ? (m_use + __log2f(l)) * 0.693147180559945309f : -INFINITY;
     }
-    typedef uint16_t elem_t;
-    elem_t* Orow = reinterpret_cast<elem_t*>(a.O) + ((size_t)bh * a.N + row) * D;
+    uint16_t* Orow = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t o[32];
       if (have_o) {
-        tmem_ld32(tO + lane_off + c0, o);
+        tmem_ld32(tO + c0, o);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;
@@ -300,12 +322,12 @@ __global__ void __launch_bounds__(192, (D == 64 ? 2 : 1))
       if (row < a.N && ok) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          uint4 pk;
-          pk.x = pack2<F16>(__uint_as_float(o[v * 8 + 0]) * inv_l, __uint_as_float(o[v * 8 + 1]) * inv_l);
-          pk.y = pack2<F16>(__uint_as_float(o[v * 8 + 2]) * inv_l, __uint_as_float(o[v * 8 + 3]) * inv_l);
-          pk.z = pack2<F16>(__uint_as_float(o[v * 8 + 4]) * inv_l, __uint_as_float(o[v * 8 + 5]) * inv_l);
-          pk.w = pack2<F16>(__uint_as_float(o[v * 8 + 6]) * inv_l, __uint_as_float(o[v * 8 + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(Orow + c0 + v * 8) = pk;
+          uint4 q;
+          q.x = pack2<F16>(__uint_as_float(o[v * 8 + 0]) * inv_l, __uint_as_float(o[v * 8 + 1]) * inv_l);
+          q.y = pack2<F16>(__uint_as_float(o[v * 8 + 2]) * inv_l, __uint_as_float(o[v * 8 + 3]) * inv_l);
+          q.z = pack2<F16>(__uint_as_float(o[v * 8 + 4]) * inv_l, __uint_as_float(o[v * 8 + 5]) * inv_l);
+          q.w = pack2<F16>(__uint_as_float(o[v * 8 + 6]) * inv_l, __uint_as_float(o[v * 8 + 7]) * inv_l);
+          *reinterpret_cast<uint4*>(Orow + c0 + v * 8) = q;
         }
       }
     }
