@@ -72,9 +72,12 @@ __device__ __forceinline__ void raise_error(const WaitCtx& w, int code) {
 // Wait until the phase with the given parity has completed.  Gives up (returns
 // false) when the time limit passes -- recording FA_ERR_TIMEOUT -- or when
 // another thread of this CTA or another CTA of this launch has given up.
-static __device__ __noinline__ bool mbar_wait(const WaitCtx& w, uint32_t bar, uint32_t parity) {
+// Inlined: a call would save and restore live registers through local memory
+// on every wait, which costs hundreds of cycles even when the phase is done.
+__device__ __forceinline__ bool mbar_wait(const WaitCtx& w, uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  uint64_t t0 = 0;
+#pragma unroll 1
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 63u) == 0) {
@@ -83,7 +86,10 @@ static __device__ __noinline__ bool mbar_wait(const WaitCtx& w, uint32_t bar, ui
         *w.abort_cta = 1;
         return false;
       }
-      if (globaltimer_ns() - t0 > w.limit_ns) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > w.limit_ns) {
         raise_error(w, FA_ERR_TIMEOUT);
         return false;
       }
