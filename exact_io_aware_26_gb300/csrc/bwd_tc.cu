@@ -20,8 +20,9 @@
 //
 // Warp roles (320 threads): warps 0-3 and 4-7 are two compute warpgroups that
 // split the 128 query columns of every tile (TMEM lane = key row); warp 8 is
-// the TMA producer (K_j, V_j once; Q_i, dO_i through a ring); warp 9 owns TMEM
-// and issues the MMAs.
+// the producer (TMA copies of K_j, V_j once and of Q_i, dO_i through a ring,
+// plus each query tile's LSE and D staged by its lanes); warp 9 owns TMEM and
+// issues the MMAs.
 #include "ptx.cuh"
 
 namespace fa {
@@ -37,21 +38,32 @@ struct BwdLayout {
   static constexpr uint32_t V = TILE;
   static constexpr uint32_t QS = 2 * TILE;             // stage s: Q at QS + 2s TILE, dO after it
   static constexpr uint32_t DST = QS + NS * 2 * TILE;  // dS^T, 128 x 128 16-bit
-  static constexpr uint32_t STAT = DST + kTile * kTile * 2;  // [2][256] fp32: LSE*log2e, D
-  static constexpr uint32_t BAR = STAT + 2 * 256 * 4;
+  // per ring stage, the query tile's row statistics: [128] LSE*log2e then [128] D
+  static constexpr uint32_t STAT = DST + kTile * kTile * 2;
+  static constexpr uint32_t BAR = STAT + NS * 256 * 4;
   // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
-  //           7 dq_full, 8 dq_free, 9 done, 10-11 stat[2], 12.. q_full[NS], 12+NS.. q_empty[NS]
-  static constexpr uint32_t NBAR = 12 + 2 * NS;
+  //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS]
+  static constexpr uint32_t NBAR = 10 + 2 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns.  S^T [0,128): warpgroup g reads columns [64g, 64g+64) and then
-  // writes its 16-bit P^T over [64g, 64g+32).  dP^T [128,256), dV and dK d columns
-  // each, dQ d columns of its own at d = 64 and over dP^T at d = 128.
+  // TMEM columns.  S^T [0,128) (warpgroup g reads [64g, 64g+64)), dP^T [128,256),
+  // dV and dK d columns each.  At d = 64, dQ [384,448) and the 16-bit P^T
+  // [448,512) have columns of their own; at d = 128 the 512 columns are full, so
+  // dQ goes over dP^T and warpgroup g writes its P^T over [64g, 64g+32) of S^T.
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
-  static constexpr bool ALIAS_DQ = (D == 128);
-  static constexpr uint32_t T_DQ = ALIAS_DQ ? T_DP : 256 + 2 * D;
+  static constexpr bool ALIAS = (D == 128);
+  static constexpr uint32_t T_DQ = ALIAS ? T_DP : 384;
+  static constexpr uint32_t T_PT = ALIAS ? T_S : 448;
+  // column of P^T that holds query pair kk*8 .. kk*8+7 (16 queries), and the
+  // columns warpgroup g writes
+  __device__ static constexpr uint32_t pt_col(int kk) {
+    return ALIAS ? 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3) : T_PT + 8u * (uint32_t)kk;
+  }
+  __device__ static constexpr uint32_t pt_write_col(int g) {
+    return ALIAS ? 64u * (uint32_t)g : T_PT + 32u * (uint32_t)g;
+  }
 };
 
 __device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
@@ -77,15 +89,13 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
                : "memory");
 }
 
-// Row statistic t of query tile qt, as the compute warps keep it: threads 0-127
-// hold LSE * log2(e) (+inf hides the row: past the end, or a row that saw no key),
-// threads 128-255 hold D.
-__device__ __forceinline__ float load_stat(const BwdArgs& a, int bh, int qt, int t) {
-  const int q = qt * kTile + (t & 127);
-  if (t < 128) {
-    const float lse = q < a.N ? a.LSE[(size_t)bh * a.N + q] : -INFINITY;
-    return (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
-  }
+// Row statistics of query q as the compute warps use them: LSE * log2(e), with
+// +inf hiding the row (past the end, or a row that saw no key), and D.
+__device__ __forceinline__ float lse2_of(const BwdArgs& a, int bh, int q) {
+  const float lse = q < a.N ? a.LSE[(size_t)bh * a.N + q] : -INFINITY;
+  return (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
+}
+__device__ __forceinline__ float d_of(const BwdArgs& a, int bh, int q) {
   return q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
 }
 
@@ -111,9 +121,8 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_dp_full = bar(2), bar_dp_free = bar(3),
                  bar_p_full = bar(4), bar_ds_full = bar(5), bar_ds_free = bar(6),
                  bar_dq_full = bar(7), bar_dq_free = bar(8), bar_done = bar(9);
-  auto bar_stat = [&](int s) { return bar(10 + s); };
-  auto bar_qf = [&](int s) { return bar(12 + s); };
-  auto bar_qe = [&](int s) { return bar(12 + NS + s); };
+  auto bar_qf = [&](int s) { return bar(10 + s); };
+  auto bar_qe = [&](int s) { return bar(10 + NS + s); };
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -132,10 +141,8 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 8);
     mbar_init(bar_done, 1);
-    mbar_init(bar_stat(0), 256);
-    mbar_init(bar_stat(1), 256);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_qf(s), 1);
+      mbar_init(bar_qf(s), 1 + 32);  // the TMA transaction arrival + every producer lane
       mbar_init(bar_qe(s), 1);
     }
     *abort_cta = 0;
@@ -152,6 +159,9 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // Lane 0 issues the TMA copies; every lane also stages four rows of the
+    // query tile's statistics into the ring stage, so that the stage's full
+    // barrier covers Q, dO and the statistics together.
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
@@ -162,19 +172,31 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sb + L::K + c * (kTile * 128), &tmK, bar_kv, c * 64, kt * kTile, bh);
         tma_load_3d(sb + L::V + c * (kTile * 128), &tmV, bar_kv, c * 64, kt * kTile, bh);
       }
-      int it = 0;
-      for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles;
-           qt = next_q(a.m, b, h, qt + 1, kt, n_tiles)) {
-        const int s = it % NS;
-        if (it >= NS && !mbar_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
+    }
+    int it = 0;
+    for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles;
+         qt = next_q(a.m, b, h, qt + 1, kt, n_tiles)) {
+      const int s = it % NS;
+      if (it >= NS && !warp_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
+      if (lane == 0) {
         const uint32_t dst = sb + L::QS + (uint32_t)s * 2u * L::TILE;
         mbar_arrive_expect_tx(bar_qf(s), 2 * L::TILE);
         for (int c = 0; c < D / 64; ++c) {
           tma_load_3d(dst + c * (kTile * 128), &tmQ, bar_qf(s), c * 64, qt * kTile, bh);
           tma_load_3d(dst + L::TILE + c * (kTile * 128), &tmdO, bar_qf(s), c * 64, qt * kTile, bh);
         }
-        ++it;
       }
+      float* st = reinterpret_cast<float*>(smem + L::STAT) + s * 256;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = lane * 4 + j, q = qt * kTile + row;
+        st[row] = lse2_of(a, bh, q);
+        st[128 + row] = d_of(a, bh, q);
+      }
+      mbar_arrive(bar_qf(s));
+      ++it;
+    }
+    if (lane == 0) {
       mbar_drain(w, bar_kv, 0);
       for (int s = 0; s < NS; ++s) {
         const int n = (it - s + NS - 1) / NS;  // loads issued into stage s
@@ -183,71 +205,100 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // Order per query tile i (the next tile's Q/dO sit in the other ring stage):
-    //   dV += P^T dO_i | S^T_{i+1} | dK += dS^T Q_i, dQ_i = dS K | dP^T_{i+1}
+    // MMAs that accumulate into one TMEM tile form a dependent chain (~90 cycles
+    // apiece whatever their size), so independent chains are issued interleaved.
+    // Per query tile i (the next tile's Q/dO sit in the other ring stage):
+    //   dV_i (+ S^T_{i+1} interleaved at d = 64, after it at d = 128)
+    //   dK_i, dQ_i (+ dP^T_{i+1} at d = 64) interleaved; dP^T_{i+1} after them at d = 128
     // so the next score tile is computed while the compute warps form dS_i, and
     // the next dP^T while they read dQ_i out.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);  // K-major x K-major
       constexpr uint32_t idKV = idesc_f16(F16, kTile, D, false, true);      // K-major x MN-major
       constexpr uint32_t idQ = idesc_f16(F16, kTile, D, true, true);        // MN-major x MN-major
+      constexpr int KS = D / 16;                                            // K steps of S^T, dP^T
       const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
       auto stage_q = [&](int it) { return sb + L::QS + (uint32_t)(it % NS) * 2u * L::TILE; };
-      auto issue_s = [&](int it) -> bool {
-        if (!mbar_wait(w, bar_qf(it % NS), (it / NS) & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tS, desc_kmajor(sb + L::K, kk, kTile), desc_kmajor(stage_q(it), kk, kTile), idS,
-                    kk > 0 ? 1u : 0u);
-        tc_commit(bar_s_full);
-        return true;
+      auto mma_s = [&](int it, int kk) {
+        tc_mma_ss(tS, desc_kmajor(sb + L::K, kk, kTile), desc_kmajor(stage_q(it), kk, kTile), idS,
+                  kk > 0 ? 1u : 0u);
       };
-      auto issue_dp = [&](int it) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tDP, desc_kmajor(sb + L::V, kk, kTile),
-                    desc_kmajor(stage_q(it) + L::TILE, kk, kTile), idS, kk > 0 ? 1u : 0u);
-        tc_commit(bar_dp_full);
+      auto mma_dp = [&](int it, int kk) {
+        tc_mma_ss(tDP, desc_kmajor(sb + L::V, kk, kTile),
+                  desc_kmajor(stage_q(it) + L::TILE, kk, kTile), idS, kk > 0 ? 1u : 0u);
+      };
+      auto mma_dv = [&](int it, int kk) {
+        tc_mma_ts(tDV, tmem + L::pt_col(kk), desc_mnmajor(stage_q(it) + L::TILE, kk, kTile), idKV,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+      };
+      auto mma_dk = [&](int it, int kk) {
+        tc_mma_ss(tDK, desc_kmajor(sb + L::DST, kk, kTile), desc_mnmajor(stage_q(it), kk, kTile),
+                  idKV, (it > 0 || kk > 0) ? 1u : 0u);
+      };
+      auto mma_dq = [&](int kk) {
+        tc_mma_ss(tDQ, desc_mnmajor(sb + L::DST, kk, kTile), desc_mnmajor(sb + L::K, kk, kTile),
+                  idQ, kk > 0 ? 1u : 0u);
       };
       bool ok = mbar_wait(w, bar_kv, 0);
       int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
-      if (ok && qt < n_tiles && (ok = issue_s(0))) issue_dp(0);
+      if (ok && qt < n_tiles && (ok = mbar_wait(w, bar_qf(0), 0))) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          mma_s(0, kk);
+          mma_dp(0, kk);
+        }
+        tc_commit(bar_s_full);
+        tc_commit(bar_dp_full);
+      }
       for (int it = 0; ok && qt < n_tiles; ++it) {
-        const uint32_t sQ = stage_q(it), sdO = sQ + L::TILE;
-        // dV += P^T dO_i, P^T read from TMEM (warpgroup g's half at columns 64g..64g+31)
-        if (!(ok = mbar_wait(w, bar_p_full, it & 1))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ts(tDV, tS + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
-                    desc_mnmajor(sdO, kk, kTile), idKV, (it > 0 || kk > 0) ? 1u : 0u);
         const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
-        // S^T_{i+1} lands in the same columns after dV has read P^T (issue order)
-        if (qn < n_tiles && !(ok = issue_s(it + 1))) break;
-        // dK += dS^T Q_i ; dQ_i = dS K_j
+        const bool next = qn < n_tiles;
+        // dV += P^T dO_i (P^T from TMEM); at d = 64 with S^T_{i+1} interleaved
+        if (!(ok = mbar_wait(w, bar_p_full, it & 1))) break;
+        if (next && !(ok = mbar_wait(w, bar_qf((it + 1) % NS), ((it + 1) / NS) & 1))) break;
+        tc_fence_after();
+        if (!L::ALIAS && next) {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_dv(it, kk);
+            if (kk < KS) mma_s(it + 1, kk);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) mma_dv(it, kk);
+          // at d = 128 S^T_{i+1} overwrites P^T: issue order puts it after dV
+          if (next) {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) mma_s(it + 1, kk);
+          }
+        }
+        if (next) tc_commit(bar_s_full);
+        // dK += dS^T Q_i, dQ_i = dS K_j (and dP^T_{i+1} at d = 64)
         if (!(ok = mbar_wait(w, bar_ds_full, it & 1))) break;
+        if (!L::ALIAS && it > 0 && !(ok = mbar_wait(w, bar_dq_free, (it - 1) & 1))) break;
+        const bool dp_now = !L::ALIAS && next;
+        if (dp_now && !(ok = mbar_wait(w, bar_dp_free, it & 1))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ss(tDK, desc_kmajor(sb + L::DST, kk, kTile), desc_mnmajor(sQ, kk, kTile), idKV,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        if (!L::ALIAS_DQ && it > 0 && !(ok = mbar_wait(w, bar_dq_free, (it - 1) & 1))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ss(tDQ, desc_mnmajor(sb + L::DST, kk, kTile), desc_mnmajor(sb + L::K, kk, kTile),
-                    idQ, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          mma_dk(it, kk);
+          mma_dq(kk);
+          if (dp_now && kk < KS) mma_dp(it + 1, kk);
+        }
         tc_commit(bar_ds_free);
         tc_commit(bar_dq_full);
         tc_commit(bar_qe(it % NS));
-        if (qn < n_tiles) {
-          // dP^T_{i+1}: dP^T_i has been read; at d = 128 dQ_i (over dP^T) too
+        if (dp_now) tc_commit(bar_dp_full);
+        if (L::ALIAS && next) {
+          // dP^T_{i+1} goes over dQ_i: wait until it has been read out
           if (!(ok = mbar_wait(w, bar_dp_free, it & 1))) break;
-          if (L::ALIAS_DQ && !(ok = mbar_wait(w, bar_dq_free, it & 1))) break;
+          if (!(ok = mbar_wait(w, bar_dq_free, it & 1))) break;
           tc_fence_after();
-          issue_dp(it + 1);
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) mma_dp(it + 1, kk);
+          tc_commit(bar_dp_full);
         }
         qt = qn;
       }
@@ -261,24 +312,15 @@ __global__ void __launch_bounds__(320, 1)
     const int key = kt * kTile + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint64_t c2p = f2pack(a.scale_log2, a.scale_log2);
-    const float* stat = reinterpret_cast<const float*>(smem + L::STAT);
-    float* stat_w = reinterpret_cast<float*>(smem + L::STAT);
-    const int t = threadIdx.x;  // 0..255
     bool ok = true;
     int it = 0;
-    int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
-    float pre = qt < n_tiles ? load_stat(a, bh, qt, t) : 0.f;
-    for (; qt < n_tiles; ++it) {
+    for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles; ++it) {
       const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
-      // publish this tile's row statistics and fetch the next tile's early
-      stat_w[(it & 1) * 256 + t] = pre;
-      mbar_arrive(bar_stat(it & 1));
-      if (qn < n_tiles) pre = load_stat(a, bh, qn, t);
-      // buffer it&1 was last read in iteration it-2, which every thread
-      // finished before arriving for iteration it-1
-      if (!(ok = warp_wait(w, bar_stat(it & 1), (it >> 1) & 1))) break;
-      const float* lse2 = stat + (it & 1) * 256 + 64 * g;
-      const float* Dq = stat + (it & 1) * 256 + 128 + 64 * g;
+      // the stage's statistics (staged by the producer with Q and dO)
+      if (!(ok = warp_wait(w, bar_qf(it % NS), (it / NS) & 1))) break;
+      const float* stat = reinterpret_cast<const float*>(smem + L::STAT) + (it % NS) * 256;
+      const float* lse2 = stat + 64 * g;
+      const float* Dq = stat + 128 + 64 * g;
 
       if (!(ok = warp_wait(w, bar_s_full, it & 1))) break;
       tc_fence_after();
@@ -304,8 +346,7 @@ __global__ void __launch_bounds__(320, 1)
         p[c + 1] = p1;
         pk[c / 2] = pack2<F16>(p0, p1);
       }
-      // P^T over the first half of this warpgroup's S^T columns
-      tmem_st32(tmem + L::T_S + lane_off + 64 * g, pk);
+      tmem_st32(tmem + L::pt_write_col(g) + lane_off, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

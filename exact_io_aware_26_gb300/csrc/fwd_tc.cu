@@ -46,15 +46,19 @@ struct FwdLayout {
   static constexpr uint32_t K0 = Q + TILE;          // K stage s at K0 + s * TILE
   static constexpr uint32_t V0 = K0 + NS * TILE;    // V stage s at V0 + s * TILE
   static constexpr uint32_t BAR = V0 + NS * TILE;
-  // barriers: 0 q_full, 1 s_full, 2 p_full, 3 o_done, 4 fin,
-  //           5.. k_full[NS], v_full[NS], k_empty[NS], v_empty[NS]
-  static constexpr uint32_t NBAR = 5 + 4 * NS;
+  // barriers: 0 q_full, 1 s_full, 2 p_full, 3 o_done, 4 fin, 5 s_free,
+  //           6.. k_full[NS], v_full[NS], k_empty[NS], v_empty[NS]
+  static constexpr uint32_t NBAR = 6 + 4 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
-  // TMEM: S at [0, 128) with P~ (16-bit pairs) over its first 64 columns; O at [128, 128 + D)
+  // TMEM (256 columns): S at [0, 128), O at [128, 128 + D).  At d = 64 the 16-bit
+  // P~ has columns of its own, [192, 256), so S_{j+1} can be computed while the
+  // softmax of tile j runs; at d = 128 P~ is written over the first 64 columns of S
+  // and the schedule is serial.
   static constexpr uint32_t TMEM_COLS = 256;
-  static constexpr uint32_t T_S = 0, T_O = 128;
+  static constexpr bool PSEP = (D == 64);
+  static constexpr uint32_t T_S = 0, T_O = 128, T_P = PSEP ? 192 : 0;
 };
 
 __device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
@@ -93,11 +97,12 @@ __global__ void __launch_bounds__(192, 2)
   const int kt_end = a.m.causal ? min(qt + 1, n_tiles) : n_tiles;
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
-  const uint32_t bar_q = bar(0), bar_s = bar(1), bar_p = bar(2), bar_o = bar(3), bar_fin = bar(4);
-  auto bar_kf = [&](int s) { return bar(5 + s); };
-  auto bar_vf = [&](int s) { return bar(5 + NS + s); };
-  auto bar_ke = [&](int s) { return bar(5 + 2 * NS + s); };
-  auto bar_ve = [&](int s) { return bar(5 + 3 * NS + s); };
+  const uint32_t bar_q = bar(0), bar_s = bar(1), bar_p = bar(2), bar_o = bar(3), bar_fin = bar(4),
+                 bar_sfree = bar(5);
+  auto bar_kf = [&](int s) { return bar(6 + s); };
+  auto bar_vf = [&](int s) { return bar(6 + NS + s); };
+  auto bar_ke = [&](int s) { return bar(6 + 2 * NS + s); };
+  auto bar_ve = [&](int s) { return bar(6 + 3 * NS + s); };
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -111,6 +116,7 @@ __global__ void __launch_bounds__(192, 2)
     mbar_init(bar_p, 4);
     mbar_init(bar_o, 1);
     mbar_init(bar_fin, 1);
+    mbar_init(bar_sfree, 4);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_kf(s), 1);
       mbar_init(bar_vf(s), 1);
@@ -187,20 +193,27 @@ __global__ void __launch_bounds__(192, 2)
       if (ok && kt < kt_end) ok = issue_s(0);
       for (int it = 0; ok && kt < kt_end; ++it) {
         const int s = it % NS;
-        // P~ V_j, with P~ read from TMEM (it overwrote the first half of S)
+        const int kn = next_kept(a.m, b, h, qt, kt + 1, kt_end);
+        // d = 64: S_{j+1} as soon as the softmax has copied S_j out of TMEM
+        if (L::PSEP && kn < kt_end) {
+          if (!(ok = mbar_wait(w, bar_sfree, it & 1))) break;
+          if (!(ok = issue_s(it + 1))) break;
+        }
+        // P~ V_j, with P~ read from TMEM
         if (!(ok = mbar_wait(w, bar_p, it & 1))) break;
         if (!(ok = mbar_wait(w, bar_vf(s), (it / NS) & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ts(tO, tS + (uint32_t)kk * 8u, desc_mnmajor(sb + L::V0 + s * L::TILE, kk, kTile),
-                    idO, (it > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tO, tmem + L::T_P + (uint32_t)kk * 8u,
+                    desc_mnmajor(sb + L::V0 + s * L::TILE, kk, kTile), idO,
+                    (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar_o);
         tc_commit(bar_ve(s));
-        // the next score tile goes into the same TMEM columns: MMAs of one
-        // thread execute in issue order, so it lands after P~ V_j has read P~
-        kt = next_kept(a.m, b, h, qt, kt + 1, kt_end);
-        if (kt < kt_end) ok = issue_s(it + 1);
+        // d = 128: the next score tile goes into the columns P~ V_j reads; MMAs
+        // of one thread execute in issue order, so it lands after they are read
+        if (!L::PSEP && kn < kt_end && !(ok = issue_s(it + 1))) break;
+        kt = kn;
       }
       // every MMA issued must have completed before TMEM is released
       tc_commit(bar_fin);
@@ -219,8 +232,9 @@ __global__ void __launch_bounds__(192, 2)
     int it = 0;
     for (int kt = next_kept(a.m, b, h, qt, 0, kt_end); kt < kt_end;
          kt = next_kept(a.m, b, h, qt, kt + 1, kt_end), ++it) {
-      // S_j is complete, and so is every earlier MMA (P~ V_{j-1} included):
-      // O is stable and P~_{j-1} has been consumed
+      // d = 128: S_j is complete, and so is every earlier MMA (P~ V_{j-1}
+      // included), so O is stable and P~_{j-1} has been consumed.  d = 64 waits
+      // for P~ V_{j-1} separately below.
       if (!(ok = warp_wait(w, bar_s, it & 1))) break;
       tc_fence_after();
       float s[kTile];
@@ -232,6 +246,11 @@ __global__ void __launch_bounds__(192, 2)
         tmem_ld64(tS + 64, u);
 #pragma unroll
         for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(u[c]);
+      }
+      if (L::PSEP) {  // S_j is in registers: the MMA warp may compute S_{j+1}
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree);
       }
       // hide keys past the end of the sequence and, on the diagonal tile,
       // keys after the query ("Le masquage causal")
@@ -271,9 +290,15 @@ __global__ void __launch_bounds__(192, 2)
       float sum0, sum1;
       f2unpack(acc, sum0, sum1);
       l = l * alpha + (sum0 + sum1);
-      // P~ over the first 64 columns of S (all of S is already in registers)
-      tmem_st32(tS, plo);
-      tmem_st32(tS + 32, phi);
+      if (L::PSEP && it > 0) {
+        // P~ V_{j-1} must be done: it reads the P~ columns and writes O
+        if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
+        tc_fence_after();
+      }
+      // P~ (16-bit pairs); at d = 128 over the first 64 columns of S, all of
+      // which is already in registers
+      tmem_st32(tmem + L::T_P + lane_off, plo);
+      tmem_st32(tmem + L::T_P + lane_off + 32, phi);
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const uint64_t ap = f2pack(alpha, alpha);
 #pragma unroll
@@ -298,8 +323,9 @@ __global__ void __launch_bounds__(192, 2)
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
     if (ok && it > 0) {
-      // every P~ V up to the (it-2)-th completed before S_{it-1} did, so the
-      // o_done barrier is at most one phase behind the last one
+      // the o_done barrier is at most one phase behind the last P~ V: at d = 64
+      // the loop waited every earlier phase, at d = 128 each earlier P~ V
+      // completed before the next S did
       ok = warp_wait(w, bar_o, (it - 1) & 1);
       tc_fence_after();
       have_o = ok;
