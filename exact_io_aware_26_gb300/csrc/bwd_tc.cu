@@ -205,59 +205,67 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // MMAs that accumulate into one TMEM tile form a dependent chain (~90 cycles
-    // apiece whatever their size), so independent chains are issued interleaved.
+    // The whole warp runs this loop converged (waits are warp-uniform); one
+    // elected lane issues each MMA and commit.  Independent accumulation chains
+    // are issued interleaved.
     // Per query tile i (the next tile's Q/dO sit in the other ring stage):
     //   dV_i (+ S^T_{i+1} interleaved at d = 64, after it at d = 128)
     //   dK_i, dQ_i (+ dP^T_{i+1} at d = 64) interleaved; dP^T_{i+1} after them at d = 128
     // so the next score tile is computed while the compute warps form dS_i, and
     // the next dP^T while they read dQ_i out.
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);  // K-major x K-major
       constexpr uint32_t idKV = idesc_f16(F16, kTile, D, false, true);      // K-major x MN-major
       constexpr uint32_t idQ = idesc_f16(F16, kTile, D, true, true);        // MN-major x MN-major
       constexpr int KS = D / 16;                                            // K steps of S^T, dP^T
       const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
-      auto stage_q = [&](int it) { return sb + L::QS + (uint32_t)(it % NS) * 2u * L::TILE; };
+      // base descriptors; per-step descriptors are one add away
+      const uint64_t dK_k = desc_kmajor_base(sb + L::K), dV_k = desc_kmajor_base(sb + L::V);
+      const uint64_t dK_mn = desc_mnmajor_base(sb + L::K, kTile);
+      const uint64_t dS_k = desc_kmajor_base(sb + L::DST);
+      const uint64_t dS_mn = desc_mnmajor_base(sb + L::DST, kTile);
+      const uint64_t dQ_k0 = desc_kmajor_base(sb + L::QS), dQ_mn0 = desc_mnmajor_base(sb + L::QS, kTile);
+      auto stage_off = [&](int it) { return (uint32_t)(it % NS) * 2u * L::TILE; };
       auto mma_s = [&](int it, int kk) {
-        tc_mma_ss(tS, desc_kmajor(sb + L::K, kk, kTile), desc_kmajor(stage_q(it), kk, kTile), idS,
-                  kk > 0 ? 1u : 0u);
+        tc_mma_ss_elect(tS, dK_k + kmajor_step(kk, kTile),
+                        desc_add(dQ_k0, stage_off(it)) + kmajor_step(kk, kTile), idS, kk > 0 ? 1u : 0u);
       };
       auto mma_dp = [&](int it, int kk) {
-        tc_mma_ss(tDP, desc_kmajor(sb + L::V, kk, kTile),
-                  desc_kmajor(stage_q(it) + L::TILE, kk, kTile), idS, kk > 0 ? 1u : 0u);
+        tc_mma_ss_elect(tDP, dV_k + kmajor_step(kk, kTile),
+                        desc_add(dQ_k0, stage_off(it) + L::TILE) + kmajor_step(kk, kTile), idS,
+                        kk > 0 ? 1u : 0u);
       };
       auto mma_dv = [&](int it, int kk) {
-        tc_mma_ts(tDV, tmem + L::pt_col(kk), desc_mnmajor(stage_q(it) + L::TILE, kk, kTile), idKV,
-                  (it > 0 || kk > 0) ? 1u : 0u);
+        tc_mma_ts_elect(tDV, tmem + L::pt_col(kk),
+                        desc_add(dQ_mn0, stage_off(it) + L::TILE) + mnmajor_step(kk), idKV,
+                        (it > 0 || kk > 0) ? 1u : 0u);
       };
       auto mma_dk = [&](int it, int kk) {
-        tc_mma_ss(tDK, desc_kmajor(sb + L::DST, kk, kTile), desc_mnmajor(stage_q(it), kk, kTile),
-                  idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_mma_ss_elect(tDK, dS_k + kmajor_step(kk, kTile), desc_add(dQ_mn0, stage_off(it)) + mnmajor_step(kk),
+                        idKV, (it > 0 || kk > 0) ? 1u : 0u);
       };
       auto mma_dq = [&](int kk) {
-        tc_mma_ss(tDQ, desc_mnmajor(sb + L::DST, kk, kTile), desc_mnmajor(sb + L::K, kk, kTile),
-                  idQ, kk > 0 ? 1u : 0u);
+        tc_mma_ss_elect(tDQ, dS_mn + mnmajor_step(kk), dK_mn + mnmajor_step(kk), idQ, kk > 0 ? 1u : 0u);
       };
-      bool ok = mbar_wait(w, bar_kv, 0);
+      bool ok = warp_wait(w, bar_kv, 0);
       int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
-      if (ok && qt < n_tiles && (ok = mbar_wait(w, bar_qf(0), 0))) {
+      if (ok && qt < n_tiles && (ok = warp_wait(w, bar_qf(0), 0))) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           mma_s(0, kk);
           mma_dp(0, kk);
         }
-        tc_commit(bar_s_full);
-        tc_commit(bar_dp_full);
+        tc_commit_elect(bar_s_full);
+        tc_commit_elect(bar_dp_full);
       }
       for (int it = 0; ok && qt < n_tiles; ++it) {
         const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
         const bool next = qn < n_tiles;
         // dV += P^T dO_i (P^T from TMEM); at d = 64 with S^T_{i+1} interleaved
-        if (!(ok = mbar_wait(w, bar_p_full, it & 1))) break;
-        if (next && !(ok = mbar_wait(w, bar_qf((it + 1) % NS), ((it + 1) / NS) & 1))) break;
+        if (!(ok = warp_wait(w, bar_p_full, it & 1))) break;
+        if (next && !(ok = warp_wait(w, bar_qf((it + 1) % NS), ((it + 1) / NS) & 1))) break;
         tc_fence_after();
         if (!L::ALIAS && next) {
 #pragma unroll
@@ -274,12 +282,12 @@ __global__ void __launch_bounds__(320, 1)
             for (int kk = 0; kk < KS; ++kk) mma_s(it + 1, kk);
           }
         }
-        if (next) tc_commit(bar_s_full);
+        if (next) tc_commit_elect(bar_s_full);
         // dK += dS^T Q_i, dQ_i = dS K_j (and dP^T_{i+1} at d = 64)
-        if (!(ok = mbar_wait(w, bar_ds_full, it & 1))) break;
-        if (!L::ALIAS && it > 0 && !(ok = mbar_wait(w, bar_dq_free, (it - 1) & 1))) break;
+        if (!(ok = warp_wait(w, bar_ds_full, it & 1))) break;
+        if (!L::ALIAS && it > 0 && !(ok = warp_wait(w, bar_dq_free, (it - 1) & 1))) break;
         const bool dp_now = !L::ALIAS && next;
-        if (dp_now && !(ok = mbar_wait(w, bar_dp_free, it & 1))) break;
+        if (dp_now && !(ok = warp_wait(w, bar_dp_free, it & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -287,23 +295,24 @@ __global__ void __launch_bounds__(320, 1)
           mma_dq(kk);
           if (dp_now && kk < KS) mma_dp(it + 1, kk);
         }
-        tc_commit(bar_ds_free);
-        tc_commit(bar_dq_full);
-        tc_commit(bar_qe(it % NS));
-        if (dp_now) tc_commit(bar_dp_full);
+        tc_commit_elect(bar_ds_free);
+        tc_commit_elect(bar_dq_full);
+        tc_commit_elect(bar_qe(it % NS));
+        if (dp_now) tc_commit_elect(bar_dp_full);
         if (L::ALIAS && next) {
           // dP^T_{i+1} goes over dQ_i: wait until it has been read out
-          if (!(ok = mbar_wait(w, bar_dp_free, it & 1))) break;
-          if (!(ok = mbar_wait(w, bar_dq_free, it & 1))) break;
+          if (!(ok = warp_wait(w, bar_dp_free, it & 1))) break;
+          if (!(ok = warp_wait(w, bar_dq_free, it & 1))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) mma_dp(it + 1, kk);
-          tc_commit(bar_dp_full);
+          tc_commit_elect(bar_dp_full);
         }
         qt = qn;
       }
-      tc_commit(bar_done);
-      mbar_drain(w, bar_done, 0);
+      tc_commit_elect(bar_done);
+      if (lane == 0) mbar_drain(w, bar_done, 0);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ compute warpgroups

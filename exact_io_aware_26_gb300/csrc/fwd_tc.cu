@@ -172,23 +172,29 @@ __global__ void __launch_bounds__(192, 2)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged (waits are warp-uniform); one
+    // elected lane issues each MMA and commit.
+    {
       constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);
       constexpr uint32_t idO = idesc_f16(F16, kTile, D, false, true);
       const uint32_t tS = tmem + L::T_S, tO = tmem + L::T_O;
+      const uint64_t dQ = desc_kmajor_base(sb + L::Q);
+      const uint64_t dK0 = desc_kmajor_base(sb + L::K0);
+      const uint64_t dV0 = desc_mnmajor_base(sb + L::V0, kTile);
       auto issue_s = [&](int it) -> bool {
         const int s = it % NS;
-        if (!mbar_wait(w, bar_kf(s), (it / NS) & 1)) return false;
+        if (!warp_wait(w, bar_kf(s), (it / NS) & 1)) return false;
         tc_fence_after();
+        const uint64_t dK = desc_add(dK0, (uint32_t)s * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tS, desc_kmajor(sb + L::Q, kk, kTile),
-                    desc_kmajor(sb + L::K0 + s * L::TILE, kk, kTile), idS, kk > 0 ? 1u : 0u);
-        tc_commit(bar_s);
-        tc_commit(bar_ke(s));
+          tc_mma_ss_elect(tS, dQ + kmajor_step(kk, kTile), dK + kmajor_step(kk, kTile), idS,
+                          kk > 0 ? 1u : 0u);
+        tc_commit_elect(bar_s);
+        tc_commit_elect(bar_ke(s));
         return true;
       };
-      bool ok = mbar_wait(w, bar_q, 0);
+      bool ok = warp_wait(w, bar_q, 0);
       int kt = next_kept(a.m, b, h, qt, 0, kt_end);
       if (ok && kt < kt_end) ok = issue_s(0);
       for (int it = 0; ok && kt < kt_end; ++it) {
@@ -196,28 +202,29 @@ __global__ void __launch_bounds__(192, 2)
         const int kn = next_kept(a.m, b, h, qt, kt + 1, kt_end);
         // d = 64: S_{j+1} as soon as the softmax has copied S_j out of TMEM
         if (L::PSEP && kn < kt_end) {
-          if (!(ok = mbar_wait(w, bar_sfree, it & 1))) break;
+          if (!(ok = warp_wait(w, bar_sfree, it & 1))) break;
           if (!(ok = issue_s(it + 1))) break;
         }
         // P~ V_j, with P~ read from TMEM
-        if (!(ok = mbar_wait(w, bar_p, it & 1))) break;
-        if (!(ok = mbar_wait(w, bar_vf(s), (it / NS) & 1))) break;
+        if (!(ok = warp_wait(w, bar_p, it & 1))) break;
+        if (!(ok = warp_wait(w, bar_vf(s), (it / NS) & 1))) break;
         tc_fence_after();
+        const uint64_t dV = desc_add(dV0, (uint32_t)s * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ts(tO, tmem + L::T_P + (uint32_t)kk * 8u,
-                    desc_mnmajor(sb + L::V0 + s * L::TILE, kk, kTile), idO,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar_o);
-        tc_commit(bar_ve(s));
+          tc_mma_ts_elect(tO, tmem + L::T_P + (uint32_t)kk * 8u, dV + mnmajor_step(kk), idO,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_elect(bar_o);
+        tc_commit_elect(bar_ve(s));
         // d = 128: the next score tile goes into the columns P~ V_j reads; MMAs
         // of one thread execute in issue order, so it lands after they are read
         if (!L::PSEP && kn < kt_end && !(ok = issue_s(it + 1))) break;
         kt = kn;
       }
       // every MMA issued must have completed before TMEM is released
-      tc_commit(bar_fin);
-      mbar_drain(w, bar_fin, 0);
+      tc_commit_elect(bar_fin);
+      if (lane == 0) mbar_drain(w, bar_fin, 0);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax

@@ -207,6 +207,38 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// The same two MMAs and a commit, issued by one lane elected from a converged
+// warp: the whole warp runs the issuing loop, so descriptors and addresses stay
+// warp-uniform, and the instruction is predicated onto the elected lane.
+// (Issuing from divergent single-lane code costs tens of cycles per MMA.)
+__device__ __forceinline__ void tc_mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with an f32 accumulator.
 //   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16, 1 = bf16);
 //   bit 15 A major (0 = K-major, 1 = MN-major); bit 16 B major;
@@ -243,6 +275,19 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk, int rows)
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk, int rows) {
   return desc_sw128(tile + (uint32_t)kk * 2048u, (uint32_t)(rows * 128), 1024u);
 }
+
+// Base descriptors of a tile and the per-step increments to add to them (the
+// start-address field is the low 14 bits, in 16-byte units, and tiles lie below
+// 256 KiB, so adding an offset never carries out of the field).
+__device__ __forceinline__ uint64_t desc_kmajor_base(uint32_t tile) { return desc_sw128(tile, 16u, 1024u); }
+__device__ __forceinline__ uint64_t desc_mnmajor_base(uint32_t tile, int rows) {
+  return desc_sw128(tile, (uint32_t)(rows * 128), 1024u);
+}
+__host__ __device__ constexpr uint32_t kmajor_step(int kk, int rows) {
+  return (uint32_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint32_t mnmajor_step(int kk) { return (uint32_t)(kk * 2048 >> 4); }
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 // Byte offset of 16-byte chunk `ch` (8 elements) of row `r` inside a tile of
 // 128-byte-swizzled atoms with `rows` rows: chunk ch lives in atom ch / 8.
