@@ -391,27 +391,46 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds_full);
 
-      // dQ_i (TMEM lane = query row) -> fp32 accumulator
+      // dQ_i (TMEM lane = query row) -> fp32 accumulator.  A warp's lanes hold
+      // 32 different rows, so adding straight from registers would touch 32
+      // cache lines per instruction; the slice goes through this warp's own
+      // 4 KiB of the dS^T buffer instead (free: the MMAs that read dS_i are
+      // done), and is added back row by row, 4 lines per instruction.
       if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
       tc_fence_after();
-      {
-        const int qrow = qt * kTile + r;
-        float* dst = a.dQacc + ((size_t)bh * a.N + qrow) * D + g * (D / 2);
-#pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t u[32];
-          tmem_ld32(tmem + L::T_DQ + lane_off + g * (D / 2) + c0, u);
-          if (qrow < a.N) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              red_add_v4(dst + c0 + 4 * v, __uint_as_float(u[4 * v]), __uint_as_float(u[4 * v + 1]),
-                         __uint_as_float(u[4 * v + 2]), __uint_as_float(u[4 * v + 3]));
-          }
-        }
+      uint32_t dq[D / 2];
+      if constexpr (D == 64) {
+        tmem_ld32(tmem + L::T_DQ + lane_off + g * (D / 2), *reinterpret_cast<uint32_t(*)[32]>(dq));
+      } else {
+        tmem_ld64(tmem + L::T_DQ + lane_off + g * (D / 2), *reinterpret_cast<uint32_t(*)[64]>(dq));
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_free);
+      {
+        const uint32_t stg = sb + L::DST + (uint32_t)g * (kTile * 128) + (uint32_t)(warp & 3) * 4096u;
+        const int qbase = qt * kTile + (warp & 3) * 32;
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          // row `lane`, 16-byte chunk x at position x ^ (lane & 7): conflict-free
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            st_shared_v4(stg + (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16), dq[c0 + 4 * x],
+                         dq[c0 + 4 * x + 1], dq[c0 + 4 * x + 2], dq[c0 + 4 * x + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int row = 4 * j + (lane >> 3), x = lane & 7;
+            const uint4 v = ld_shared_v4(stg + (uint32_t)row * 128u + (uint32_t)((x ^ (row & 7)) * 16));
+            const int q = qbase + row;
+            if (q < a.N)
+              red_add_v4(a.dQacc + ((size_t)bh * a.N + q) * D + g * (D / 2) + c0 + 4 * x,
+                         __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                         __uint_as_float(v.w));
+          }
+          __syncwarp();
+        }
+      }
       qt = qn;
     }
     // ------------------------------------------------------------ dK, dV epilogue
