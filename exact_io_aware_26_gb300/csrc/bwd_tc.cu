@@ -13,8 +13,9 @@
 //   dV  += P^T dO_i                      (tcgen05, P^T read from TMEM)
 //   dS^T = P^T * (dP^T - D_i)            (CUDA cores)
 //   dK  += dS^T Q_i                      (tcgen05)
-//   dQ_i = dS K_j                        (tcgen05, read back and added to the
-//                                         fp32 accumulator with vector atomics)
+//   dQ_i = dS K_j                        (tcgen05, read back, staged in shared
+//                                         memory and added to the fp32
+//                                         accumulator by a TMA reduce-add)
 // The score scale is applied once at the end: dK = scale * sum dS^T Q here,
 // dQ = scale * accumulator in the finalize kernel.
 //
@@ -40,10 +41,15 @@ struct BwdLayout {
   static constexpr uint32_t DST = QS + NS * 2 * TILE;  // dS^T, 128 x 128 16-bit
   // per ring stage, the query tile's row statistics: [128] LSE*log2e then [128] D
   static constexpr uint32_t STAT = DST + kTile * kTile * 2;
-  static constexpr uint32_t BAR = STAT + NS * 256 * 4;
+  // dQ staging (fp32, two 128 x 32 boxes): a buffer of its own at d = 64; at
+  // d = 128 shared memory is full and the dS^T buffer doubles as staging
+  static constexpr bool STG_SEP = (D == 64);
+  static constexpr uint32_t STG = STG_SEP ? STAT + NS * 256 * 4 : DST;
+  static constexpr uint32_t BAR = STAT + NS * 256 * 4 + (STG_SEP ? 2 * kTile * 128 : 0);
   // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
-  //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS]
-  static constexpr uint32_t NBAR = 10 + 2 * NS;
+  //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS],
+  //           10+2NS.. stg_full[2], stg_free[2] (dQ staging, one pair per warpgroup)
+  static constexpr uint32_t NBAR = 10 + 2 * NS + 4;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
@@ -83,12 +89,6 @@ __device__ __forceinline__ int next_q(const MaskArgs& m, int b, int h, int qt, i
   return qt;
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
-
 // Row statistics of query q as the compute warps use them: LSE * log2(e), with
 // +inf hiding the row (past the end, or a row that saw no key), and D.
 __device__ __forceinline__ float lse2_of(const BwdArgs& a, int bh, int q) {
@@ -103,7 +103,7 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(320, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const BwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
   using L = BwdLayout<D>;
   constexpr int NS = L::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -123,6 +123,8 @@ __global__ void __launch_bounds__(320, 1)
                  bar_dq_full = bar(7), bar_dq_free = bar(8), bar_done = bar(9);
   auto bar_qf = [&](int s) { return bar(10 + s); };
   auto bar_qe = [&](int s) { return bar(10 + NS + s); };
+  auto bar_stg_full = [&](int g) { return bar(10 + 2 * NS + g); };
+  auto bar_stg_free = [&](int g) { return bar(12 + 2 * NS + g); };
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -141,6 +143,10 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 8);
     mbar_init(bar_done, 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bar_stg_full(g), 4);
+      mbar_init(bar_stg_free(g), 1);
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_qf(s), 1 + 32);  // the TMA transaction arrival + every producer lane
       mbar_init(bar_qe(s), 1);
@@ -316,72 +322,108 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ------------------------------------------------------------ compute warpgroups
+    // Software-pipelined per query tile i:  dS_i | P_{i+1} | dQ_i, so that the
+    // exponentials of the next tile run while the tensor core computes dK_i,
+    // dQ_i and dP^T_{i+1}.
     const int g = warp >> 2;                 // 0: query columns 0-63, 1: 64-127
     const int r = (warp & 3) * 32 + lane;    // key row in the tile = TMEM lane
     const int key = kt * kTile + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint64_t c2p = f2pack(a.scale_log2, a.scale_log2);
-    bool ok = true;
-    int it = 0;
-    for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles; ++it) {
-      const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
+    const bool rows_out = __any_sync(0xffffffffu, key >= a.N);  // a tail key tile
+    // dQ staging: this warpgroup's 16 KiB box (this warp's 4 KiB of it), laid
+    // out as the 128-byte-swizzled box {32, 128} of tmdQ
+    const uint32_t stg_wg = sb + L::STG + (uint32_t)g * (kTile * 128);
+    const uint32_t stg = stg_wg + (uint32_t)(warp & 3) * 4096u;
+    // A staging round's TMA reduce reads the box asynchronously.  The box is
+    // released lazily: only when it is about to be written again does the
+    // warpgroup's first lane wait for that read and arrive on stg_free, which
+    // the other warps of the warpgroup wait for.
+    bool pend = false;  // (first warp of the warpgroup) a round is not yet released
+    int nstg = 0;       // staging rounds of this warpgroup
+    auto stg_acquire = [&]() -> bool {
+      if (nstg == 0) return true;
+      if ((warp & 3) == 0) {
+        if (lane == 0 && pend) {
+          bulk_wait_group_read0();
+          mbar_arrive(bar_stg_free(g));
+        }
+        pend = false;
+        __syncwarp();
+      }
+      return warp_wait(w, bar_stg_free(g), (nstg - 1) & 1);
+    };
+    auto stat = [&](int it) {
+      return reinterpret_cast<const float*>(smem + L::STAT) + (it % NS) * 256;
+    };
+    float p[64];
+    // S^T -> P^T: fp32 in p[] for dS, 16-bit into TMEM for dV; then p_full
+    auto p_phase = [&](int it, int qtile) -> bool {
       // the stage's statistics (staged by the producer with Q and dO)
-      if (!(ok = warp_wait(w, bar_qf(it % NS), (it / NS) & 1))) break;
-      const float* stat = reinterpret_cast<const float*>(smem + L::STAT) + (it % NS) * 256;
-      const float* lse2 = stat + 64 * g;
-      const float* Dq = stat + 128 + 64 * g;
-
-      if (!(ok = warp_wait(w, bar_s_full, it & 1))) break;
+      if (!warp_wait(w, bar_qf(it % NS), (it / NS) & 1)) return false;
+      if (!warp_wait(w, bar_s_full, it & 1)) return false;
       tc_fence_after();
-      float p[64];
       {
         uint32_t u[64];
         tmem_ld64(tmem + L::T_S + lane_off + 64 * g, u);
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(u[c]);
       }
-      const int q0 = qt * kTile + 64 * g;
-      const bool row_out = key >= a.N;
-      const bool diag = a.m.causal && qt == kt;
+      const float* lse2 = stat(it) + 64 * g;
+      const int q0 = qtile * kTile + 64 * g;
+      const bool diag = a.m.causal && qtile == kt;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         float x0, x1;
         f2unpack(ffma2(f2pack(p[c], p[c + 1]), c2p, f2pack(-lse2[c], -lse2[c + 1])), x0, x1);
-        float p0 = ex2(x0), p1 = ex2(x1);
-        if (row_out || (diag && q0 + c < key)) p0 = 0.f;
-        if (row_out || (diag && q0 + c + 1 < key)) p1 = 0.f;
-        p[c] = p0;
-        p[c + 1] = p1;
-        pk[c / 2] = pack2<F16>(p0, p1);
+        p[c] = ex2(x0);
+        p[c + 1] = ex2(x1);
       }
+      if (rows_out || diag) {  // warp-uniform: only tail and diagonal tiles mask
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (key >= a.N || (diag && q0 + c < key)) p[c] = 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
       tmem_st32(tmem + L::pt_write_col(g) + lane_off, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_full);
-
+      return true;
+    };
+    bool ok = true;
+    int it = 0;
+    int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
+    if (qt < n_tiles) ok = p_phase(0, qt);
+    for (; ok && qt < n_tiles; ++it) {
+      const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
+      // ---- dS_i = P_i * (dP_i - D)
       if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
       tc_fence_after();
-      float ds[64];
+      uint32_t pk[32];
       {
         uint32_t u[64];
         tmem_ld64(tmem + L::T_DP + lane_off + 64 * g, u);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dp_free);
+        const float* Dq = stat(it) + 128 + 64 * g;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) ds[c] = __uint_as_float(u[c]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dp_free);
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float y0, y1;
-        f2unpack(fmul2(f2pack(p[c], p[c + 1]),
-                       fadd2(f2pack(ds[c], ds[c + 1]), f2pack(-Dq[c], -Dq[c + 1]))),
-                 y0, y1);
-        pk[c / 2] = pack2<F16>(y0, y1);
+        for (int c = 0; c < 64; c += 2) {
+          float y0, y1;
+          f2unpack(fmul2(f2pack(p[c], p[c + 1]),
+                         fadd2(f2pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
+                               f2pack(-Dq[c], -Dq[c + 1]))),
+                   y0, y1);
+          pk[c / 2] = pack2<F16>(y0, y1);
+        }
       }
       if (it > 0 && !(ok = warp_wait(w, bar_ds_free, (it - 1) & 1))) break;
+      // at d = 128 the last dQ reduction must have finished reading this region
+      if (!L::STG_SEP && !(ok = stg_acquire())) break;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         st_shared_v4(sb + L::DST + sw128_chunk_offset(r, 8 * g + ch, kTile), pk[ch * 4 + 0],
@@ -391,11 +433,10 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds_full);
 
-      // dQ_i (TMEM lane = query row) -> fp32 accumulator.  A warp's lanes hold
-      // 32 different rows, so adding straight from registers would touch 32
-      // cache lines per instruction; the slice goes through this warp's own
-      // 4 KiB of the dS^T buffer instead (free: the MMAs that read dS_i are
-      // done), and is added back row by row, 4 lines per instruction.
+      // ---- P of the next query tile, while dK_i, dQ_i, dP^T_{i+1} run
+      if (qn < n_tiles && !(ok = p_phase(it + 1, qn))) break;
+
+      // ---- dQ_i (TMEM lane = query row) -> fp32 accumulator by TMA reduce-add
       if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
       tc_fence_after();
       uint32_t dq[D / 2];
@@ -407,32 +448,33 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_free);
-      {
-        const uint32_t stg = sb + L::DST + (uint32_t)g * (kTile * 128) + (uint32_t)(warp & 3) * 4096u;
-        const int qbase = qt * kTile + (warp & 3) * 32;
 #pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          // row `lane`, 16-byte chunk x at position x ^ (lane & 7): conflict-free
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        if (!(ok = stg_acquire())) break;
+        // row `lane` of this warp's 32, 16-byte chunk x at x ^ (row & 7)
 #pragma unroll
-          for (int x = 0; x < 8; ++x)
-            st_shared_v4(stg + (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16), dq[c0 + 4 * x],
-                         dq[c0 + 4 * x + 1], dq[c0 + 4 * x + 2], dq[c0 + 4 * x + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int row = 4 * j + (lane >> 3), x = lane & 7;
-            const uint4 v = ld_shared_v4(stg + (uint32_t)row * 128u + (uint32_t)((x ^ (row & 7)) * 16));
-            const int q = qbase + row;
-            if (q < a.N)
-              red_add_v4(a.dQacc + ((size_t)bh * a.N + q) * D + g * (D / 2) + c0 + 4 * x,
-                         __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                         __uint_as_float(v.w));
+        for (int x = 0; x < 8; ++x)
+          st_shared_v4(stg + (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16), dq[c0 + 4 * x],
+                       dq[c0 + 4 * x + 1], dq[c0 + 4 * x + 2], dq[c0 + 4 * x + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_stg_full(g));
+        if ((warp & 3) == 0) {
+          // the warpgroup's first warp adds the staged 128 x 32 tile into dQacc
+          if (!(ok = warp_wait(w, bar_stg_full(g), nstg & 1))) break;
+          if (lane == 0) {
+            tma_reduce_add_3d(&tmdQ, stg_wg, g * (D / 2) + c0, qt * kTile, bh);
+            bulk_commit_group();
           }
+          pend = true;
           __syncwarp();
         }
+        ++nstg;
       }
+      if (!ok) break;
       qt = qn;
     }
+    if ((warp & 3) == 0 && lane == 0) bulk_wait_group0();  // dQ reductions fully done
     // ------------------------------------------------------------ dK, dV epilogue
     bool have = false;
     if (ok) {
@@ -488,7 +530,7 @@ cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  kern<<<(unsigned)(n_tiles * a.B * a.H), 320, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], a);
+  kern<<<(unsigned)(n_tiles * a.B * a.H), 320, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], a);
   return cudaGetLastError();
 }
 

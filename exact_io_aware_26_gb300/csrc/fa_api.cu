@@ -139,6 +139,28 @@ fa_status encode_bhnd(CUtensorMap* m, const void* ptr, const fa_params* p) {
   return FA_OK;
 }
 
+// The fp32 dQ accumulator [B*H][N][d] as a 3-D TMA map {d, N, B*H}; box
+// {32, 128, 1} (128-byte rows), 128-byte swizzle; rows past N are not written.
+fa_status encode_dqacc(CUtensorMap* m, const float* ptr, const fa_params* p) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_err("cuTensorMapEncodeTiled is not available from the driver");
+    return FA_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)p->d, (cuuint64_t)p->N, (cuuint64_t)p->B * p->H};
+  const cuuint64_t strides[2] = {(cuuint64_t)p->d * 4, (cuuint64_t)p->N * p->d * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_err("cuTensorMapEncodeTiled (dQ accumulator) failed (CUresult %d)", (int)r);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 MaskArgs mask_args(const fa_params* p) {
   MaskArgs m;
   m.causal = p->causal ? 1 : 0;
@@ -347,11 +369,12 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
   a.dK = dK;
   a.dV = dV;
   a.rep = make_report(st);
-  CUtensorMap tm[4];
+  CUtensorMap tm[5];
   FA_TRY(encode_bhnd(&tm[0], Q, p));
   FA_TRY(encode_bhnd(&tm[1], K, p));
   FA_TRY(encode_bhnd(&tm[2], V, p));
   FA_TRY(encode_bhnd(&tm[3], dO, p));
+  FA_TRY(encode_dqacc(&tm[4], a.dQacc, p));
   cudaError_t e = launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) {
     set_err("backward main kernel not available in this build");
