@@ -34,7 +34,7 @@ constexpr int kTile = 128;
 template <int D>
 struct BwdLayout {
   static constexpr uint32_t TILE = kTile * D * 2;
-  static constexpr int NS = 2;                         // Q/dO ring depth
+  static constexpr int NS = (D == 64) ? 3 : 2;         // Q/dO ring depth
   static constexpr uint32_t K = 0;
   static constexpr uint32_t V = TILE;
   static constexpr uint32_t QS = 2 * TILE;             // stage s: Q at QS + 2s TILE, dO after it
@@ -48,8 +48,7 @@ struct BwdLayout {
   static constexpr uint32_t BAR = STAT + NS * 256 * 4 + (STG_SEP ? 2 * kTile * 128 : 0);
   // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
   //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS],
-  //           10+2NS.. stg_full[2], stg_free[2] (dQ staging, one pair per warpgroup)
-  static constexpr uint32_t NBAR = 10 + 2 * NS + 4;
+  static constexpr uint32_t NBAR = 10 + 2 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
@@ -123,8 +122,7 @@ __global__ void __launch_bounds__(320, 1)
                  bar_dq_full = bar(7), bar_dq_free = bar(8), bar_done = bar(9);
   auto bar_qf = [&](int s) { return bar(10 + s); };
   auto bar_qe = [&](int s) { return bar(10 + NS + s); };
-  auto bar_stg_full = [&](int g) { return bar(10 + 2 * NS + g); };
-  auto bar_stg_free = [&](int g) { return bar(12 + 2 * NS + g); };
+
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -143,10 +141,6 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 8);
     mbar_init(bar_done, 1);
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(bar_stg_full(g), 4);
-      mbar_init(bar_stg_free(g), 1);
-    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_qf(s), 1 + 32);  // the TMA transaction arrival + every producer lane
       mbar_init(bar_qe(s), 1);
@@ -331,27 +325,18 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint64_t c2p = f2pack(a.scale_log2, a.scale_log2);
     const bool rows_out = __any_sync(0xffffffffu, key >= a.N);  // a tail key tile
-    // dQ staging: this warpgroup's 16 KiB box (this warp's 4 KiB of it), laid
-    // out as the 128-byte-swizzled box {32, 128} of tmdQ
-    const uint32_t stg_wg = sb + L::STG + (uint32_t)g * (kTile * 128);
-    const uint32_t stg = stg_wg + (uint32_t)(warp & 3) * 4096u;
-    // A staging round's TMA reduce reads the box asynchronously.  The box is
-    // released lazily: only when it is about to be written again does the
-    // warpgroup's first lane wait for that read and arrive on stg_free, which
-    // the other warps of the warpgroup wait for.
-    bool pend = false;  // (first warp of the warpgroup) a round is not yet released
-    int nstg = 0;       // staging rounds of this warpgroup
-    auto stg_acquire = [&]() -> bool {
-      if (nstg == 0) return true;
-      if ((warp & 3) == 0) {
-        if (lane == 0 && pend) {
-          bulk_wait_group_read0();
-          mbar_arrive(bar_stg_free(g));
-        }
-        pend = false;
+    // dQ staging: this warp's 4 KiB, laid out as the 128-byte-swizzled box
+    // {32 columns, 32 rows} of tmdQ.  Each warp reduces its own box, so no warp
+    // waits for another.  The TMA reduce reads the box asynchronously; the box
+    // is released lazily, when it is about to be written again.
+    const uint32_t stg = sb + L::STG + (uint32_t)g * (kTile * 128) + (uint32_t)(warp & 3) * 4096u;
+    bool pend = false;  // a reduce may still be reading the box
+    auto stg_acquire = [&]() {
+      if (pend) {
+        if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
+        pend = false;
       }
-      return warp_wait(w, bar_stg_free(g), (nstg - 1) & 1);
     };
     auto stat = [&](int it) {
       return reinterpret_cast<const float*>(smem + L::STAT) + (it % NS) * 256;
@@ -423,7 +408,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (it > 0 && !(ok = warp_wait(w, bar_ds_free, (it - 1) & 1))) break;
       // at d = 128 the last dQ reduction must have finished reading this region
-      if (!L::STG_SEP && !(ok = stg_acquire())) break;
+      if (!L::STG_SEP) stg_acquire();
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         st_shared_v4(sb + L::DST + sw128_chunk_offset(r, 8 * g + ch, kTile), pk[ch * 4 + 0],
@@ -450,7 +435,7 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) mbar_arrive(bar_dq_free);
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        if (!(ok = stg_acquire())) break;
+        stg_acquire();
         // row `lane` of this warp's 32, 16-byte chunk x at x ^ (row & 7)
 #pragma unroll
         for (int x = 0; x < 8; ++x)
@@ -458,23 +443,16 @@ __global__ void __launch_bounds__(320, 1)
                        dq[c0 + 4 * x + 1], dq[c0 + 4 * x + 2], dq[c0 + 4 * x + 3]);
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_stg_full(g));
-        if ((warp & 3) == 0) {
-          // the warpgroup's first warp adds the staged 128 x 32 tile into dQacc
-          if (!(ok = warp_wait(w, bar_stg_full(g), nstg & 1))) break;
-          if (lane == 0) {
-            tma_reduce_add_3d(&tmdQ, stg_wg, g * (D / 2) + c0, qt * kTile, bh);
-            bulk_commit_group();
-          }
-          pend = true;
-          __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tmdQ, stg, g * (D / 2) + c0, qt * kTile + (warp & 3) * 32, bh);
+          bulk_commit_group();
         }
-        ++nstg;
+        pend = true;
       }
       if (!ok) break;
       qt = qn;
     }
-    if ((warp & 3) == 0 && lane == 0) bulk_wait_group0();  // dQ reductions fully done
+    if (lane == 0) bulk_wait_group0();  // this warp's dQ reductions fully done
     // ------------------------------------------------------------ dK, dV epilogue
     bool have = false;
     if (ok) {

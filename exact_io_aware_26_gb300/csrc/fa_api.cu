@@ -140,7 +140,8 @@ fa_status encode_bhnd(CUtensorMap* m, const void* ptr, const fa_params* p) {
 }
 
 // The fp32 dQ accumulator [B*H][N][d] as a 3-D TMA map {d, N, B*H}; box
-// {32, 128, 1} (128-byte rows), 128-byte swizzle; rows past N are not written.
+// {32, 32, 1} (128-byte rows, one warp's slice), 128-byte swizzle; rows past N
+// are not written.
 fa_status encode_dqacc(CUtensorMap* m, const float* ptr, const fa_params* p) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
@@ -149,7 +150,7 @@ fa_status encode_dqacc(CUtensorMap* m, const float* ptr, const fa_params* p) {
   }
   const cuuint64_t dims[3] = {(cuuint64_t)p->d, (cuuint64_t)p->N, (cuuint64_t)p->B * p->H};
   const cuuint64_t strides[2] = {(cuuint64_t)p->d * 4, (cuuint64_t)p->N * p->d * 4};
-  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t box[3] = {32, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
