@@ -269,10 +269,17 @@ __global__ void __launch_bounds__(192, 2)
         for (int c = 0; c < kTile; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx = fmax3(s[0], s[1], s[2]);
+      // row max as four independent chains (a single chain of dependent maxes
+      // would expose its latency: only two softmax warps share a sub-partition)
+      float m4[4];
 #pragma unroll
-      for (int c = 3; c + 1 < kTile; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
-      mx = fmaxf(mx, s[kTile - 1]);
+      for (int j = 0; j < 4; ++j) {
+        float mj = fmax3(s[32 * j], s[32 * j + 1], s[32 * j + 2]);
+#pragma unroll
+        for (int c = 3; c + 1 < 32; c += 2) mj = fmax3(mj, s[32 * j + c], s[32 * j + c + 1]);
+        m4[j] = fmaxf(mj, s[32 * j + 31]);
+      }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       const float m_tile = mx * c2;
       float alpha = 1.f;
       if (m_tile > m_use + kRescaleThr) {
@@ -281,22 +288,25 @@ __global__ void __launch_bounds__(192, 2)
       }
       const float mneg = (m_use == -INFINITY) ? 0.f : -m_use;
       const uint64_t c2p = f2pack(c2, c2), mp = f2pack(mneg, mneg);
-      uint64_t acc = f2pack(0.f, 0.f);
+      uint64_t acc[4] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
       uint32_t plo[32], phi[32];  // P~ as 16-bit pairs: keys [0, 64) and [64, 128)
 #pragma unroll
       for (int c = 0; c < kTile; c += 2) {
         float x0, x1;
         f2unpack(ffma2(f2pack(s[c], s[c + 1]), c2p, mp), x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
-        acc = fadd2(acc, f2pack(p0, p1));
+        acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], f2pack(p0, p1));  // four independent sums
         if (c < 64)
           plo[c / 2] = pack2<F16>(p0, p1);
         else
           phi[(c - 64) / 2] = pack2<F16>(p0, p1);
       }
-      float sum0, sum1;
-      f2unpack(acc, sum0, sum1);
-      l = l * alpha + (sum0 + sum1);
+      float sum0, sum1, sum2, sum3, sum4, sum5, sum6, sum7;
+      f2unpack(acc[0], sum0, sum1);
+      f2unpack(acc[1], sum2, sum3);
+      f2unpack(acc[2], sum4, sum5);
+      f2unpack(acc[3], sum6, sum7);
+      l = l * alpha + (((sum0 + sum1) + (sum2 + sum3)) + ((sum4 + sum5) + (sum6 + sum7)));
       if (L::PSEP && it > 0) {
         // P~ V_{j-1} must be done: it reads the P~ columns and writes O
         if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
