@@ -186,13 +186,19 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(dst + L::TILE + c * (kTile * 128), &tmdO, bar_qf(s), c * 64, qt * kTile, bh);
         }
       }
+      // negated, as the compute warps use them: -LSE*log2(e) and -D
       float* st = reinterpret_cast<float*>(smem + L::STAT) + s * 256;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = lane * 4 + j, q = qt * kTile + row;
-        st[row] = lse2_of(a, bh, q);
-        st[128 + row] = d_of(a, bh, q);
-      }
+      float4 l4, d4;
+      l4.x = -lse2_of(a, bh, qt * kTile + lane * 4 + 0);
+      l4.y = -lse2_of(a, bh, qt * kTile + lane * 4 + 1);
+      l4.z = -lse2_of(a, bh, qt * kTile + lane * 4 + 2);
+      l4.w = -lse2_of(a, bh, qt * kTile + lane * 4 + 3);
+      d4.x = -d_of(a, bh, qt * kTile + lane * 4 + 0);
+      d4.y = -d_of(a, bh, qt * kTile + lane * 4 + 1);
+      d4.z = -d_of(a, bh, qt * kTile + lane * 4 + 2);
+      d4.w = -d_of(a, bh, qt * kTile + lane * 4 + 3);
+      reinterpret_cast<float4*>(st)[lane] = l4;
+      reinterpret_cast<float4*>(st + 128)[lane] = d4;
       mbar_arrive(bar_qf(s));
       ++it;
     }
@@ -210,7 +216,8 @@ __global__ void __launch_bounds__(320, 1)
     // are issued interleaved.
     // Per query tile i (the next tile's Q/dO sit in the other ring stage):
     //   dV_i (+ S^T_{i+1} interleaved at d = 64, after it at d = 128)
-    //   dK_i, dQ_i (+ dP^T_{i+1} at d = 64) interleaved; dP^T_{i+1} after them at d = 128
+    //   dP^T_{i+1} (d = 64; at d = 128 it goes over dQ_i and follows it)
+    //   dK_i, dQ_i interleaved
     // so the next score tile is computed while the compute warps form dS_i, and
     // the next dP^T while they read dQ_i out.
     {
@@ -283,22 +290,27 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         if (next) tc_commit_elect(bar_s_full);
-        // dK += dS^T Q_i, dQ_i = dS K_j (and dP^T_{i+1} at d = 64)
+        // d = 64: dP^T_{i+1} as soon as the compute warps have read dP^T_i (before
+        // they form dS_i), so that the next dS finds it ready
+        if (!L::ALIAS && next) {
+          if (!(ok = warp_wait(w, bar_dp_free, it & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) mma_dp(it + 1, kk);
+          tc_commit_elect(bar_dp_full);
+        }
+        // dK += dS^T Q_i, dQ_i = dS K_j
         if (!(ok = warp_wait(w, bar_ds_full, it & 1))) break;
         if (!L::ALIAS && it > 0 && !(ok = warp_wait(w, bar_dq_free, (it - 1) & 1))) break;
-        const bool dp_now = !L::ALIAS && next;
-        if (dp_now && !(ok = warp_wait(w, bar_dp_free, it & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           mma_dk(it, kk);
           mma_dq(kk);
-          if (dp_now && kk < KS) mma_dp(it + 1, kk);
         }
         tc_commit_elect(bar_ds_free);
         tc_commit_elect(bar_dq_full);
         tc_commit_elect(bar_qe(it % NS));
-        if (dp_now) tc_commit_elect(bar_dp_full);
         if (L::ALIAS && next) {
           // dP^T_{i+1} goes over dQ_i: wait until it has been read out
           if (!(ok = warp_wait(w, bar_dp_free, it & 1))) break;
@@ -354,16 +366,20 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(u[c]);
       }
-      const float* lse2 = stat(it) + 64 * g;
+      const float4* nl4 = reinterpret_cast<const float4*>(stat(it) + 64 * g);  // -LSE*log2(e)
       const int q0 = qtile * kTile + 64 * g;
       const bool diag = a.m.causal && qtile == kt;
       uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float x0, x1;
-        f2unpack(ffma2(f2pack(p[c], p[c + 1]), c2p, f2pack(-lse2[c], -lse2[c + 1])), x0, x1);
+      for (int c = 0; c < 64; c += 4) {
+        const float4 nl = nl4[c / 4];
+        float x0, x1, x2, x3;
+        f2unpack(ffma2(f2pack(p[c], p[c + 1]), c2p, f2pack(nl.x, nl.y)), x0, x1);
+        f2unpack(ffma2(f2pack(p[c + 2], p[c + 3]), c2p, f2pack(nl.z, nl.w)), x2, x3);
         p[c] = ex2(x0);
         p[c + 1] = ex2(x1);
+        p[c + 2] = ex2(x2);
+        p[c + 3] = ex2(x3);
       }
       if (rows_out || diag) {  // warp-uniform: only tail and diagonal tiles mask
 #pragma unroll
@@ -395,15 +411,19 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_dp_free);
-        const float* Dq = stat(it) + 128 + 64 * g;
+        const float4* nd4 = reinterpret_cast<const float4*>(stat(it) + 128 + 64 * g);  // -D
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float y0, y1;
+        for (int c = 0; c < 64; c += 4) {
+          const float4 nd = nd4[c / 4];
+          float y0, y1, y2, y3;
           f2unpack(fmul2(f2pack(p[c], p[c + 1]),
-                         fadd2(f2pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
-                               f2pack(-Dq[c], -Dq[c + 1]))),
+                         fadd2(f2pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), f2pack(nd.x, nd.y))),
                    y0, y1);
+          f2unpack(fmul2(f2pack(p[c + 2], p[c + 3]),
+                         fadd2(f2pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), f2pack(nd.z, nd.w))),
+                   y2, y3);
           pk[c / 2] = pack2<F16>(y0, y1);
+          pk[c / 2 + 1] = pack2<F16>(y2, y3);
         }
       }
       if (it > 0 && !(ok = warp_wait(w, bar_ds_free, (it - 1) & 1))) break;
