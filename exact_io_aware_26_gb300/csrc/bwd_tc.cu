@@ -212,14 +212,12 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop converged (waits are warp-uniform); one
-    // elected lane issues each MMA and commit.  Independent accumulation chains
-    // are issued interleaved.
-    // Per query tile i (the next tile's Q/dO sit in the other ring stage):
-    //   dV_i (+ S^T_{i+1} interleaved at d = 64, after it at d = 128)
-    //   dP^T_{i+1} (d = 64; at d = 128 it goes over dQ_i and follows it)
-    //   dK_i, dQ_i interleaved
+    // elected lane issues each MMA and commit.
+    // Per query tile i (the next tile's Q/dO sit in another ring stage):
+    //   d = 64:  S^T_{i+1}, dV_i, dP^T_{i+1}, then dQ_i, dK_i
+    //   d = 128: dV_i, S^T_{i+1} (over P^T), then dQ_i, dK_i, dP^T_{i+1} (over dQ_i)
     // so the next score tile is computed while the compute warps form dS_i, and
-    // the next dP^T while they read dQ_i out.
+    // dQ_i is ready for them right after the next tile's exponentials.
     {
       constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);  // K-major x K-major
       constexpr uint32_t idKV = idesc_f16(F16, kTile, D, false, true);      // K-major x MN-major
@@ -270,46 +268,52 @@ __global__ void __launch_bounds__(320, 1)
       for (int it = 0; ok && qt < n_tiles; ++it) {
         const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
         const bool next = qn < n_tiles;
-        // dV += P^T dO_i (P^T from TMEM); at d = 64 with S^T_{i+1} interleaved
+        // Within each group the MMA the compute warps wait for next goes first
+        // (MMAs execute in issue order).
         if (!(ok = warp_wait(w, bar_p_full, it & 1))) break;
         if (next && !(ok = warp_wait(w, bar_qf((it + 1) % NS), ((it + 1) / NS) & 1))) break;
         tc_fence_after();
-        if (!L::ALIAS && next) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            mma_dv(it, kk);
-            if (kk < KS) mma_s(it + 1, kk);
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) mma_dv(it, kk);
-          // at d = 128 S^T_{i+1} overwrites P^T: issue order puts it after dV
+        if (!L::ALIAS) {
+          // S^T_{i+1}, then dV += P^T dO_i (P^T has columns of its own)
           if (next) {
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) mma_s(it + 1, kk);
+            tc_commit_elect(bar_s_full);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) mma_dv(it, kk);
+          // dP^T_{i+1} as soon as the compute warps have read dP^T_i (before
+          // they form dS_i), so that the next dS finds it ready
+          if (next) {
+            if (!(ok = warp_wait(w, bar_dp_free, it & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) mma_dp(it + 1, kk);
+            tc_commit_elect(bar_dp_full);
+          }
+        } else {
+          // d = 128: S^T_{i+1} overwrites P^T, so it follows dV in issue order
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) mma_dv(it, kk);
+          if (next) {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) mma_s(it + 1, kk);
+            tc_commit_elect(bar_s_full);
           }
         }
-        if (next) tc_commit_elect(bar_s_full);
-        // d = 64: dP^T_{i+1} as soon as the compute warps have read dP^T_i (before
-        // they form dS_i), so that the next dS finds it ready
-        if (!L::ALIAS && next) {
-          if (!(ok = warp_wait(w, bar_dp_free, it & 1))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < KS; ++kk) mma_dp(it + 1, kk);
-          tc_commit_elect(bar_dp_full);
-        }
-        // dK += dS^T Q_i, dQ_i = dS K_j
+        // dQ_i = dS K_j (read out next by the compute warps), then dK += dS^T Q_i
         if (!(ok = warp_wait(w, bar_ds_full, it & 1))) break;
         if (!L::ALIAS && it > 0 && !(ok = warp_wait(w, bar_dq_free, (it - 1) & 1))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_dk(it, kk);
-          mma_dq(kk);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk) mma_dq(kk);
+        // at d = 64 dQ_i may be read out while dK_i runs; at d = 128 the dQ staging
+        // reuses the dS^T buffer that dK_i reads, so dq_full waits for dK_i too
+        if (L::STG_SEP) tc_commit_elect(bar_dq_full);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) mma_dk(it, kk);
+        if (!L::STG_SEP) tc_commit_elect(bar_dq_full);
         tc_commit_elect(bar_ds_free);
-        tc_commit_elect(bar_dq_full);
         tc_commit_elect(bar_qe(it % NS));
         if (L::ALIAS && next) {
           // dP^T_{i+1} goes over dQ_i: wait until it has been read out
