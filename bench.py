@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--fwd-splits", type=int, default=0,
+                    help="key-range slices of the forward (0: the library's choice for this GPU)")
     return ap.parse_args()
 
 
@@ -186,9 +188,9 @@ def heads_for_seconds(w, target_s: float) -> int:
     return max(1, min(n, w.B * w.H))
 
 
-def config_of(w):
+def config_of(w, fwd_splits=None):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
-            "causal": list(w.causal), "block_mask_p": w.mask_p,
+            "causal": list(w.causal), "block_mask_p": w.mask_p, "fwd_splits": fwd_splits,
             "passes": "fwd+bwd per causal setting",
             "l2": "flushed between steps (256 MiB write outside the timed events)"}
 
@@ -244,6 +246,14 @@ def measured_traffic(workload: str, kernel: str):
         return None
 
 
+def fwd(fa, r, q, k, v, o, lse, stream):
+    """The forward of one run: fa_fwd, or fa_fwd_split when the run uses slices."""
+    if r["splits"] > 1:
+        fa.fwd_split_raw(r["p"], q, k, v, o, lse, r["splits"], r["fws"], stream)
+    else:
+        fa.fwd_raw(r["p"], q, k, v, o, lse, stream)
+
+
 def run_e2e(fa, inp, runs, flops, steps, dev, stream):
     """Same metric with host buffers.  Every step copies its inputs from pinned host
     memory, runs the path, and copies every output back to pinned host memory.  The
@@ -279,7 +289,7 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream):
                 stream.wait_event(ev_d2h[i - 2])  # outputs of set bsel copied out
             x = dev_in[bsel]
             for r, o in zip(runs, dev_out[bsel]):
-                fa.fwd_raw(r["p"], x["q"], x["k"], x["v"], o["o"], o["lse"], stream)
+                fwd(fa, r, x["q"], x["k"], x["v"], o["o"], o["lse"], stream)
                 fa.bwd_preprocess(r["p"], o["o"], x["do"], r["ws"], stream)
                 fa.bwd_main(r["p"], x["q"], x["k"], x["v"], x["do"], o["lse"], o["dk"], o["dv"],
                             r["ws"], stream)
@@ -339,7 +349,11 @@ def main():
         p, keep = fa.make_params(q, w.scale, c, mask, w.mask_block)
         ws = torch.empty(int(lib.fa_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8,
                          device=dev)
-        runs.append(dict(causal=c, p=p, keep=keep, o=torch.empty_like(q),
+        splits = args.fwd_splits if args.fwd_splits > 0 else fa.num_splits(p)
+        fws = None
+        if splits > 1:
+            fws = torch.empty(fa.split_workspace_bytes(p, splits), dtype=torch.uint8, device=dev)
+        runs.append(dict(causal=c, p=p, keep=keep, splits=splits, fws=fws, o=torch.empty_like(q),
                          lse=torch.empty(q.shape[:3], dtype=torch.float32, device=dev),
                          dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
                          ws=ws))
@@ -350,7 +364,7 @@ def main():
         for i, r in enumerate(runs):
             if ev_fwd is not None:
                 ev_fwd[i][0].record(stream)
-            fa.fwd_raw(r["p"], q, k, v, r["o"], r["lse"], stream)
+            fwd(fa, r, q, k, v, r["o"], r["lse"], stream)
             if ev_fwd is not None:
                 ev_fwd[i][1].record(stream)
             fa.bwd_preprocess(r["p"], r["o"], do, r["ws"], stream)
@@ -428,7 +442,8 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": 1000.0 * total_s / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic", "config": config_of(w),
+            "dtype": w.dtype, "data": "synthetic",
+            "config": config_of(w, [r["splits"] for r in runs]),
             "breakdown": {
                 "fwd_tflops": fwd_tflops, "bwd_main_tflops": achieved,
                 "fwd_frac_of_bf16_peak": fwd_tflops / peak,
@@ -442,7 +457,8 @@ def main():
                                          if peak_src == "measured" else "fallback bf16 burst"),
                          "traffic": measured_traffic(w.name, "bwd_main"),
                          "algorithmic_flops_per_launch": bwd_flops / launches},
-            "clocks": clk, "e2e": e2e, "gpu_launches": launches * 4,
+            "clocks": clk, "e2e": e2e,
+            "gpu_launches": K * sum(4 + (r["splits"] > 1) for r in runs),
             "cpu_baseline": cpu}), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -1,6 +1,7 @@
 // fa_api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument
 // validation, TMA tensor-map encoding, the device status word, and the kernel
 // launches.  Everything here is host code except the status word.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -307,6 +308,8 @@ fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V
   a.m = mask_args(p);
   a.O = O;
   a.LSE = LSE;
+  a.n_splits = 1;
+  a.split_tiles = (p->N + 127) / 128;
   a.rep = make_report(st);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -321,6 +324,127 @@ fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V
     e = launch_fwd_tc(a, p->d, p->dtype == FA_F16, tm, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return FA_OK;
+}
+
+namespace {
+// key tiles per slice and the number of non-empty slices for a request of
+// `splits` slices over n_tiles key tiles
+void split_shape(int n_tiles, int splits, int* per, int* used) {
+  *per = (n_tiles + splits - 1) / splits;
+  *used = (n_tiles + *per - 1) / *per;
+}
+
+fa_status check_splits(const fa_params* p, int num_splits) {
+  const int n_tiles = (p->N + 127) / 128;
+  if (num_splits < 1 || num_splits > FA_MAX_SPLITS || num_splits > n_tiles) {
+    set_err("num_splits out of range [1, min(FA_MAX_SPLITS, ceil(N / 128))]");
+    return FA_ERR_INVALID;
+  }
+  if (num_splits > 1 && p->dtype == FA_F32) {
+    set_err("split forward needs fp16 or bf16");
+    return FA_ERR_UNSUPPORTED;
+  }
+  return FA_OK;
+}
+}  // namespace
+
+int fa_fwd_num_splits(const fa_params* p, int num_sms) {
+  if (fa_check(p, 0) != FA_OK) return 0;
+  if (p->dtype == FA_F32) return 1;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        num_sms <= 0) {
+      cudaGetLastError();
+      return 1;
+    }
+  }
+  // Model: two CTAs share an SM, so a launch runs in waves of 2 * num_sms
+  // CTAs, and a wave lasts about as long as its CTAs' key tiles plus two tiles
+  // for loading Q, writing the partial result and merging it.  A grid that
+  // fills the first wave is left whole (splitting it would only trade a tail
+  // for the partials' extra traffic); otherwise pick the split count with the
+  // lowest modelled time (ties to fewer splits).
+  const long long n_tiles = (p->N + 127) / 128;
+  const long long ctas = (long long)p->B * p->H * n_tiles;
+  const long long slots = 2LL * num_sms;
+  if (ctas >= slots) return 1;
+  const int max_s = (int)std::min<long long>(FA_MAX_SPLITS, n_tiles);
+  int best = 1;
+  long long best_cost = -1;
+  for (int sp = 1; sp <= max_s; ++sp) {
+    int per = 0, used = 0;
+    split_shape((int)n_tiles, sp, &per, &used);
+    if (used != sp) continue;  // a split count that leaves a slice empty
+    const long long waves = (ctas * sp + slots - 1) / slots;
+    const long long cost = waves * (per + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = sp;
+    }
+  }
+  return best;
+}
+
+size_t fa_fwd_split_workspace_size(const fa_params* p, int num_splits) {
+  if (fa_check(p, 0) != FA_OK || check_splits(p, num_splits) != FA_OK) return 0;
+  if (num_splits == 1) return 0;
+  const size_t rows = (size_t)p->B * p->H * p->N;
+  return align256((size_t)num_splits * rows * (size_t)p->d * 4) + align256((size_t)num_splits * rows * 4);
+}
+
+fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
+                       float* LSE, int num_splits, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  FA_TRY(fa_check(p, 0));
+  FA_TRY(check_splits(p, num_splits));
+  if (num_splits == 1) return fa_fwd(p, Q, K, V, O, LSE, stream);
+  FA_TRY(need16(Q, "Q"));
+  FA_TRY(need16(K, "K"));
+  FA_TRY(need16(V, "V"));
+  FA_TRY(need16(O, "O"));
+  if (!LSE || !aligned(LSE, 4)) {
+    set_err("LSE is NULL or misaligned");
+    return FA_ERR_INVALID;
+  }
+  const size_t need = fa_fwd_split_workspace_size(p, num_splits);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) {
+    set_err("split workspace is NULL, not 256-byte aligned or too small");
+    return FA_ERR_WORKSPACE;
+  }
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  const int n_tiles = (p->N + 127) / 128;
+  int per = 0, used = 0;
+  split_shape(n_tiles, num_splits, &per, &used);
+  const size_t rows = (size_t)p->B * p->H * p->N;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = p->B;
+  a.H = p->H;
+  a.N = p->N;
+  a.scale = p->scale;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.m = mask_args(p);
+  a.O = O;
+  a.LSE = LSE;
+  a.n_splits = used;
+  a.split_tiles = per;
+  a.Opart = static_cast<float*>(workspace);
+  a.LSEpart = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       align256((size_t)num_splits * rows * (size_t)p->d * 4));
+  a.rep = make_report(st);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tm[3];
+  FA_TRY(encode_bhnd(&tm[0], Q, p));
+  FA_TRY(encode_bhnd(&tm[1], K, p));
+  FA_TRY(encode_bhnd(&tm[2], V, p));
+  cudaError_t e = launch_fwd_tc(a, p->d, p->dtype == FA_F16, tm, s);
+  if (e != cudaSuccess) return cuda_fail(e, "split forward launch");
+  e = launch_fwd_merge(a, p->d, p->dtype == FA_F16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
   return FA_OK;
 }
 

@@ -91,10 +91,14 @@ __global__ void __launch_bounds__(192, 2)
 
   const int BH = a.B * a.H;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const int qt = n_tiles - 1 - (int)(blockIdx.x / BH);  // heaviest (causal) tiles first
-  const int bh = (int)(blockIdx.x % BH);
+  const int split = (int)(blockIdx.x % a.n_splits);
+  const int tile = (int)(blockIdx.x / a.n_splits);
+  const int qt = n_tiles - 1 - tile / BH;  // heaviest (causal) tiles first
+  const int bh = tile % BH;
   const int b = bh / a.H, h = bh % a.H;
-  const int kt_end = a.m.causal ? min(qt + 1, n_tiles) : n_tiles;
+  // this CTA's key tiles: [kt_begin, kt_end)
+  const int kt_begin = split * a.split_tiles;
+  const int kt_end = min(a.m.causal ? min(qt + 1, n_tiles) : n_tiles, kt_begin + a.split_tiles);
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
   const uint32_t bar_q = bar(0), bar_s = bar(1), bar_p = bar(2), bar_o = bar(3), bar_fin = bar(4),
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(192, 2)
       for (int c = 0; c < D / 64; ++c)
         tma_load_3d(sb + L::Q + c * (kTile * 128), &tmQ, bar_q, c * 64, qt * kTile, bh);
       int nk = 0, nv = 0;  // K and V copies issued
-      for (int kt = next_kept(a.m, b, h, qt, 0, kt_end); kt < kt_end;
+      for (int kt = next_kept(a.m, b, h, qt, kt_begin, kt_end); kt < kt_end;
            kt = next_kept(a.m, b, h, qt, kt + 1, kt_end)) {
         const int s = nk % NS;
         const uint32_t ph = ((nk / NS) - 1) & 1;
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(192, 2)
         return true;
       };
       bool ok = warp_wait(w, bar_q, 0);
-      int kt = next_kept(a.m, b, h, qt, 0, kt_end);
+      int kt = next_kept(a.m, b, h, qt, kt_begin, kt_end);
       if (ok && kt < kt_end) ok = issue_s(0);
       for (int it = 0; ok && kt < kt_end; ++it) {
         const int s = it % NS;
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(192, 2)
     float l = 0.f;            // running sum of P~ (fp32)
     bool ok = true;
     int it = 0;
-    for (int kt = next_kept(a.m, b, h, qt, 0, kt_end); kt < kt_end;
+    for (int kt = next_kept(a.m, b, h, qt, kt_begin, kt_end); kt < kt_end;
          kt = next_kept(a.m, b, h, qt, kt + 1, kt_end), ++it) {
       // d = 128: S_j is complete, and so is every earlier MMA (P~ V_{j-1}
       // included), so O is stable and P~_{j-1} has been consumed.  d = 64 waits
@@ -348,29 +352,52 @@ __global__ void __launch_bounds__(192, 2)
       have_o = ok;
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    if (row < a.N && ok) {
-      a.LSE[(size_t)bh * a.N + row] =
-          (l > 0.f) ? (m_use + __log2f(l)) * 0.693147180559945309f : -INFINITY;
-    }
-    uint16_t* Orow = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D;
+    const float lse = (l > 0.f) ? (m_use + __log2f(l)) * 0.693147180559945309f : -INFINITY;
+    if (a.n_splits == 1) {
+      if (row < a.N && ok) a.LSE[(size_t)bh * a.N + row] = lse;
+      uint16_t* Orow = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      if (have_o) {
-        tmem_ld32(tO + c0, o);
-      } else {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        if (have_o) {
+          tmem_ld32(tO + c0, o);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (row < a.N && ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 q;
+            q.x = pack2<F16>(__uint_as_float(o[v * 8 + 0]) * inv_l, __uint_as_float(o[v * 8 + 1]) * inv_l);
+            q.y = pack2<F16>(__uint_as_float(o[v * 8 + 2]) * inv_l, __uint_as_float(o[v * 8 + 3]) * inv_l);
+            q.z = pack2<F16>(__uint_as_float(o[v * 8 + 4]) * inv_l, __uint_as_float(o[v * 8 + 5]) * inv_l);
+            q.w = pack2<F16>(__uint_as_float(o[v * 8 + 6]) * inv_l, __uint_as_float(o[v * 8 + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(Orow + c0 + v * 8) = q;
+          }
+        }
       }
-      if (row < a.N && ok) {
+    } else {
+      // a slice of the key range: normalised fp32 partial O and its LSE (an
+      // empty slice gives O = 0, LSE = -inf and weighs nothing in the merge)
+      const size_t prow = (size_t)split * BH * a.N + (size_t)bh * a.N + row;
+      if (row < a.N && ok) a.LSEpart[prow] = lse;
+      float* Prow = a.Opart + prow * D;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 q;
-          q.x = pack2<F16>(__uint_as_float(o[v * 8 + 0]) * inv_l, __uint_as_float(o[v * 8 + 1]) * inv_l);
-          q.y = pack2<F16>(__uint_as_float(o[v * 8 + 2]) * inv_l, __uint_as_float(o[v * 8 + 3]) * inv_l);
-          q.z = pack2<F16>(__uint_as_float(o[v * 8 + 4]) * inv_l, __uint_as_float(o[v * 8 + 5]) * inv_l);
-          q.w = pack2<F16>(__uint_as_float(o[v * 8 + 6]) * inv_l, __uint_as_float(o[v * 8 + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(Orow + c0 + v * 8) = q;
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        if (have_o) {
+          tmem_ld32(tO + c0, o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (row < a.N && ok) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(Prow + c0 + v * 4) =
+                make_float4(__uint_as_float(o[v * 4 + 0]) * inv_l, __uint_as_float(o[v * 4 + 1]) * inv_l,
+                            __uint_as_float(o[v * 4 + 2]) * inv_l, __uint_as_float(o[v * 4 + 3]) * inv_l);
         }
       }
     }
@@ -391,12 +418,68 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const unsigned grid = (unsigned)(n_tiles * a.B * a.H);
+  const unsigned grid = (unsigned)(n_tiles * a.B * a.H * a.n_splits);
   kern<<<grid, 192, L::BYTES, s>>>(tm[0], tm[1], tm[2], a);
   return cudaGetLastError();
 }
 
+// Merge of the key-range slices of every query row with the running-statistics
+// merge of "Rastreamento Incremental do Softmax" (FlashAttention reading guide),
+// in log-sum-exp form: LSE = log sum_s exp(LSE_s) and O = sum_s exp(LSE_s - LSE) O_s,
+// each O_s normalised by its own slice's sum.  One warp per row; lane j holds
+// columns [j * D/32, (j + 1) * D/32).
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
+  constexpr int C = D / 32;
+  const long long rows = (long long)a.B * a.H * a.N;
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long r = warp0; r < rows; r += nwarps) {
+    float m = -INFINITY;
+    for (int sp = 0; sp < a.n_splits; ++sp) m = fmaxf(m, a.LSEpart[(size_t)sp * rows + r]);
+    float acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
+    float sum = 0.f;
+    if (m != -INFINITY) {
+      for (int sp = 0; sp < a.n_splits; ++sp) {
+        const float lse = a.LSEpart[(size_t)sp * rows + r];
+        const float wgt = ex2((lse - m) * 1.4426950408889634f);  // 0 for an empty slice
+        sum += wgt;
+        const float* src = a.Opart + ((size_t)sp * rows + r) * D + lane * C;
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] = fmaf(wgt, src[c], acc[c]);
+      }
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(a.O) + r * D + lane * C;
+#pragma unroll
+    for (int c = 0; c < C; c += 2) {
+      const uint32_t pk = pack2<F16>(acc[c] * inv, acc[c + 1] * inv);
+      *reinterpret_cast<uint32_t*>(dst + c) = pk;
+    }
+    if (lane == 0) a.LSE[r] = sum > 0.f ? m + __logf(sum) : -INFINITY;
+  }
+}
+
+template <int D, bool F16>
+cudaError_t merge_t(const FwdArgs& a, cudaStream_t s) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long rows = (long long)a.B * a.H * a.N;
+  long long blocks = (rows + 7) / 8;  // 8 warps per block
+  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
+  fwd_merge_kernel<D, F16><<<(unsigned)blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_fwd_merge(const FwdArgs& a, int d, bool f16, cudaStream_t s) {
+  if (d == 64) return f16 ? merge_t<64, true>(a, s) : merge_t<64, false>(a, s);
+  return f16 ? merge_t<128, true>(a, s) : merge_t<128, false>(a, s);
+}
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, int d, bool f16, const CUtensorMap* tm, cudaStream_t s) {
   if (d == 64) return f16 ? launch_t<64, true>(a, tm, s) : launch_t<64, false>(a, tm, s);

@@ -42,6 +42,13 @@ struct FwdArgs {
   MaskArgs m;
   void* O;
   float* LSE;
+  // split key range: with n_splits > 1, CTA split s covers key tiles
+  // [s * split_tiles, (s + 1) * split_tiles) and writes its normalised fp32
+  // partial O and its LSE to Opart / LSEpart [s] instead of O / LSE
+  int n_splits;
+  int split_tiles;
+  float* Opart;    // [n_splits][B*H*N][d]
+  float* LSEpart;  // [n_splits][B*H*N]
   Report rep;
 };
 
@@ -66,6 +73,7 @@ cudaError_t launch_fwd_f32(const FwdArgs& a, int d, const float* Q, const float*
                            const float* V, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);
+cudaError_t launch_fwd_merge(const FwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);

@@ -98,3 +98,53 @@ def test_library_links_no_cuda_driver_at_load_time():
     import subprocess
     out = subprocess.run(["ldd", fa.LIB_PATH], capture_output=True, text=True).stdout
     assert "libcuda.so" not in out
+
+
+def test_split_count_model(lib):
+    """fa_fwd_num_splits with an explicit SM count is host arithmetic: few query
+    tiles get split, a full grid does not, and the count always divides the key
+    tiles into non-empty slices."""
+    one_head = _p(B=1, H=1, N=8192, d=64, dtype=fa.FA_F16)
+    s = fa.num_splits(one_head, 152)
+    assert s > 1
+    per = -(-64 // s)
+    assert -(-64 // per) == s
+    assert fa.num_splits(_p(B=4, H=12, N=2048), 152) == 1
+    assert fa.num_splits(_p(N=23400, H=12), 152) == 1
+    assert fa.num_splits(_p(N=128), 152) == 1          # one key tile: nothing to split
+    assert fa.num_splits(_p(N=8192, dtype=fa.FA_F32), 152) == 1
+    assert fa.num_splits(_p(d=32), 152) == 0
+    for n in (256, 1000, 4096, 65536):
+        s = fa.num_splits(_p(N=n), 152)
+        t = -(-n // 128)
+        assert 1 <= s <= min(t, 64)
+        per = -(-t // s)
+        assert -(-t // per) == s
+
+
+def test_split_workspace_size(lib):
+    up = lambda x: (x + 255) // 256 * 256
+    p = _p(B=1, H=1, N=8192, d=64)
+    rows = 8192
+    assert fa.split_workspace_bytes(p, 1) == 0
+    assert fa.split_workspace_bytes(p, 4) == up(4 * rows * 64 * 4) + up(4 * rows * 4)
+    assert fa.split_workspace_bytes(p, 64) > 0
+    assert fa.split_workspace_bytes(p, 65) == 0    # above FA_MAX_SPLITS
+    assert fa.split_workspace_bytes(p, 0) == 0
+    assert fa.split_workspace_bytes(_p(N=300), 4) == 0   # more slices than key tiles
+
+
+def test_split_invalid_calls_return_before_any_launch(lib):
+    p = _p(N=1024)
+    ok_ptr = 1 << 20  # never dereferenced: every call below fails validation first
+    need = fa.split_workspace_bytes(p, 4)
+    args = [ok_ptr] * 5
+    call = lambda q, s, ws, n: lib.fa_fwd_split(ctypes.byref(q), *args, s, ws, n, None)
+    assert call(p, 0, ok_ptr, need) == fa.FA_ERR_INVALID
+    assert call(p, 9, ok_ptr, need) == fa.FA_ERR_INVALID       # 8 key tiles
+    assert call(p, 4, ok_ptr, need - 1) == fa.FA_ERR_WORKSPACE
+    assert call(p, 4, None, need) == fa.FA_ERR_WORKSPACE
+    assert call(p, 4, ok_ptr + 16, need) == fa.FA_ERR_WORKSPACE
+    assert call(_p(N=1024, dtype=fa.FA_F32), 4, ok_ptr, need) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_split(ctypes.byref(p), ok_ptr + 2, ok_ptr, ok_ptr, ok_ptr, ok_ptr, 4,
+                            ok_ptr, need, None) == fa.FA_ERR_INVALID
