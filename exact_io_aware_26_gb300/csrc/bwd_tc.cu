@@ -48,7 +48,8 @@ struct BwdLayout {
   static constexpr uint32_t BAR = STAT + NS * 256 * 4 + (STG_SEP ? 2 * kTile * 128 : 0);
   // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
   //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS],
-  static constexpr uint32_t NBAR = 10 + 2 * NS;
+  //           10+2NS pt_free (d = 64: dV_i has finished reading P^T_i)
+  static constexpr uint32_t NBAR = 11 + 2 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(320, 1)
                  bar_dq_full = bar(7), bar_dq_free = bar(8), bar_done = bar(9);
   auto bar_qf = [&](int s) { return bar(10 + s); };
   auto bar_qe = [&](int s) { return bar(10 + NS + s); };
+  const uint32_t bar_pt_free = bar(10 + 2 * NS);
 
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 8);
     mbar_init(bar_done, 1);
+    mbar_init(bar_pt_free, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_qf(s), 1 + 32);  // the TMA transaction arrival + every producer lane
       mbar_init(bar_qe(s), 1);
@@ -282,6 +285,9 @@ __global__ void __launch_bounds__(320, 1)
           }
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) mma_dv(it, kk);
+          // P^T_{i+1} may be written once dV_i has read P^T_i; s_full (committed
+          // before dV_i) does not cover that
+          tc_commit_elect(bar_pt_free);
           // dP^T_{i+1} as soon as the compute warps have read dP^T_i (before
           // they form dS_i), so that the next dS finds it ready
           if (next) {
@@ -392,6 +398,14 @@ __global__ void __launch_bounds__(320, 1)
       }
 #pragma unroll
       for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
+      if constexpr (!L::ALIAS) {
+        // d = 64: P^T has one buffer; dV of the previous tile must be done with it
+        // (at d = 128 P^T goes over S^T, which s_full already orders after dV)
+        if (it > 0) {
+          if (!warp_wait(w, bar_pt_free, (it - 1) & 1)) return false;
+          tc_fence_after();
+        }
+      }
       tmem_st32(tmem + L::pt_write_col(g) + lane_off, pk);
       tmem_st_wait();
       tc_fence_before();
