@@ -293,7 +293,7 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream):
                 fa.bwd_preprocess(r["p"], o["o"], x["do"], r["ws"], stream)
                 fa.bwd_main(r["p"], x["q"], x["k"], x["v"], x["do"], o["lse"], o["dk"], o["dv"],
                             r["ws"], stream)
-                fa.bwd_finalize(r["p"], o["dq"], r["ws"], stream)
+                fa.bwd_finalize(r["p"], o["dq"], o["dk"], o["dv"], r["ws"], stream)
             ev_comp[i].record(stream)
             s_d2h.wait_event(ev_comp[i])
             with torch.cuda.stream(s_d2h):
@@ -373,7 +373,7 @@ def main():
             fa.bwd_main(r["p"], q, k, v, do, r["lse"], r["dk"], r["dv"], r["ws"], stream)
             if ev_main is not None:
                 ev_main[i][1].record(stream)
-            fa.bwd_finalize(r["p"], r["dq"], r["ws"], stream)
+            fa.bwd_finalize(r["p"], r["dq"], r["dk"], r["dv"], r["ws"], stream)
 
     W = max(args.warmup, 3)
     for _ in range(W):

@@ -77,7 +77,8 @@ def load() -> ctypes.CDLL:
         "fa_bwd": (I, [PP, P, P, P, P, P, P, P, P, P, P, S, P]),
         "fa_bwd_preprocess": (I, [PP, P, P, P, S, P]),
         "fa_bwd_main": (I, [PP, P, P, P, P, P, P, P, P, S, P]),
-        "fa_bwd_finalize": (I, [PP, P, P, S, P]),
+        "fa_bwd_finalize": (I, [PP, P, P, P, P, S, P]),
+        "fa_set_bwd_ctas": (I, [I]),
         "fa_get_status": (I, [P]),
         "fa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
         "fa_selftest_timeout": (I, [P]),
@@ -252,9 +253,14 @@ def bwd_main(p: FaParams, q, k, v, do, lse, dk, dv, workspace, stream=None):
                               _stream(stream)), "fa_bwd_main")
 
 
-def bwd_finalize(p: FaParams, dq, workspace, stream=None):
-    _check(load().fa_bwd_finalize(ctypes.byref(p), _ptr(dq), _ptr(workspace), workspace.numel(),
-                                  _stream(stream)), "fa_bwd_finalize")
+def bwd_finalize(p: FaParams, dq, dk, dv, workspace, stream=None):
+    _check(load().fa_bwd_finalize(ctypes.byref(p), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "fa_bwd_finalize")
+
+
+def set_bwd_ctas(n: int) -> int:
+    """fa_set_bwd_ctas: cap on the persistent backward CTAs (0 = one per SM)."""
+    return int(load().fa_set_bwd_ctas(int(n)))
 
 
 def fwd_raw(p: FaParams, q, k, v, o, lse, stream=None):

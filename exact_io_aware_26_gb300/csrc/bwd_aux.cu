@@ -4,9 +4,13 @@
 //   preprocess: D_i = sum_k dO_ik O_ik (fp32) for every row, and the fp32 dQ
 //               accumulator zeroed.  D_i equals sum_j P_ij dP_ij, the row term
 //               of dS = P * (dP - D), because O_i = sum_j P_ij v_j.
-//   finalize:   dQ = scale * accumulator, rounded to the 16-bit output type.
+//   finalize:   dQ = scale * accumulator, rounded to the 16-bit output type;
+//               and, after a persistent (stream-K) main kernel, dK and dV of
+//               every key tile that several CTAs shared: the sum of their fp32
+//               partial slots (bwd_sched.cuh).
 // Both are plain streaming kernels: 16-byte vector loads/stores, coalesced,
 // grid sized to a multiple of the SM count.
+#include "bwd_sched.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -60,6 +64,65 @@ __global__ void __launch_bounds__(256) bwd_finalize_kernel(const float4* __restr
   }
 }
 
+// Block `boundary` looks at the boundary between CTA c = boundary and c + 1 of
+// the main kernel; if a key tile is shared there (sched_shared), the block
+// adds the partial slots of the CTAs that share it and writes its dK, dV.
+template <int D, bool F16>
+__device__ void fixup_key_tile(const BwdArgs& a, int boundary) {
+  const int BH = a.B * a.H;
+  const Sched s = make_sched((a.N + 127) / 128, BH, a.m.causal, a.G);
+  const int c = boundary;
+  int bh, kt, c_last, fs;
+  if (!sched_shared(s, c, bh, kt, c_last, fs)) return;
+  const float* first_slot = a.slots + (size_t)fs * (2 * 128 * D);
+  constexpr int PER = 2 * 128 * D / 4;  // float4 per slot ([dV | dK])
+  for (int e = threadIdx.x; e < PER; e += blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(first_slot)[e];
+    for (int cc = c + 1; cc <= c_last; ++cc) {
+      const float4 v = reinterpret_cast<const float4*>(a.slots + (size_t)(2 * cc) * (2 * 128 * D))[e];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int f = e * 4;                 // first float of the four
+    const int which = f / (128 * D);     // 0: dV, 1: dK
+    const int row = (f / D) % 128;
+    const int col = f % D;
+    const int key = kt * 128 + row;
+    if (key >= a.N) continue;
+    const float mul = which == 0 ? 1.f : a.scale;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? a.dV : a.dK) + ((size_t)bh * a.N + key) * D + col;
+    uint2 o;
+    o.x = pack2<F16>(acc.x * mul, acc.y * mul);
+    o.y = pack2<F16>(acc.z * mul, acc.w * mul);
+    *reinterpret_cast<uint2*>(dst) = o;
+  }
+}
+
+// Blocks [0, dq_blocks) convert the dQ accumulator; blocks after them, one per
+// CTA boundary of a persistent main kernel, finish the shared key tiles.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_finalize_fixup_kernel(const BwdArgs a, int dq_blocks) {
+  if ((int)blockIdx.x >= dq_blocks) {
+    fixup_key_tile<D, F16>(a, (int)blockIdx.x - dq_blocks);
+    return;
+  }
+  const long long n8 = (long long)a.B * a.H * a.N * D / 8;
+  const float4* acc = reinterpret_cast<const float4*>(a.dQacc);
+  uint4* dQ = reinterpret_cast<uint4*>(a.dQ);
+  const long long nthreads = (long long)dq_blocks * blockDim.x;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += nthreads) {
+    const float4 x = acc[2 * t], y = acc[2 * t + 1];
+    uint4 o;
+    o.x = pack2<F16>(x.x * a.scale, x.y * a.scale);
+    o.y = pack2<F16>(x.z * a.scale, x.w * a.scale);
+    o.z = pack2<F16>(y.x * a.scale, y.y * a.scale);
+    o.w = pack2<F16>(y.z * a.scale, y.w * a.scale);
+    dQ[t] = o;
+  }
+}
+
 __global__ void wait_selftest_kernel(Report rep) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_cta;
@@ -95,6 +158,12 @@ cudaError_t pre_t(const BwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int D, bool F16>
+cudaError_t fin_fixup_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
+  bwd_finalize_fixup_kernel<D, F16><<<dq_blocks + a.G - 1, 256, 0, s>>>(a, dq_blocks);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_t s) {
@@ -105,6 +174,11 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_
 cudaError_t launch_bwd_finalize(const BwdArgs& a, int d, bool f16, cudaStream_t s) {
   const long long n8 = (long long)a.B * a.H * a.N * d / 8;
   const int grid = grid_for(n8, 256);
+  if (a.G > 1) {
+    // persistent main kernel: the same launch also finishes the shared key tiles
+    if (d == 64) return f16 ? fin_fixup_t<64, true>(a, grid, s) : fin_fixup_t<64, false>(a, grid, s);
+    return f16 ? fin_fixup_t<128, true>(a, grid, s) : fin_fixup_t<128, false>(a, grid, s);
+  }
   if (f16)
     bwd_finalize_kernel<true><<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(a.dQacc),
                                                    reinterpret_cast<uint4*>(a.dQ), a.scale, n8);

@@ -1,0 +1,127 @@
+// bwd_sched.cuh -- how the backward main kernel splits its work over CTAs.
+//
+// The unit of work is one (key tile, query tile) iteration.  Without a block
+// mask the iterations of all heads are numbered head-major, then by key tile,
+// then by query tile (causal: the query tiles from the key tile's own index
+// up), and cut into G contiguous ranges of nearly equal length, one per
+// persistent CTA (G about the SM count).  A range may begin or end inside a
+// key tile: that key tile's dK, dV are then written by each CTA that touched
+// it as fp32 partial sums into a slot of its own (slot 2c for CTA c's first
+// range piece, 2c + 1 for its last), and the finalize kernel adds the slots.
+// With a block mask the kept query tiles are known on the device only, and
+// each CTA takes one whole key tile instead.
+#pragma once
+#include <cmath>
+#include <cstdint>
+
+#ifndef __CUDACC__  // host-only compilers (the schedule is also checked on the CPU)
+#define __host__
+#define __device__
+#endif
+
+namespace fa {
+
+struct Sched {
+  int n;        // tiles per sequence (ceil(N / 128))
+  int causal;   // query tiles before the key tile are skipped
+  int G;        // CTAs
+  long long W;  // iterations per head
+  long long T;  // iterations in all
+};
+
+// Most CTAs a stream-K launch uses (and that the workspace holds slots for).
+constexpr int kBwdMaxCtas = 160;
+
+__host__ __device__ inline long long sched_per_head(int n, int causal) {
+  return causal ? (long long)n * (n + 1) / 2 : (long long)n * n;
+}
+// iterations of the key tiles before kt in one head
+__host__ __device__ inline long long sched_before(int kt, int n, int causal) {
+  return causal ? (long long)kt * n - (long long)kt * (kt - 1) / 2 : (long long)kt * n;
+}
+// query tiles key tile kt visits
+__host__ __device__ inline int sched_visited(int kt, int n, int causal) {
+  return causal ? n - kt : n;
+}
+__host__ __device__ inline Sched make_sched(int n, int BH, int causal, int G) {
+  Sched s;
+  s.n = n;
+  s.causal = causal;
+  s.G = G;
+  s.W = sched_per_head(n, causal);
+  s.T = s.W * BH;
+  return s;
+}
+// first iteration of CTA c (c = G gives T)
+__host__ __device__ inline long long sched_start(const Sched& s, int c) {
+  return (long long)c * s.T / s.G;
+}
+// head, key tile and index among the key tile's visited query tiles of iteration g
+__host__ __device__ inline void sched_locate(const Sched& s, long long g, int& bh, int& kt, int& j) {
+  bh = (int)(g / s.W);
+  const long long r = g - (long long)bh * s.W;
+  if (!s.causal) {
+    kt = (int)(r / s.n);
+    j = (int)(r - (long long)kt * s.n);
+    return;
+  }
+  // largest k with sched_before(k) <= r: a root of k^2 - (2n+1) k + 2r, then
+  // corrected by exact integer comparisons
+  const double b2 = 2.0 * s.n + 1.0;
+  int k = (int)((b2 - sqrt(b2 * b2 - 8.0 * (double)r)) * 0.5);
+  if (k < 0) k = 0;
+  if (k > s.n - 1) k = s.n - 1;
+  while (k > 0 && sched_before(k, s.n, 1) > r) --k;
+  while (k + 1 < s.n && sched_before(k + 1, s.n, 1) <= r) ++k;
+  kt = k;
+  j = (int)(r - sched_before(k, s.n, 1));
+}
+
+// One piece of a CTA's range: key tile kt of head bh, query tiles [q_first, q_end).
+struct Seg {
+  int bh, kt, q_first, q_end;
+  int slot;  // -1: the whole key tile (dK, dV written directly); else the partial-sum slot
+};
+
+// The next piece of CTA c's range [g, g_end); advances g.
+__host__ __device__ inline bool sched_next(const Sched& s, int c, long long& g, long long g_end,
+                                           bool& first, Seg& sg) {
+  if (g >= g_end) return false;
+  int bh, kt, j;
+  sched_locate(s, g, bh, kt, j);
+  const int vis = sched_visited(kt, s.n, s.causal);
+  const long long left = g_end - g;
+  const int j_end = (long long)(vis - j) <= left ? vis : j + (int)left;
+  const int qbase = s.causal ? kt : 0;
+  sg.bh = bh;
+  sg.kt = kt;
+  sg.q_first = qbase + j;
+  sg.q_end = qbase + j_end;
+  sg.slot = (j == 0 && j_end == vis) ? -1 : (first ? 2 * c : 2 * c + 1);
+  g += j_end - j;
+  first = false;
+  return true;
+}
+
+// The key tile that CTAs c and c + 1 share, if their boundary falls inside one
+// and is the first boundary inside it: its head and key tile, the last CTA that
+// shares it, and CTA c's slot for it (its last piece 2c + 1, or its first 2c
+// when its range starts at the key tile).  CTAs c + 1 .. c_last hold it in
+// their first slots, 2c'.
+__host__ __device__ inline bool sched_shared(const Sched& s, int c, int& bh, int& kt, int& c_last,
+                                             int& first_slot) {
+  const long long p = sched_start(s, c + 1);
+  int j;
+  sched_locate(s, p, bh, kt, j);
+  if (j == 0) return false;  // the boundary is at a key tile's start
+  const long long u_start = p - j;
+  const long long u_end = u_start + sched_visited(kt, s.n, s.causal);
+  const long long c_start = sched_start(s, c);
+  if (c_start > u_start) return false;  // an earlier boundary lies inside the key tile
+  c_last = c + 1;
+  while (c_last + 1 < s.G && sched_start(s, c_last + 1) < u_end) ++c_last;
+  first_slot = c_start < u_start ? 2 * c + 1 : 2 * c;
+  return true;
+}
+
+}  // namespace fa

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "bwd_sched.cuh"
 #include "internal.h"
 
 using namespace fa;
@@ -39,11 +40,13 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<uint32_t> g_epoch{0};
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+std::atomic<int> g_bwd_ctas{0};  // cap on persistent backward CTAs; 0 = one per SM
 
 constexpr int kMaxDev = 64;
 struct DevState {
   bool checked = false;
   bool supported = false;
+  int sms = 0;
   DevStatus* st = nullptr;
 };
 DevState g_dev[kMaxDev];
@@ -67,6 +70,8 @@ fa_status device_ready(DevStatus** st) {
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
     d.supported = (major == 10 && minor == 3);
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
     if (d.supported) {
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_status)) != cudaSuccess)
@@ -81,6 +86,14 @@ fa_status device_ready(DevStatus** st) {
   if (!d.supported) return FA_ERR_DEVICE;
   *st = d.st;
   return FA_OK;
+}
+
+// SM count of the current device (after device_ready).
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_dev[dev].sms > 0 ? g_dev[dev].sms : 1;
 }
 
 Report make_report(DevStatus* st) {
@@ -186,6 +199,25 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
   const size_t rows = (size_t)p->B * p->H * p->N;
   a.Dsum = static_cast<float*>(ws);
   a.dQacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * 4));
+  a.slots = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * 4) +
+                                     align256(rows * (size_t)p->d * 4));
+  a.G = 0;
+  if (!p->block_mask) {
+    // One CTA per key tile, unless that leaves SMs idle (fewer key tiles than
+    // SMs) or a cap was set with fa_set_bwd_ctas: then persistent CTAs, one per
+    // SM or the cap, never more than the iterations or the slots the workspace
+    // holds
+    const Sched s0 = make_sched((p->N + 127) / 128, p->B * p->H, p->causal ? 1 : 0, 1);
+    const long long units = (long long)p->B * p->H * ((p->N + 127) / 128);
+    long long G = device_sms();
+    const int cap = g_bwd_ctas.load();
+    if (G > kBwdMaxCtas) G = kBwdMaxCtas;
+    if (cap > 0 || units < G) {
+      if (cap > 0 && cap < G) G = cap;
+      if (G > s0.T) G = s0.T;
+      a.G = (int)G;
+    }
+  }
   return a;
 }
 
@@ -451,8 +483,17 @@ fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const v
 size_t fa_bwd_workspace_size(const fa_params* p) {
   if (fa_check(p, 0) != FA_OK) return 0;
   const size_t rows = (size_t)p->B * p->H * p->N;
-  return align256(rows * 4) + align256(rows * (size_t)p->d * 4);
+  size_t slots = 0;
+  if (!p->block_mask) {
+    // two fp32 [dV | dK] partial-sum slots of 128 x d each per persistent CTA
+    const Sched s0 = make_sched((p->N + 127) / 128, p->B * p->H, p->causal ? 1 : 0, 1);
+    const long long G = s0.T < kBwdMaxCtas ? s0.T : kBwdMaxCtas;
+    slots = align256((size_t)G * 2 * 2 * 128 * (size_t)p->d * 4);
+  }
+  return align256(rows * 4) + align256(rows * (size_t)p->d * 4) + slots;
 }
+
+int fa_set_bwd_ctas(int n) { return g_bwd_ctas.exchange(n < 0 ? 0 : n); }
 
 fa_status fa_bwd_preprocess(const fa_params* p, const void* O, const void* dO, void* ws,
                             size_t ws_bytes, void* stream) {
@@ -500,7 +541,8 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
   FA_TRY(encode_bhnd(&tm[2], V, p));
   FA_TRY(encode_bhnd(&tm[3], dO, p));
   FA_TRY(encode_dqacc(&tm[4], a.dQacc, p));
-  cudaError_t e = launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
+  cudaError_t e = a.G > 0 ? launch_bwd_persist(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream))
+                          : launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) {
     set_err("backward main kernel not available in this build");
     return FA_ERR_UNSUPPORTED;
@@ -509,14 +551,19 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
   return FA_OK;
 }
 
-fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* ws, size_t ws_bytes, void* stream) {
+fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* dK, void* dV, void* ws,
+                          size_t ws_bytes, void* stream) {
   FA_TRY(fa_check(p, 1));
   FA_TRY(need16(dQ, "dQ"));
+  FA_TRY(need16(dK, "dK"));
+  FA_TRY(need16(dV, "dV"));
   FA_TRY(check_ws(p, ws, ws_bytes));
   DevStatus* st = nullptr;
   FA_TRY(device_ready(&st));
   BwdArgs a = bwd_args(p, ws);
   a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
   a.rep = make_report(st);
   cudaError_t e = launch_bwd_finalize(a, p->d, p->dtype == FA_F16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward finalize launch");
@@ -530,7 +577,7 @@ fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V
   FA_TRY(need16(dQ, "dQ"));
   FA_TRY(fa_bwd_preprocess(p, O, dO, ws, ws_bytes, stream));
   FA_TRY(fa_bwd_main(p, Q, K, V, dO, LSE, dK, dV, ws, ws_bytes, stream));
-  return fa_bwd_finalize(p, dQ, ws, ws_bytes, stream);
+  return fa_bwd_finalize(p, dQ, dK, dV, ws, ws_bytes, stream);
 }
 
 fa_status fa_get_status(void* stream) {

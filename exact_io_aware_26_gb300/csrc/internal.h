@@ -65,6 +65,11 @@ struct BwdArgs {
   void* dQ;
   float* Dsum;   // [B*H*N]  rowsum(dO * O)
   float* dQacc;  // [B*H*N*d] fp32 accumulator of dQ / scale
+  // stream-K split (no block mask): G persistent CTAs, and per CTA two slots
+  // of fp32 partial [dV | dK] sums [128][d] each for key tiles it shares;
+  // G = 0: one CTA per key tile
+  int G;
+  float* slots;
   Report rep;
 };
 
@@ -77,6 +82,8 @@ cudaError_t launch_fwd_merge(const FwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);
+cudaError_t launch_bwd_persist(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
+                               cudaStream_t s);
 cudaError_t launch_bwd_finalize(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_wait_selftest(const Report& rep, cudaStream_t s);
 

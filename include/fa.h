@@ -140,8 +140,12 @@ size_t fa_fwd_split_workspace_size(const fa_params* p, int num_splits);
  * FA_F32, 0 on invalid p.  Host-only when num_sms > 0. */
 int fa_fwd_num_splits(const fa_params* p, int num_sms);
 
-/* Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * O) [B*H*N] and
- * the fp32 dQ accumulator [B*H*N*d], each 256-byte aligned.  0 on invalid p. */
+/* Bytes of device workspace fa_bwd needs, each part 256-byte aligned: fp32
+ * D = rowsum(dO * O) [B*H*N], the fp32 dQ accumulator [B*H*N*d] and, without a
+ * block mask, the fp32 partial-sum slots of the persistent main kernel
+ * (2 x 2 x 128 x d values for each of up to min(160, iterations) CTAs, where
+ * iterations = B*H*T^2 or B*H*T(T+1)/2 causal, T = ceil(N / 128)).  0 on
+ * invalid p. */
 size_t fa_bwd_workspace_size(const fa_params* p);
 
 /*
@@ -160,20 +164,33 @@ fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V
 
 /* The three stages of fa_bwd, exported so that each can be timed on its own.
  * preprocess: D = rowsum(dO * O) into the workspace, dQ accumulator zeroed.
- * main: recompute P tile by tile, accumulate dK, dV per key tile (written to
- *       dK, dV) and add scale-free dQ contributions into the accumulator.
- * finalize: dQ = scale * accumulator, converted to `dtype`. */
+ * main: recompute P tile by tile, accumulate dK, dV per key tile and add
+ *       scale-free dQ contributions into the accumulator.  Without a block
+ *       mask the kernel is persistent (about one CTA per SM) and splits the
+ *       (key tile, query tile) iterations evenly: a key tile whose iterations
+ *       several CTAs share gets fp32 partial sums in the workspace instead of
+ *       its dK, dV.  Every other key tile's dK, dV are written here.
+ * finalize: dQ = scale * accumulator, converted to `dtype`, and dK, dV of the
+ *       shared key tiles from their partial sums.  Must follow the main stage
+ *       of the same call sequence (same p, workspace and fa_set_bwd_ctas). */
 fa_status fa_bwd_preprocess(const fa_params* p, const void* O, const void* dO, void* workspace,
                             size_t workspace_bytes, void* stream);
 fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const void* V,
                       const void* dO, const float* LSE, void* dK, void* dV, void* workspace,
                       size_t workspace_bytes, void* stream);
-fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* workspace, size_t workspace_bytes,
-                          void* stream);
+fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* dK, void* dV, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Upper bound on the CTAs of the persistent backward main kernel (0, the
+ * default: one per SM, at most 160).  Applies to backward calls made after it;
+ * do not change it between the main and finalize stages of one backward pass.
+ * Returns the previous value.  Smaller values make more key tiles shared
+ * between CTAs, which the tests use to exercise that path on small problems. */
+int fa_set_bwd_ctas(int n);
 
 /*
- * Maximum workspace, in bytes, that fa_bwd_noalloc can serve (64 MiB): enough for
- * B*H*N*(d+1) <= 16 Mi fp32 values, e.g. B=4, H=12, N=2048, d=64.
+ * Maximum workspace, in bytes, that fa_bwd_noalloc can serve (64 MiB); e.g.
+ * B=4, H=12, N=2048, d=64 needs about 47 MiB (fa_bwd_workspace_size).
  */
 #define FA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 
@@ -186,7 +203,7 @@ fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* workspace, size_t 
  * those callers only.
  *
  * Same arguments and results as fa_bwd without the workspace: the fp32 scratch
- * (D and the dQ accumulator) comes from a FA_NOALLOC_SCRATCH_BYTES array that
+ * (D, the dQ accumulator and the partial-sum slots) comes from a FA_NOALLOC_SCRATCH_BYTES array that
  * is part of the library image, so every GPU that loads libfa.so holds that
  * memory until the process exits.  No call here allocates or frees device
  * memory.  A problem whose workspace (fa_bwd_workspace_size) exceeds the array

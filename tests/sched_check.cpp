@@ -1,0 +1,90 @@
+// Brute-force check of the backward kernel's work split (bwd_sched.cuh) on the
+// CPU: every (head, key tile, query tile) iteration is taken by exactly one
+// CTA, pieces that cover a whole key tile have no slot, every other piece has
+// a slot of its own, and the shared key tiles that sched_shared reports (one
+// boundary each) name exactly the CTAs and slots that hold their partial sums.
+// Usage: sched_check n BH causal G   (exit status 0 when every check holds)
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <set>
+#include <utility>
+#include <vector>
+
+#include "bwd_sched.cuh"
+
+using namespace fa;
+
+#define CHECK(c)                                                         \
+  do {                                                                   \
+    if (!(c)) {                                                          \
+      std::fprintf(stderr, "check failed at line %d: %s\n", __LINE__, #c); \
+      return 1;                                                          \
+    }                                                                    \
+  } while (0)
+
+int main(int argc, char** argv) {
+  if (argc != 5) return 2;
+  const int n = std::atoi(argv[1]), BH = std::atoi(argv[2]), causal = std::atoi(argv[3]),
+            G = std::atoi(argv[4]);
+  const Sched s = make_sched(n, BH, causal, G);
+  // iteration order: head-major, then key tile, then query tile
+  long long g = 0;
+  for (int bh = 0; bh < BH; ++bh)
+    for (int kt = 0; kt < n; ++kt)
+      for (int q = causal ? kt : 0; q < n; ++q, ++g) {
+        int b2, k2, j2;
+        sched_locate(s, g, b2, k2, j2);
+        CHECK(b2 == bh && k2 == kt && j2 == q - (causal ? kt : 0));
+      }
+  CHECK(g == s.T);
+  CHECK(sched_start(s, 0) == 0 && sched_start(s, G) == s.T);
+  std::vector<int> seen((size_t)BH * n * n, 0);
+  // key tile -> {(cta, slot)} of its partial pieces
+  std::map<std::pair<int, int>, std::set<std::pair<int, int>>> parts;
+  std::set<int> slots;
+  for (int c = 0; c < G; ++c) {
+    long long gg = sched_start(s, c);
+    const long long ge = sched_start(s, c + 1);
+    CHECK(ge > gg);  // no CTA without work
+    bool first = true;
+    Seg sg;
+    int pieces = 0;
+    std::vector<Seg> mine;
+    while (sched_next(s, c, gg, ge, first, sg)) {
+      mine.push_back(sg);
+      ++pieces;
+      CHECK(sg.bh >= 0 && sg.bh < BH && sg.kt >= 0 && sg.kt < n);
+      CHECK(sg.q_first >= (causal ? sg.kt : 0) && sg.q_first < sg.q_end && sg.q_end <= n);
+      for (int q = sg.q_first; q < sg.q_end; ++q) ++seen[((size_t)sg.bh * n + sg.kt) * n + q];
+      const bool whole = sg.q_first == (causal ? sg.kt : 0) && sg.q_end == n;
+      CHECK(whole == (sg.slot < 0));
+      if (sg.slot >= 0) {
+        CHECK(slots.insert(sg.slot).second);
+        parts[{sg.bh, sg.kt}].insert({c, sg.slot});
+      }
+    }
+    CHECK(gg == ge && pieces >= 1);
+    for (size_t k = 0; k < mine.size(); ++k) {
+      if (mine[k].slot < 0) continue;
+      if (k == 0) CHECK(mine[k].slot == 2 * c);
+      else CHECK(k + 1 == mine.size() && mine[k].slot == 2 * c + 1);
+    }
+  }
+  for (int bh = 0; bh < BH; ++bh)
+    for (int kt = 0; kt < n; ++kt)
+      for (int q = 0; q < n; ++q)
+        CHECK(seen[((size_t)bh * n + kt) * n + q] == ((!causal || q >= kt) ? 1 : 0));
+  // the finalize stage's view of the shared key tiles
+  std::map<std::pair<int, int>, std::set<std::pair<int, int>>> fixed;
+  for (int c = 0; c + 1 < G; ++c) {
+    int bh, kt, c_last, fs;
+    if (!sched_shared(s, c, bh, kt, c_last, fs)) continue;
+    std::set<std::pair<int, int>> want{{c, fs}};
+    for (int cc = c + 1; cc <= c_last; ++cc) want.insert({cc, 2 * cc});
+    CHECK(fixed.emplace(std::make_pair(bh, kt), want).second);  // one boundary per key tile
+  }
+  CHECK(fixed == parts);
+  std::printf("ok n=%d BH=%d causal=%d G=%d T=%lld shared=%zu\n", n, BH, causal, G, s.T, parts.size());
+  return 0;
+}

@@ -53,6 +53,36 @@ def test_bwd_small(cuda_lib, dtype, d, N, causal):
     check_grads(got, _ref(inp, causal), dtype)
 
 
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 50])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_persistent_ctas_share_key_tiles(cuda_lib, d, causal, ctas):
+    """Few persistent CTAs: each walks several key tiles and most key tiles are
+    split between CTAs, so their dK, dV come from the finalize stage's sums."""
+    inp = synth.make_inputs(2, 2, 777, d, "bf16", seed=4200 + ctas + d)
+    old = fa.set_bwd_ctas(ctas)
+    try:
+        got = _run(inp, causal, guard=True)
+    finally:
+        fa.set_bwd_ctas(old)
+    check_grads(got, _ref(inp, causal), "bf16")
+
+
+def test_bwd_persistent_and_single_key_tile_paths_agree(cuda_lib):
+    """The same gradients (up to summation order) whatever the CTA count."""
+    inp = synth.make_inputs(1, 3, 1100, 64, "f16", seed=4300)
+    outs = []
+    for ctas in (0, 1, 5, 23):
+        old = fa.set_bwd_ctas(ctas)
+        try:
+            outs.append([to_np64(g) for g in _run(inp, True)])
+        finally:
+            fa.set_bwd_ctas(old)
+    for o in outs[1:]:
+        for g, g0 in zip(o, outs[0]):
+            assert rel_fro(g, g0) <= 2e-3
+
+
 @pytest.mark.parametrize("mask_block", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bwd_block_mask(cuda_lib, mask_block, causal):
@@ -117,7 +147,12 @@ def test_bwd_workload_fp16_n8192_full_and_no_score_matrix(cuda_lib):
     torch.cuda.synchronize()
     peak = torch.cuda.max_memory_allocated() - base
     assert peak <= 1 << 20, f"backward allocated {peak} bytes"
-    assert ws.numel() < 8192 * 8192 * 2 // 16
+    # linear in N (D and the dQ accumulator) plus the persistent CTAs' partial-sum
+    # slots, whose size does not depend on N; the score matrix would be N^2 * 2 bytes
+    linear = 8192 * 4 + 8192 * 64 * 4
+    slots = 160 * 2 * 2 * 128 * 64 * 4
+    assert ws.numel() <= linear + slots + 3 * 256
+    assert ws.numel() < 8192 * 8192 * 2 // 4
     assert fa.get_status() == fa.FA_OK
     check_grads((dq, dk, dv), _ref(inp), "f16")
 

@@ -66,14 +66,28 @@ def test_backward_limits(lib):
 
 
 def test_workspace_size(lib):
+    up = lambda x: (x + 255) // 256 * 256
+    # D, the dQ accumulator and, without a block mask, two [dV | dK] fp32 slots
+    # of 128 x d per persistent CTA (at most 160, at most one per iteration)
+    slots = lambda ctas, d: up(ctas * 2 * 2 * 128 * d * 4)
     p = _p(B=4, H=12, N=2048, d=64)
     rows = 4 * 12 * 2048
-    up = lambda x: (x + 255) // 256 * 256
-    assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4)
-    p = _p(N=23400, H=12, d=64)
+    assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4) + slots(160, 64)
+    p = _p(N=23400, H=12, d=64, causal=1)
     rows = 12 * 23400
+    assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4) + slots(160, 64)
+    p = _p(N=300, H=1, d=128, causal=1)  # 3 tiles: 6 causal iterations, so 6 CTAs at most
+    assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(300 * 4) + up(300 * 128 * 4) + slots(6, 128)
+    p = _p(B=2, H=3, N=700, d=64, block_mask=4096)  # one CTA per key tile: no slots
+    rows = 2 * 3 * 700
     assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4)
     assert lib.fa_bwd_workspace_size(ctypes.byref(_p(d=32))) == 0
+
+
+def test_bwd_cta_cap_setter(lib):
+    old = fa.set_bwd_ctas(7)
+    assert fa.set_bwd_ctas(-3) == 7   # negative clamps to 0 (one per SM)
+    assert fa.set_bwd_ctas(old) == 0
 
 
 def test_invalid_calls_return_before_any_launch(lib):
