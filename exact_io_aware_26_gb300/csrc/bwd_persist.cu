@@ -178,8 +178,13 @@ __global__ void __launch_bounds__(320, 1)
   // K/V buffer of piece pc and the phase of its use of that buffer
   auto kv_buf = [&](int pc) { return KV2 ? (pc & 1) : 0; };
   auto kv_phase = [&](int pc) { return (uint32_t)(KV2 ? (pc >> 1) & 1 : pc & 1); };
-  auto info = [&](int it) {
-    return reinterpret_cast<const volatile int*>(smem + L::STAT + (it % NQ) * L::STAT_STRIDE + 1024);
+  // tile it's coordinates {kt, bh, qt, slot} and {pc, flags}: plain vector
+  // loads, read only after the stage's full barrier (whose wait orders them)
+  auto info_a = [&](int it) {
+    return *reinterpret_cast<const int4*>(smem + L::STAT + (it % NQ) * L::STAT_STRIDE + 1024);
+  };
+  auto info_b = [&](int it) {
+    return *reinterpret_cast<const int2*>(smem + L::STAT + (it % NQ) * L::STAT_STRIDE + 1040);
   };
 
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
@@ -262,6 +267,17 @@ __global__ void __launch_bounds__(320, 1)
     bool live = open();
     int qt = live ? next_q(a.m, sg.bh / a.H, sg.bh % a.H, sg.q_first, sg.kt, sg.q_end) : 0;
     bool at_start = true;
+    // the next tile's statistics, loaded one tile ahead so that their latency
+    // hides behind the previous tile's copies: -LSE*log2(e) and -D of rows
+    // 4 lane .. 4 lane + 3, negated as the compute warps use them
+    float4 l4, d4;
+    auto load_stats = [&](int bh, int q0) {
+      l4 = make_float4(-lse2_of(a, bh, q0 + lane * 4 + 0), -lse2_of(a, bh, q0 + lane * 4 + 1),
+                       -lse2_of(a, bh, q0 + lane * 4 + 2), -lse2_of(a, bh, q0 + lane * 4 + 3));
+      d4 = make_float4(-d_of(a, bh, q0 + lane * 4 + 0), -d_of(a, bh, q0 + lane * 4 + 1),
+                       -d_of(a, bh, q0 + lane * 4 + 2), -d_of(a, bh, q0 + lane * 4 + 3));
+    };
+    if (live) load_stats(sg.bh, qt * kTile);
     while (ok && live) {
       // this tile, and whether another follows (in this piece or the next)
       const int kt = sg.kt, bh = sg.bh, slot = sg.slot;
@@ -301,29 +317,16 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(dst + c * (kTile * 128), &tmQ, bar_qf(s), c * 64, this_qt * kTile, bh);
       }
-      // negated, as the compute warps use them: -LSE*log2(e) and -D
       float* st = reinterpret_cast<float*>(smem + L::STAT + s * L::STAT_STRIDE);
-      float4 l4, d4;
-      l4.x = -lse2_of(a, bh, this_qt * kTile + lane * 4 + 0);
-      l4.y = -lse2_of(a, bh, this_qt * kTile + lane * 4 + 1);
-      l4.z = -lse2_of(a, bh, this_qt * kTile + lane * 4 + 2);
-      l4.w = -lse2_of(a, bh, this_qt * kTile + lane * 4 + 3);
-      d4.x = -d_of(a, bh, this_qt * kTile + lane * 4 + 0);
-      d4.y = -d_of(a, bh, this_qt * kTile + lane * 4 + 1);
-      d4.z = -d_of(a, bh, this_qt * kTile + lane * 4 + 2);
-      d4.w = -d_of(a, bh, this_qt * kTile + lane * 4 + 3);
       reinterpret_cast<float4*>(st)[lane] = l4;
       reinterpret_cast<float4*>(st + 128)[lane] = d4;
       if (lane == 0) {
-        int* ti = reinterpret_cast<int*>(st + 256);
-        ti[0] = kt;
-        ti[1] = bh;
-        ti[2] = this_qt;
-        ti[3] = slot;
-        ti[4] = this_pc;
-        ti[5] = (first ? kFirst : 0) | (last ? kLast : 0) | (live ? kMore : 0);
+        *reinterpret_cast<int4*>(st + 256) = make_int4(kt, bh, this_qt, slot);
+        *reinterpret_cast<int2*>(st + 260) =
+            make_int2(this_pc, (first ? kFirst : 0) | (last ? kLast : 0) | (live ? kMore : 0));
       }
       mbar_arrive(bar_qf(s));
+      if (live) load_stats(sg.bh, qt * kTile);  // the next tile's
       const int os = it % NO;
       if (it >= NO && !(ok = warp_wait(w, bar_oe(os), ((it / NO) - 1) & 1))) break;
       if (lane == 0) {
@@ -401,7 +404,8 @@ __global__ void __launch_bounds__(320, 1)
     int it = 0, pieces = 0;
     while (ok) {
       if (!(ok = q_ready(it))) break;
-      const int pc = info(it)[4], fl = info(it)[5];
+      const int2 ib = info_b(it);
+      const int pc = ib.x, fl = ib.y;
       const int b = kv_buf(pc);
       const bool first = fl & kFirst, last = fl & kLast, more = fl & kMore;
       if (first) pieces = pc + 1;
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = warp_wait(w, bar_p_full, it & 1))) break;
       if (ahead) {
         if (!(ok = q_ready(it + 1))) break;
-        const int npc = info(it + 1)[4];
+        const int npc = info_b(it + 1).x;
         nb = kv_buf(npc);
         if (npc != pc && !(ok = warp_wait(w, bar_kv_full(nb), kv_phase(npc)))) break;
       }
@@ -544,9 +548,11 @@ __global__ void __launch_bounds__(320, 1)
     auto p_phase = [&](int it) -> bool {
       // the stage's statistics and coordinates (staged by the producer with Q and dO)
       if (!q_ready(it)) return false;
-      const int kt = info(it)[0], qtile = info(it)[2];
+      const int4 ia = info_a(it);
+      const int kt = ia.x, qtile = ia.z;
       const int key = kt * kTile + r;
-      const bool rows_out = __any_sync(0xffffffffu, key >= a.N);  // a tail key tile
+      // a tail key tile: some row of this warp's 32 lies past N (warp-uniform)
+      const bool rows_out = kt * kTile + (warp & 3) * 32 + 31 >= a.N;
       if (!warp_wait(w, bar_s_full, it & 1)) return false;
       tc_fence_after();
       {
@@ -651,8 +657,10 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = p_phase(0);
       for (int it = 0; ok; ++it) {
         // this tile's coordinates (its stage is not reused before dK_i completes)
-        const int kt = info(it)[0], bh = info(it)[1], qt = info(it)[2], slot = info(it)[3];
-        const int pc = info(it)[4], fl = info(it)[5];
+        const int4 ia = info_a(it);
+        const int2 ib = info_b(it);
+        const int kt = ia.x, bh = ia.y, qt = ia.z, slot = ia.w;
+        const int pc = ib.x, fl = ib.y;
         const bool last = fl & kLast, more = fl & kMore;
         // ---- dS_i = P_i * (dP_i - D)
         if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
