@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(256) bwd_finalize_kernel(const float4* __restr
 template <int D, bool F16>
 __device__ void fixup_key_tile(const BwdArgs& a, int boundary) {
   const int BH = a.B * a.H;
-  const Sched s = make_sched((a.N + 127) / 128, BH, a.m.causal, a.G);
+  const Sched s = make_sched((a.N + 127) / 128, BH, a.m.causal, a.G, a.u0);
   const int c = boundary;
   int bh, kt, c_last, fs;
   if (!sched_shared(s, c, bh, kt, c_last, fs)) return;

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(320, 1)
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
     }
-    const Sched sc = make_sched(n_tiles, BH, a.m.causal, a.G > 0 ? a.G : 1);
+    const Sched sc = make_sched(n_tiles, BH, a.m.causal, a.G > 0 ? a.G : 1, a.u0);
     long long g = a.G > 0 ? sched_start(sc, (int)blockIdx.x) : 0;
     const long long g_stop = a.G > 0 ? sched_start(sc, (int)blockIdx.x + 1) : 1;
     bool first_piece = true;

@@ -1,15 +1,17 @@
 // bwd_sched.cuh -- how the backward main kernel splits its work over CTAs.
 //
-// The unit of work is one (key tile, query tile) iteration.  Without a block
-// mask the iterations of all heads are numbered head-major, then by key tile,
-// then by query tile (causal: the query tiles from the key tile's own index
-// up), and cut into G contiguous ranges of nearly equal length, one per
-// persistent CTA (G about the SM count).  A range may begin or end inside a
-// key tile: that key tile's dK, dV are then written by each CTA that touched
-// it as fp32 partial sums into a slot of its own (slot 2c for CTA c's first
-// range piece, 2c + 1 for its last), and the finalize kernel adds the slots.
-// With a block mask the kept query tiles are known on the device only, and
-// each CTA takes one whole key tile instead.
+// A unit is one key tile of one head; the units are numbered key-tile-major,
+// u = kt * (B*H) + bh, and each unit's iterations are its visited query tiles
+// (causal: from the key tile's own index up).  The units from u0 on are split
+// "stream-K": their iterations, in that order, are cut into G contiguous
+// ranges of nearly equal length, one per persistent CTA (G about the SM
+// count).  A range may begin or end inside a unit: that key tile's dK, dV are
+// then written by each CTA that touched it as fp32 partial sums into a slot
+// of its own (slot 2c for CTA c's first range piece, 2c + 1 for its last), and
+// the finalize kernel adds the slots.  Units before u0 are whole-key-tile
+// CTAs of the one-CTA-per-key-tile kernel (so that only the last, ragged
+// wave is split), and with a block mask, whose kept query tiles are known on
+// the device only, every unit is.
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -22,19 +24,17 @@
 namespace fa {
 
 struct Sched {
-  int n;        // tiles per sequence (ceil(N / 128))
-  int causal;   // query tiles before the key tile are skipped
-  int G;        // CTAs
-  long long W;  // iterations per head
-  long long T;  // iterations in all
+  int n;         // tiles per sequence (ceil(N / 128))
+  int BH;        // heads (B * H)
+  int causal;    // query tiles before the key tile are skipped
+  int G;         // CTAs
+  long long P0;  // iterations of the units before u0
+  long long T;   // iterations of units u0 .. n*BH - 1
 };
 
 // Most CTAs a stream-K launch uses (and that the workspace holds slots for).
 constexpr int kBwdMaxCtas = 160;
 
-__host__ __device__ inline long long sched_per_head(int n, int causal) {
-  return causal ? (long long)n * (n + 1) / 2 : (long long)n * n;
-}
 // iterations of the key tiles before kt in one head
 __host__ __device__ inline long long sched_before(int kt, int n, int causal) {
   return causal ? (long long)kt * n - (long long)kt * (kt - 1) / 2 : (long long)kt * n;
@@ -43,38 +43,49 @@ __host__ __device__ inline long long sched_before(int kt, int n, int causal) {
 __host__ __device__ inline int sched_visited(int kt, int n, int causal) {
   return causal ? n - kt : n;
 }
-__host__ __device__ inline Sched make_sched(int n, int BH, int causal, int G) {
+// iterations of the units before unit u
+__host__ __device__ inline long long sched_unit_start(long long u, int n, int BH, int causal) {
+  const int kt = (int)(u / BH), bh = (int)(u - (long long)kt * BH);
+  return (long long)BH * sched_before(kt, n, causal) + (long long)bh * sched_visited(kt, n, causal);
+}
+__host__ __device__ inline Sched make_sched(int n, int BH, int causal, int G, long long u0 = 0) {
   Sched s;
   s.n = n;
+  s.BH = BH;
   s.causal = causal;
   s.G = G;
-  s.W = sched_per_head(n, causal);
-  s.T = s.W * BH;
+  s.P0 = sched_unit_start(u0, n, BH, causal);
+  s.T = (long long)BH * sched_before(n, n, causal) - s.P0;
   return s;
 }
-// first iteration of CTA c (c = G gives T)
+// first iteration of CTA c (c = G gives T), counted from unit u0
 __host__ __device__ inline long long sched_start(const Sched& s, int c) {
   return (long long)c * s.T / s.G;
 }
 // head, key tile and index among the key tile's visited query tiles of iteration g
 __host__ __device__ inline void sched_locate(const Sched& s, long long g, int& bh, int& kt, int& j) {
-  bh = (int)(g / s.W);
-  const long long r = g - (long long)bh * s.W;
+  const long long a = g + s.P0;  // from the first unit
+  // the key tile: the largest k with BH * sched_before(k) <= a, i.e. with
+  // sched_before(k) <= r
+  const long long r = a / s.BH;
+  int k;
   if (!s.causal) {
-    kt = (int)(r / s.n);
-    j = (int)(r - (long long)kt * s.n);
-    return;
+    k = (int)(r / s.n);
+  } else {
+    // a root of k^2 - (2n+1) k + 2r, then corrected by exact integer comparisons
+    const double b2 = 2.0 * s.n + 1.0;
+    const double disc = b2 * b2 - 8.0 * (double)r;
+    k = (int)((b2 - sqrt(disc > 0.0 ? disc : 0.0)) * 0.5);
   }
-  // largest k with sched_before(k) <= r: a root of k^2 - (2n+1) k + 2r, then
-  // corrected by exact integer comparisons
-  const double b2 = 2.0 * s.n + 1.0;
-  int k = (int)((b2 - sqrt(b2 * b2 - 8.0 * (double)r)) * 0.5);
   if (k < 0) k = 0;
   if (k > s.n - 1) k = s.n - 1;
-  while (k > 0 && sched_before(k, s.n, 1) > r) --k;
-  while (k + 1 < s.n && sched_before(k + 1, s.n, 1) <= r) ++k;
+  while (k > 0 && sched_before(k, s.n, s.causal) > r) --k;
+  while (k + 1 < s.n && sched_before(k + 1, s.n, s.causal) <= r) ++k;
   kt = k;
-  j = (int)(r - sched_before(k, s.n, 1));
+  const long long rem = a - (long long)s.BH * sched_before(k, s.n, s.causal);
+  const int v = sched_visited(k, s.n, s.causal);
+  bh = (int)(rem / v);
+  j = (int)(rem - (long long)bh * v);
 }
 
 // One piece of a CTA's range: key tile kt of head bh, query tiles [q_first, q_end).

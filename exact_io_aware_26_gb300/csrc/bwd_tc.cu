@@ -545,8 +545,9 @@ cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   auto kern = bwd_tc_kernel<D, F16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
-  const int n_tiles = (a.N + kTile - 1) / kTile;
-  kern<<<(unsigned)(n_tiles * a.B * a.H), 320, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], a);
+  // the first a.direct key tiles, one CTA each (the rest, if any, go to the
+  // persistent kernel)
+  kern<<<(unsigned)a.direct, 320, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], a);
   return cudaGetLastError();
 }
 

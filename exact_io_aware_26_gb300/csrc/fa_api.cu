@@ -201,20 +201,33 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
   a.dQacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * 4));
   a.slots = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * 4) +
                                      align256(rows * (size_t)p->d * 4));
+  const int n = (p->N + 127) / 128;
+  const long long units = (long long)p->B * p->H * n;
+  a.direct = (int)units;  // one CTA per key tile ...
   a.G = 0;
+  a.u0 = (int)units;
   if (!p->block_mask) {
-    // One CTA per key tile, unless that leaves SMs idle (fewer key tiles than
-    // SMs) or a cap was set with fa_set_bwd_ctas: then persistent CTAs, one per
-    // SM or the cap, never more than the iterations or the slots the workspace
-    // holds
-    const Sched s0 = make_sched((p->N + 127) / 128, p->B * p->H, p->causal ? 1 : 0, 1);
-    const long long units = (long long)p->B * p->H * ((p->N + 127) / 128);
+    // ... unless that leaves SMs idle: with fewer key tiles than CTAs (one per
+    // SM, at most kBwdMaxCtas, or the cap set by fa_set_bwd_ctas) persistent
+    // stream-K CTAs take them all.  A cap also splits the last one to two
+    // waves' worth of a non-causal grid that would end in a partly filled wave
+    // (off by default: on GB300 the persistent kernel's slower tiles cancel
+    // what the fuller last wave gains).
     long long G = device_sms();
-    const int cap = g_bwd_ctas.load();
     if (G > kBwdMaxCtas) G = kBwdMaxCtas;
-    if (cap > 0 || units < G) {
-      if (cap > 0 && cap < G) G = cap;
+    const int cap = g_bwd_ctas.load();
+    if (cap > 0 && cap < G) G = cap;
+    long long u0 = -1;
+    if (units < G) {
+      u0 = 0;
+    } else if (cap > 0 && !p->causal && units % G != 0) {
+      u0 = (units / G - 1) * G;
+    }
+    if (u0 >= 0) {
+      const Sched s0 = make_sched(n, p->B * p->H, p->causal ? 1 : 0, 1, u0);
       if (G > s0.T) G = s0.T;
+      a.direct = (int)u0;
+      a.u0 = (int)u0;
       a.G = (int)G;
     }
   }
@@ -541,8 +554,10 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
   FA_TRY(encode_bhnd(&tm[2], V, p));
   FA_TRY(encode_bhnd(&tm[3], dO, p));
   FA_TRY(encode_dqacc(&tm[4], a.dQacc, p));
-  cudaError_t e = a.G > 0 ? launch_bwd_persist(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream))
-                          : launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaSuccess;
+  if (a.direct > 0) e = launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && a.G > 0)
+    e = launch_bwd_persist(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) {
     set_err("backward main kernel not available in this build");
     return FA_ERR_UNSUPPORTED;

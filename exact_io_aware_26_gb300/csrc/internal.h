@@ -65,10 +65,13 @@ struct BwdArgs {
   void* dQ;
   float* Dsum;   // [B*H*N]  rowsum(dO * O)
   float* dQacc;  // [B*H*N*d] fp32 accumulator of dQ / scale
-  // stream-K split (no block mask): G persistent CTAs, and per CTA two slots
-  // of fp32 partial [dV | dK] sums [128][d] each for key tiles it shares;
-  // G = 0: one CTA per key tile
+  // Work split: key tiles (units, numbered u = kt * B*H + bh) [0, direct) run
+  // one CTA each; units [u0, B*H*ceil(N/128)) are split "stream-K" over G
+  // persistent CTAs (G = 0: none), each with two slots of fp32 partial
+  // [dV | dK] sums [128][d] for key tiles it shares
+  int direct;
   int G;
+  int u0;
   float* slots;
   Report rep;
 };

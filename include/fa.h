@@ -165,11 +165,11 @@ fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V
 /* The three stages of fa_bwd, exported so that each can be timed on its own.
  * preprocess: D = rowsum(dO * O) into the workspace, dQ accumulator zeroed.
  * main: recompute P tile by tile, accumulate dK, dV per key tile and add
- *       scale-free dQ contributions into the accumulator.  Without a block
- *       mask the kernel is persistent (about one CTA per SM) and splits the
- *       (key tile, query tile) iterations evenly: a key tile whose iterations
- *       several CTAs share gets fp32 partial sums in the workspace instead of
- *       its dK, dV.  Every other key tile's dK, dV are written here.
+ *       scale-free dQ contributions into the accumulator.  One CTA per key
+ *       tile, whose dK, dV it writes; without a block mask and with fewer key
+ *       tiles than SMs, persistent CTAs (about one per SM) split the
+ *       (key tile, query tile) iterations evenly instead: a key tile whose
+ *       iterations several CTAs share gets fp32 partial sums in the workspace.
  * finalize: dQ = scale * accumulator, converted to `dtype`, and dK, dV of the
  *       shared key tiles from their partial sums.  Must follow the main stage
  *       of the same call sequence (same p, workspace and fa_set_bwd_ctas). */
@@ -182,10 +182,11 @@ fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* dK, void* dV, void
                           size_t workspace_bytes, void* stream);
 
 /* Upper bound on the CTAs of the persistent backward main kernel (0, the
- * default: one per SM, at most 160).  Applies to backward calls made after it;
- * do not change it between the main and finalize stages of one backward pass.
- * Returns the previous value.  Smaller values make more key tiles shared
- * between CTAs, which the tests use to exercise that path on small problems. */
+ * default: one per SM, at most 160).  A cap n > 0 also hands the last one to
+ * two waves' worth of a non-causal, unmasked problem to n persistent CTAs.
+ * Applies to backward calls made after it; do not change it between the main
+ * and finalize stages of one backward pass.  Returns the previous value.  The
+ * tests use it to make key tiles shared between CTAs on small problems. */
 int fa_set_bwd_ctas(int n);
 
 /*

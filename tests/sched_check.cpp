@@ -1,9 +1,10 @@
 // Brute-force check of the backward kernel's work split (bwd_sched.cuh) on the
-// CPU: every (head, key tile, query tile) iteration is taken by exactly one
-// CTA, pieces that cover a whole key tile have no slot, every other piece has
-// a slot of its own, and the shared key tiles that sched_shared reports (one
-// boundary each) name exactly the CTAs and slots that hold their partial sums.
-// Usage: sched_check n BH causal G   (exit status 0 when every check holds)
+// CPU: every (head, key tile, query tile) iteration of the units from u0 on is
+// taken by exactly one CTA (and none before u0), pieces that cover a whole key
+// tile have no slot, every other piece has a slot of its own, and the shared
+// key tiles that sched_shared reports (one boundary each) name exactly the
+// CTAs and slots that hold their partial sums.
+// Usage: sched_check n BH causal G u0   (exit status 0 when every check holds)
 #include <cstdio>
 #include <cstdlib>
 #include <map>
@@ -24,19 +25,21 @@ using namespace fa;
   } while (0)
 
 int main(int argc, char** argv) {
-  if (argc != 5) return 2;
+  if (argc != 6) return 2;
   const int n = std::atoi(argv[1]), BH = std::atoi(argv[2]), causal = std::atoi(argv[3]),
-            G = std::atoi(argv[4]);
-  const Sched s = make_sched(n, BH, causal, G);
-  // iteration order: head-major, then key tile, then query tile
+            G = std::atoi(argv[4]), u0 = std::atoi(argv[5]);
+  const Sched s = make_sched(n, BH, causal, G, u0);
+  // iteration order: key tile, then head (unit u = kt * BH + bh), then query tile
   long long g = 0;
-  for (int bh = 0; bh < BH; ++bh)
-    for (int kt = 0; kt < n; ++kt)
-      for (int q = causal ? kt : 0; q < n; ++q, ++g) {
-        int b2, k2, j2;
-        sched_locate(s, g, b2, k2, j2);
-        CHECK(b2 == bh && k2 == kt && j2 == q - (causal ? kt : 0));
-      }
+  for (int u = u0; u < n * BH; ++u) {
+    const int kt = u / BH, bh = u % BH;
+    CHECK(sched_unit_start(u, n, BH, causal) == s.P0 + g);
+    for (int q = causal ? kt : 0; q < n; ++q, ++g) {
+      int b2, k2, j2;
+      sched_locate(s, g, b2, k2, j2);
+      CHECK(b2 == bh && k2 == kt && j2 == q - (causal ? kt : 0));
+    }
+  }
   CHECK(g == s.T);
   CHECK(sched_start(s, 0) == 0 && sched_start(s, G) == s.T);
   std::vector<int> seen((size_t)BH * n * n, 0);
@@ -74,7 +77,8 @@ int main(int argc, char** argv) {
   for (int bh = 0; bh < BH; ++bh)
     for (int kt = 0; kt < n; ++kt)
       for (int q = 0; q < n; ++q)
-        CHECK(seen[((size_t)bh * n + kt) * n + q] == ((!causal || q >= kt) ? 1 : 0));
+        CHECK(seen[((size_t)bh * n + kt) * n + q] ==
+              ((kt * BH + bh >= u0 && (!causal || q >= kt)) ? 1 : 0));
   // the finalize stage's view of the shared key tiles
   std::map<std::pair<int, int>, std::set<std::pair<int, int>>> fixed;
   for (int c = 0; c + 1 < G; ++c) {
@@ -85,6 +89,7 @@ int main(int argc, char** argv) {
     CHECK(fixed.emplace(std::make_pair(bh, kt), want).second);  // one boundary per key tile
   }
   CHECK(fixed == parts);
-  std::printf("ok n=%d BH=%d causal=%d G=%d T=%lld shared=%zu\n", n, BH, causal, G, s.T, parts.size());
+  std::printf("ok n=%d BH=%d causal=%d G=%d u0=%d T=%lld shared=%zu\n", n, BH, causal, G, u0, s.T,
+              parts.size());
   return 0;
 }

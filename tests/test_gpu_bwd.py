@@ -53,12 +53,14 @@ def test_bwd_small(cuda_lib, dtype, d, N, causal):
     check_grads(got, _ref(inp, causal), dtype)
 
 
-@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 50])
+@pytest.mark.parametrize("ctas", [1, 3, 5, 9, 50])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
 def test_bwd_persistent_ctas_share_key_tiles(cuda_lib, d, causal, ctas):
-    """Few persistent CTAs: each walks several key tiles and most key tiles are
-    split between CTAs, so their dK, dV come from the finalize stage's sums."""
+    """28 key tiles (B=2, H=2, N=777) under a cap of `ctas` CTAs: 50 puts them all
+    on persistent CTAs; 3, 5 and 9 (non-causal) run most key tiles one CTA each
+    and split the last waves' worth over the persistent CTAs; 1 runs one CTA
+    per key tile.  Split key tiles get their dK, dV from the finalize stage."""
     inp = synth.make_inputs(2, 2, 777, d, "bf16", seed=4200 + ctas + d)
     old = fa.set_bwd_ctas(ctas)
     try:
@@ -68,14 +70,15 @@ def test_bwd_persistent_ctas_share_key_tiles(cuda_lib, d, causal, ctas):
     check_grads(got, _ref(inp, causal), "bf16")
 
 
-def test_bwd_persistent_and_single_key_tile_paths_agree(cuda_lib):
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_persistent_and_single_key_tile_paths_agree(cuda_lib, causal):
     """The same gradients (up to summation order) whatever the CTA count."""
-    inp = synth.make_inputs(1, 3, 1100, 64, "f16", seed=4300)
+    inp = synth.make_inputs(1, 3, 1100, 64, "f16", seed=4300)  # 27 key tiles
     outs = []
-    for ctas in (0, 1, 5, 23):
+    for ctas in (0, 1, 5, 23, 40):
         old = fa.set_bwd_ctas(ctas)
         try:
-            outs.append([to_np64(g) for g in _run(inp, True)])
+            outs.append([to_np64(g) for g in _run(inp, causal)])
         finally:
             fa.set_bwd_ctas(old)
     for o in outs[1:]:
