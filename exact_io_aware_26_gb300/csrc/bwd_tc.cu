@@ -132,7 +132,13 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) raise_error(w, FA_ERR_CUDA);
     return;
   }
-  if (threadIdx.x == 0) {
+  // The producer lane sets up the barriers and, before the block-wide setup
+  // barrier, already issues the copies that need no wait (K_j, V_j and the
+  // first NS query tiles' Q, dO), so that their latency overlaps the TMEM
+  // allocation.  The statistics of those stages are staged after the barrier.
+  const bool producer = (warp == 8 && lane == 0);
+  int pre = 0;  // producer lane: query-tile stages already being copied
+  if (producer) {
     mbar_init(bar_kv, 1);
     mbar_init(bar_s_full, 1);
     mbar_init(bar_dp_full, 1);
@@ -150,6 +156,24 @@ __global__ void __launch_bounds__(320, 1)
     }
     *abort_cta = 0;
     fence_barrier_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmdO);
+    mbar_arrive_expect_tx(bar_kv, 2 * L::TILE);
+    for (int c = 0; c < D / 64; ++c) {
+      tma_load_3d(sb + L::K + c * (kTile * 128), &tmK, bar_kv, c * 64, kt * kTile, bh);
+      tma_load_3d(sb + L::V + c * (kTile * 128), &tmV, bar_kv, c * 64, kt * kTile, bh);
+    }
+    for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles && pre < NS;
+         qt = next_q(a.m, b, h, qt + 1, kt, n_tiles), ++pre) {
+      const uint32_t dst = sb + L::QS + (uint32_t)pre * 2u * L::TILE;
+      mbar_arrive_expect_tx(bar_qf(pre), 2 * L::TILE);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(dst + c * (kTile * 128), &tmQ, bar_qf(pre), c * 64, qt * kTile, bh);
+        tma_load_3d(dst + L::TILE + c * (kTile * 128), &tmdO, bar_qf(pre), c * 64, qt * kTile, bh);
+      }
+    }
   }
   if (warp == 9) {
     tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
@@ -165,23 +189,13 @@ __global__ void __launch_bounds__(320, 1)
     // Lane 0 issues the TMA copies; every lane also stages four rows of the
     // query tile's statistics into the ring stage, so that the stage's full
     // barrier covers Q, dO and the statistics together.
-    if (lane == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(bar_kv, 2 * L::TILE);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sb + L::K + c * (kTile * 128), &tmK, bar_kv, c * 64, kt * kTile, bh);
-        tma_load_3d(sb + L::V + c * (kTile * 128), &tmV, bar_kv, c * 64, kt * kTile, bh);
-      }
-    }
+    pre = __shfl_sync(0xffffffffu, pre, 0);
     int it = 0;
     for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles;
          qt = next_q(a.m, b, h, qt + 1, kt, n_tiles)) {
       const int s = it % NS;
       if (it >= NS && !warp_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
-      if (lane == 0) {
+      if (lane == 0 && it >= pre) {
         const uint32_t dst = sb + L::QS + (uint32_t)s * 2u * L::TILE;
         mbar_arrive_expect_tx(bar_qf(s), 2 * L::TILE);
         for (int c = 0; c < D / 64; ++c) {
@@ -207,8 +221,9 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (lane == 0) {
       mbar_drain(w, bar_kv, 0);
+      const int issued = it > pre ? it : pre;  // stages copied (some before the loop)
       for (int s = 0; s < NS; ++s) {
-        const int n = (it - s + NS - 1) / NS;  // loads issued into stage s
+        const int n = (issued - s + NS - 1) / NS;  // loads issued into stage s
         if (n > 0) mbar_drain(w, bar_qf(s), (n - 1) & 1);
       }
     }

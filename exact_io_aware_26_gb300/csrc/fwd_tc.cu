@@ -114,7 +114,13 @@ __global__ void __launch_bounds__(192, 2)
     if (threadIdx.x == 0) raise_error(w, FA_ERR_CUDA);
     return;
   }
-  if (threadIdx.x == 0) {
+  // The producer lane sets up the barriers and, before the block-wide setup
+  // barrier, already issues the copies that need no wait (Q and the first NS
+  // K, V tiles), so that their latency overlaps the TMEM allocation.
+  const bool producer = (warp == 4 && lane == 0);
+  int nk = 0, nv = 0;  // producer lane: K and V copies issued
+  int kt_next = kt_end;  // producer lane: the next key tile to copy
+  if (producer) {
     mbar_init(bar_q, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 4);
@@ -129,6 +135,26 @@ __global__ void __launch_bounds__(192, 2)
     }
     *abort_cta = 0;
     fence_barrier_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    mbar_arrive_expect_tx(bar_q, L::TILE);
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_3d(sb + L::Q + c * (kTile * 128), &tmQ, bar_q, c * 64, qt * kTile, bh);
+    kt_next = next_kept(a.m, b, h, qt, kt_begin, kt_end);
+    for (; kt_next < kt_end && nk < NS; kt_next = next_kept(a.m, b, h, qt, kt_next + 1, kt_end)) {
+      const int s = nk;
+      mbar_arrive_expect_tx(bar_kf(s), L::TILE);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sb + L::K0 + s * L::TILE + c * (kTile * 128), &tmK, bar_kf(s), c * 64,
+                    kt_next * kTile, bh);
+      ++nk;
+      mbar_arrive_expect_tx(bar_vf(s), L::TILE);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sb + L::V0 + s * L::TILE + c * (kTile * 128), &tmV, bar_vf(s), c * 64,
+                    kt_next * kTile, bh);
+      ++nv;
+    }
   }
   if (warp == 5) {
     tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
@@ -142,15 +168,8 @@ __global__ void __launch_bounds__(192, 2)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(bar_q, L::TILE);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sb + L::Q + c * (kTile * 128), &tmQ, bar_q, c * 64, qt * kTile, bh);
-      int nk = 0, nv = 0;  // K and V copies issued
-      for (int kt = next_kept(a.m, b, h, qt, kt_begin, kt_end); kt < kt_end;
-           kt = next_kept(a.m, b, h, qt, kt + 1, kt_end)) {
+      // the rest of the K, V tiles, each into a stage once it is released
+      for (int kt = kt_next; kt < kt_end; kt = next_kept(a.m, b, h, qt, kt + 1, kt_end)) {
         const int s = nk % NS;
         const uint32_t ph = ((nk / NS) - 1) & 1;
         if (nk >= NS && !mbar_wait(w, bar_ke(s), ph)) break;
