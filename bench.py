@@ -6,9 +6,11 @@ A step is one pass of the whole path over one batch of the workload: for every
 causal setting the workload runs, fa_fwd then the three fa_bwd stages
 (preprocess, main, finalize), all through the C ABI of libfa.so.  Inputs are
 resident in device memory; L2 is flushed (a 256 MiB write) between steps,
-outside the timed events.  Each step is bracketed by CUDA events on the
-launching stream, and so is every launch of the dominant kernel (the backward
-main kernel), which gives the roofline figure.  FLOPs follow the usual
+outside the timed events.  The timed step is one CUDA graph holding those
+launches (captured once, replayed every step), bracketed by CUDA events on the
+launching stream; a separate pass launches the kernels one by one and brackets
+every forward and every backward main kernel (the dominant kernel) with
+events, which gives the breakdown and the roofline figure.  FLOPs follow the usual
 convention: forward 4 B H N^2 d, backward 2.5 x forward, halved for causal,
 scaled by the kept-tile fraction for a block mask.
 
@@ -58,6 +60,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time separately launched kernels instead of one CUDA graph per step")
     ap.add_argument("--fwd-splits", type=int, default=0,
                     help="key-range slices of the forward (0: the library's choice for this GPU)")
     return ap.parse_args()
@@ -360,31 +364,52 @@ def main():
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step(ev_main=None, ev_fwd=None):
+    def step(s, ev_main=None, ev_fwd=None):
         for i, r in enumerate(runs):
             if ev_fwd is not None:
-                ev_fwd[i][0].record(stream)
-            fwd(fa, r, q, k, v, r["o"], r["lse"], stream)
+                ev_fwd[i][0].record(s)
+            fwd(fa, r, q, k, v, r["o"], r["lse"], s)
             if ev_fwd is not None:
-                ev_fwd[i][1].record(stream)
-            fa.bwd_preprocess(r["p"], r["o"], do, r["ws"], stream)
+                ev_fwd[i][1].record(s)
+            fa.bwd_preprocess(r["p"], r["o"], do, r["ws"], s)
             if ev_main is not None:
-                ev_main[i][0].record(stream)
-            fa.bwd_main(r["p"], q, k, v, do, r["lse"], r["dk"], r["dv"], r["ws"], stream)
+                ev_main[i][0].record(s)
+            fa.bwd_main(r["p"], q, k, v, do, r["lse"], r["dk"], r["dv"], r["ws"], s)
             if ev_main is not None:
-                ev_main[i][1].record(stream)
-            fa.bwd_finalize(r["p"], r["dq"], r["dk"], r["dv"], r["ws"], stream)
+                ev_main[i][1].record(s)
+            fa.bwd_finalize(r["p"], r["dq"], r["dk"], r["dv"], r["ws"], s)
 
     W = max(args.warmup, 3)
     for _ in range(W):
-        step()
+        step(stream)
     torch.cuda.synchronize()
     if fa.get_status() != fa.FA_OK:
         raise RuntimeError("device status not OK after warm-up")
 
+    # The step as one CUDA graph (its kernels launched back to back, without
+    # the host in between); the per-kernel breakdown comes from a pass of
+    # separately launched, separately timed kernels.
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.graph(graph, stream=side):
+                step(torch.cuda.current_stream())
+            stream.wait_stream(side)
+            graph.replay()
+            torch.cuda.synchronize()
+            if fa.get_status() != fa.FA_OK:
+                raise RuntimeError("device status not OK after the graph's first replay")
+        except RuntimeError as e:
+            print(f"# CUDA graph capture failed ({e}); timing launched steps", file=sys.stderr)
+            graph = None
+
     K = args.steps
     E = lambda: torch.cuda.Event(enable_timing=True)
     ev_step = [(E(), E()) for _ in range(K)]
+    ev_kstep = [(E(), E()) for _ in range(K)]
     ev_main = [[(E(), E()) for _ in runs] for _ in range(K)]
     ev_fwd = [[(E(), E()) for _ in runs] for _ in range(K)]
     uuid = getattr(torch.cuda.get_device_properties(local), "uuid", None)
@@ -395,11 +420,24 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks.mark(0)
+    # per-kernel pass
+    for i in range(K):
+        flush.zero_()
+        ev_kstep[i][0].record(stream)
+        step(stream, ev_main[i], ev_fwd[i])
+        ev_kstep[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    # timed pass: the whole step
     wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()
         ev_step[i][0].record(stream)
-        step(ev_main[i], ev_fwd[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(stream)
         ev_step[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -412,6 +450,7 @@ def main():
         raise RuntimeError(f"device status {status} after the timed region")
 
     total_s = sum(a.elapsed_time(b) for a, b in ev_step) / 1000.0
+    launched_s = sum(a.elapsed_time(b) for a, b in ev_kstep) / 1000.0
     main_s = sum(a.elapsed_time(b) for row in ev_main for a, b in row) / 1000.0
     fwd_s = sum(a.elapsed_time(b) for row in ev_fwd for a, b in row) / 1000.0
     if dist:
@@ -443,13 +482,16 @@ def main():
             "steps": K, "warmup": W, "ms_per_step": 1000.0 * total_s / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
-            "config": config_of(w, [r["splits"] for r in runs]),
+            "config": dict(config_of(w, [r["splits"] for r in runs]),
+                           launch="one CUDA graph per step" if graph is not None
+                           else "kernels launched one by one"),
             "breakdown": {
                 "fwd_tflops": fwd_tflops, "bwd_main_tflops": achieved,
                 "fwd_frac_of_bf16_peak": fwd_tflops / peak,
                 "bwd_main_frac_of_bf16_peak": achieved / peak,
                 "step_frac_of_bf16_peak": value / world / peak,
-                "wall_s_timed_region": wall},
+                "wall_s_timed_region": wall,
+                "ms_per_step_launched_one_by_one": 1000.0 * launched_s / K},
             "roofline": {"kernel": "bwd_tc_kernel (backward main)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
