@@ -67,19 +67,38 @@ __global__ void __launch_bounds__(256) bwd_finalize_kernel(const float4* __restr
 // Block `boundary` looks at the boundary between CTA c = boundary and c + 1 of
 // the main kernel; if a key tile is shared there (sched_shared), the block
 // adds the partial slots of the CTAs that share it and writes its dK, dV.
+// Fixup blocks per CTA boundary: each adds one slice of the key tile's slots,
+// so that enough loads are in flight to hide their latency.
+constexpr int kFixupParts = 8;
+
+// Block `part` of boundary `boundary` (between CTA c = boundary and c + 1 of the
+// main kernel): if a key tile is shared there (sched_shared), the block adds
+// its slice of the partial slots of the CTAs that share it and writes that
+// slice of the key tile's dK, dV.
 template <int D, bool F16>
-__device__ void fixup_key_tile(const BwdArgs& a, int boundary) {
+__device__ void fixup_key_tile(const BwdArgs& a, int boundary, int part) {
   const int BH = a.B * a.H;
   const Sched s = make_sched((a.N + 127) / 128, BH, a.m.causal, a.G, a.u0);
   const int c = boundary;
   int bh, kt, c_last, fs;
   if (!sched_shared(s, c, bh, kt, c_last, fs)) return;
-  const float* first_slot = a.slots + (size_t)fs * (2 * 128 * D);
   constexpr int PER = 2 * 128 * D / 4;  // float4 per slot ([dV | dK])
-  for (int e = threadIdx.x; e < PER; e += blockDim.x) {
-    float4 acc = reinterpret_cast<const float4*>(first_slot)[e];
-    for (int cc = c + 1; cc <= c_last; ++cc) {
-      const float4 v = reinterpret_cast<const float4*>(a.slots + (size_t)(2 * cc) * (2 * 128 * D))[e];
+  constexpr int SLICE = PER / kFixupParts;
+  const float4* first = reinterpret_cast<const float4*>(a.slots) + (size_t)fs * PER;
+  for (int e = part * SLICE + (int)threadIdx.x; e < (part + 1) * SLICE; e += blockDim.x) {
+    float4 acc = first[e];
+    // the other contributors' slots (2c'); usually one or two
+    int cc = c + 1;
+    for (; cc + 1 <= c_last; cc += 2) {
+      const float4 v0 = reinterpret_cast<const float4*>(a.slots)[(size_t)(2 * cc) * PER + e];
+      const float4 v1 = reinterpret_cast<const float4*>(a.slots)[(size_t)(2 * cc + 2) * PER + e];
+      acc.x += v0.x + v1.x;
+      acc.y += v0.y + v1.y;
+      acc.z += v0.z + v1.z;
+      acc.w += v0.w + v1.w;
+    }
+    if (cc <= c_last) {
+      const float4 v = reinterpret_cast<const float4*>(a.slots)[(size_t)(2 * cc) * PER + e];
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
@@ -100,12 +119,14 @@ __device__ void fixup_key_tile(const BwdArgs& a, int boundary) {
   }
 }
 
-// Blocks [0, dq_blocks) convert the dQ accumulator; blocks after them, one per
-// CTA boundary of a persistent main kernel, finish the shared key tiles.
+// Blocks [0, dq_blocks) convert the dQ accumulator; blocks after them,
+// kFixupParts per CTA boundary of a persistent main kernel, finish the shared
+// key tiles.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) bwd_finalize_fixup_kernel(const BwdArgs a, int dq_blocks) {
   if ((int)blockIdx.x >= dq_blocks) {
-    fixup_key_tile<D, F16>(a, (int)blockIdx.x - dq_blocks);
+    const int k = (int)blockIdx.x - dq_blocks;
+    fixup_key_tile<D, F16>(a, k / kFixupParts, k % kFixupParts);
     return;
   }
   const long long n8 = (long long)a.B * a.H * a.N * D / 8;
@@ -160,7 +181,7 @@ cudaError_t pre_t(const BwdArgs& a, cudaStream_t s) {
 
 template <int D, bool F16>
 cudaError_t fin_fixup_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
-  bwd_finalize_fixup_kernel<D, F16><<<dq_blocks + a.G - 1, 256, 0, s>>>(a, dq_blocks);
+  bwd_finalize_fixup_kernel<D, F16><<<dq_blocks + (a.G - 1) * kFixupParts, 256, 0, s>>>(a, dq_blocks);
   return cudaGetLastError();
 }
 
