@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
-SOURCES = ["fa_api.cu", "fwd_tc.cu", "fwd_f32.cu", "bwd_tc.cu", "bwd_persist.cu", "bwd_aux.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fwd_tc.cu", "fwd_persist.cu", "fwd_f32.cu", "bwd_tc.cu", "bwd_persist.cu", "bwd_aux.cu", "fa_noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "bwd_sched.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
