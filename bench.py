@@ -7,8 +7,9 @@ causal setting the workload runs, fa_fwd then the three fa_bwd stages
 (preprocess, main, finalize), all through the C ABI of libfa.so.  Inputs are
 resident in device memory; L2 is flushed (a 256 MiB write) between steps,
 outside the timed events.  The timed step is one CUDA graph holding those
-launches (captured once, replayed every step), bracketed by CUDA events on the
-launching stream; a separate pass launches the kernels one by one and brackets
+launches (captured once, replayed every step; the causal settings, which share
+only the inputs, are two concurrent branches of it), bracketed by CUDA events
+on the launching stream; a separate pass launches the kernels one by one and brackets
 every forward and every backward main kernel (the dominant kernel) with
 events, which gives the breakdown and the roofline figure.  FLOPs follow the usual
 convention: forward 4 B H N^2 d, backward 2.5 x forward, halved for causal,
@@ -364,20 +365,42 @@ def main():
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    def run_one(i, r, s, ev_main=None, ev_fwd=None):
+        if ev_fwd is not None:
+            ev_fwd[i][0].record(s)
+        fwd(fa, r, q, k, v, r["o"], r["lse"], s)
+        if ev_fwd is not None:
+            ev_fwd[i][1].record(s)
+        fa.bwd_preprocess(r["p"], r["o"], do, r["ws"], s)
+        if ev_main is not None:
+            ev_main[i][0].record(s)
+        fa.bwd_main(r["p"], q, k, v, do, r["lse"], r["dk"], r["dv"], r["ws"], s)
+        if ev_main is not None:
+            ev_main[i][1].record(s)
+        fa.bwd_finalize(r["p"], r["dq"], r["dk"], r["dv"], r["ws"], s)
+
     def step(s, ev_main=None, ev_fwd=None):
         for i, r in enumerate(runs):
-            if ev_fwd is not None:
-                ev_fwd[i][0].record(s)
-            fwd(fa, r, q, k, v, r["o"], r["lse"], s)
-            if ev_fwd is not None:
-                ev_fwd[i][1].record(s)
-            fa.bwd_preprocess(r["p"], r["o"], do, r["ws"], s)
-            if ev_main is not None:
-                ev_main[i][0].record(s)
-            fa.bwd_main(r["p"], q, k, v, do, r["lse"], r["dk"], r["dv"], r["ws"], s)
-            if ev_main is not None:
-                ev_main[i][1].record(s)
-            fa.bwd_finalize(r["p"], r["dq"], r["dk"], r["dv"], r["ws"], s)
+            run_one(i, r, s, ev_main, ev_fwd)
+
+    def step_branches(s):
+        # the causal settings are independent (same inputs, separate outputs and
+        # workspaces): one branch each, forked from and joined to `s`
+        if len(runs) == 1:
+            run_one(0, runs[0], s)
+            return
+        fork = torch.cuda.Event()
+        fork.record(s)
+        side_streams = [torch.cuda.Stream(dev) for _ in runs[1:]]
+        for b in side_streams:
+            b.wait_event(fork)
+        run_one(0, runs[0], s)
+        for i, (r, b) in enumerate(zip(runs[1:], side_streams), start=1):
+            run_one(i, r, b)
+        for b in side_streams:
+            join = torch.cuda.Event()
+            join.record(b)
+            s.wait_event(join)
 
     W = max(args.warmup, 3)
     for _ in range(W):
@@ -396,7 +419,7 @@ def main():
             side = torch.cuda.Stream(dev)
             side.wait_stream(stream)
             with torch.cuda.graph(graph, stream=side):
-                step(torch.cuda.current_stream())
+                step_branches(torch.cuda.current_stream())
             stream.wait_stream(side)
             graph.replay()
             torch.cuda.synchronize()
@@ -483,8 +506,9 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": dict(config_of(w, [r["splits"] for r in runs]),
-                           launch="one CUDA graph per step" if graph is not None
-                           else "kernels launched one by one"),
+                           launch=("one CUDA graph per step, the causal settings as concurrent "
+                                   "branches" if len(runs) > 1 else "one CUDA graph per step")
+                           if graph is not None else "kernels launched one by one"),
             "breakdown": {
                 "fwd_tflops": fwd_tflops, "bwd_main_tflops": achieved,
                 "fwd_frac_of_bf16_peak": fwd_tflops / peak,
