@@ -263,7 +263,9 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream):
     """Same metric with host buffers.  Every step copies its inputs from pinned host
     memory, runs the path, and copies every output back to pinned host memory.  The
     copies run on their own streams with double-buffered device tensors, so step i's
-    input copy and step i-1's output copy overlap step i's kernels."""
+    input copy and step i-1's output copy overlap step i's kernels; as in the timed
+    step, each causal setting runs on a stream of its own, and its outputs are copied
+    back on a copy stream of its own as soon as its kernels are done."""
     import torch
     names_in = ("q", "k", "v", "do")
     names_out = ("o", "lse", "dq", "dk", "dv")
@@ -274,38 +276,41 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream):
                 for r in runs]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for ho in host_out for t in ho.values())
-    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_h2d = torch.cuda.Stream(dev)
+    s_comp = [stream] + [torch.cuda.Stream(dev) for _ in runs[1:]]
+    s_d2h = [torch.cuda.Stream(dev) for _ in runs]
     E = lambda: torch.cuda.Event(enable_timing=False)
 
     def run(n):
         ev_h2d = [E() for _ in range(n)]
-        ev_comp = [E() for _ in range(n)]
-        ev_d2h = [E() for _ in range(n)]
+        ev_comp = [[E() for _ in runs] for _ in range(n)]
+        ev_d2h = [[E() for _ in runs] for _ in range(n)]
         for i in range(n):
             bsel = i % 2
             if i >= 2:
-                s_h2d.wait_event(ev_comp[i - 2])  # inputs of set bsel no longer read
+                for ev in ev_comp[i - 2]:
+                    s_h2d.wait_event(ev)  # inputs of set bsel no longer read
             with torch.cuda.stream(s_h2d):
                 for nm in names_in:
                     dev_in[bsel][nm].copy_(host_in[nm], non_blocking=True)
             ev_h2d[i].record(s_h2d)
-            stream.wait_event(ev_h2d[i])
-            if i >= 2:
-                stream.wait_event(ev_d2h[i - 2])  # outputs of set bsel copied out
             x = dev_in[bsel]
-            for r, o in zip(runs, dev_out[bsel]):
-                fwd(fa, r, x["q"], x["k"], x["v"], o["o"], o["lse"], stream)
-                fa.bwd_preprocess(r["p"], o["o"], x["do"], r["ws"], stream)
+            for j, (r, o) in enumerate(zip(runs, dev_out[bsel])):
+                cs = s_comp[j]
+                cs.wait_event(ev_h2d[i])
+                if i >= 2:
+                    cs.wait_event(ev_d2h[i - 2][j])  # outputs of set bsel copied out
+                fwd(fa, r, x["q"], x["k"], x["v"], o["o"], o["lse"], cs)
+                fa.bwd_preprocess(r["p"], o["o"], x["do"], r["ws"], cs)
                 fa.bwd_main(r["p"], x["q"], x["k"], x["v"], x["do"], o["lse"], o["dk"], o["dv"],
-                            r["ws"], stream)
-                fa.bwd_finalize(r["p"], o["dq"], o["dk"], o["dv"], r["ws"], stream)
-            ev_comp[i].record(stream)
-            s_d2h.wait_event(ev_comp[i])
-            with torch.cuda.stream(s_d2h):
-                for o, ho in zip(dev_out[bsel], host_out):
+                            r["ws"], cs)
+                fa.bwd_finalize(r["p"], o["dq"], o["dk"], o["dv"], r["ws"], cs)
+                ev_comp[i][j].record(cs)
+                s_d2h[j].wait_event(ev_comp[i][j])
+                with torch.cuda.stream(s_d2h[j]):
                     for nm in names_out:
-                        ho[nm].copy_(o[nm], non_blocking=True)
-            ev_d2h[i].record(s_d2h)
+                        host_out[j][nm].copy_(o[nm], non_blocking=True)
+                ev_d2h[i][j].record(s_d2h[j])
 
     run(2)
     torch.cuda.synchronize()
@@ -317,7 +322,8 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream):
     return {"value": step_flops * steps / s / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "host clock around all steps, synchronised on both sides",
-            "overlap": "copies on their own streams, double-buffered device tensors"}
+            "overlap": "copies on their own streams, double-buffered device tensors; one "
+                       "compute and one copy-back stream per causal setting"}
 
 
 def main():
