@@ -19,11 +19,14 @@
 // The score scale is applied once at the end: dK = scale * sum dS^T Q here,
 // dQ = scale * accumulator in the finalize kernel.
 //
-// Warp roles (320 threads): warps 0-3 and 4-7 are two compute warpgroups that
-// split the 128 query columns of every tile (TMEM lane = key row); warp 8 is
-// the producer (TMA copies of K_j, V_j once and of Q_i, dO_i through a ring,
-// plus each query tile's LSE and D staged by its lanes); warp 9 owns TMEM and
-// issues the MMAs.
+// Warp roles (32 (4 NG + 2) threads): warps 0 .. 4 NG - 1 form NG compute
+// warpgroups that split the 128 query columns of every tile into NG groups of
+// 128 / NG (TMEM lane = key row; warp w reads the lanes of quadrant w mod 4);
+// warp 4 NG is the producer (TMA copies of K_j, V_j once and of Q_i, dO_i
+// through a ring, plus each query tile's LSE and D staged by its lanes); warp
+// 4 NG + 1 owns TMEM and issues the MMAs.  More compute warps per SM
+// sub-partition hide more of the TMEM, shared-memory and barrier latencies of
+// the elementwise steps, which (with one CTA per SM) bound the loop.
 #include "ptx.cuh"
 
 namespace fa {
@@ -31,8 +34,20 @@ namespace {
 
 constexpr int kTile = 128;
 
-template <int D>
+template <int D, int NG>
 struct BwdLayout {
+  static_assert(NG == 2 || NG == 4, "compute warpgroups");
+  static_assert(D == 64 || NG == 2, "at d = 128 the dQ staging aliases dS^T per warp only with NG = 2");
+  static constexpr int CW = kTile / NG;   // query columns per compute warpgroup
+  static constexpr int KPG = CW / 16;     // MMA K steps (16 queries) per warpgroup
+  static constexpr int NCW = 4 * NG;      // compute warps
+  static constexpr int NT = 32 * (NCW + 2);
+  // dQ read-out: each compute warp stages boxes of 32 query rows x DQC fp32
+  // columns (128-byte rows with the 128-byte swizzle when DQC = 32, 64-byte
+  // rows with the 64-byte swizzle when DQC = 16) for the TMA reduce-add
+  static constexpr int DQG = D / NG;      // dQ columns per warpgroup
+  static constexpr int DQC = (NG == 2) ? 32 : 16;
+  static constexpr uint32_t BOXB = 32u * DQC * 4u;
   static constexpr uint32_t TILE = kTile * D * 2;
   static constexpr int NS = (D == 64) ? 3 : 2;         // Q/dO ring depth
   static constexpr uint32_t K = 0;
@@ -41,10 +56,12 @@ struct BwdLayout {
   static constexpr uint32_t DST = QS + NS * 2 * TILE;  // dS^T, 128 x 128 16-bit
   // per ring stage, the query tile's row statistics: [128] LSE*log2e then [128] D
   static constexpr uint32_t STAT = DST + kTile * kTile * 2;
-  // dQ staging (fp32, two 128 x 32 boxes): a buffer of its own at d = 64; at
-  // d = 128 shared memory is full and the dS^T buffer doubles as staging
+  // dQ staging (one box per compute warp, 32 KiB in all): a buffer of its own
+  // at d = 64; at d = 128 shared memory is full and the dS^T buffer doubles as
+  // staging
   static constexpr bool STG_SEP = (D == 64);
   static constexpr uint32_t STG = STG_SEP ? STAT + NS * 256 * 4 : DST;
+  static_assert(NCW * BOXB == 2 * kTile * 128, "staging size");
   static constexpr uint32_t BAR = STAT + NS * 256 * 4 + (STG_SEP ? 2 * kTile * 128 : 0);
   // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
   //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS],
@@ -54,21 +71,23 @@ struct BwdLayout {
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns.  S^T [0,128) (warpgroup g reads [64g, 64g+64)), dP^T [128,256),
-  // dV and dK d columns each.  At d = 64, dQ [384,448) and the 16-bit P^T
-  // [448,512) have columns of their own; at d = 128 the 512 columns are full, so
-  // dQ goes over dP^T and warpgroup g writes its P^T over [64g, 64g+32) of S^T.
+  // TMEM columns.  S^T [0,128) (warpgroup g reads [CW g, CW g + CW)), dP^T
+  // [128,256), dV and dK d columns each.  At d = 64, dQ [384,448) and the 16-bit
+  // P^T [448,512) have columns of their own; at d = 128 the 512 columns are
+  // full, so dQ goes over dP^T and warpgroup g writes its P^T over the first
+  // CW / 2 of its own S^T columns (which it has read by then).
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
   static constexpr bool ALIAS = (D == 128);
   static constexpr uint32_t T_DQ = ALIAS ? T_DP : 384;
   static constexpr uint32_t T_PT = ALIAS ? T_S : 448;
-  // column of P^T that holds query pair kk*8 .. kk*8+7 (16 queries), and the
-  // columns warpgroup g writes
+  // first of the 8 P^T columns that hold queries 16 kk .. 16 kk + 15 (as
+  // 16-bit pairs), and the first of the CW / 2 columns warpgroup g writes
   __device__ static constexpr uint32_t pt_col(int kk) {
-    return ALIAS ? 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3) : T_PT + 8u * (uint32_t)kk;
+    return ALIAS ? (uint32_t)CW * (uint32_t)(kk / KPG) + 8u * (uint32_t)(kk % KPG)
+                 : T_PT + 8u * (uint32_t)kk;
   }
   __device__ static constexpr uint32_t pt_write_col(int g) {
-    return ALIAS ? 64u * (uint32_t)g : T_PT + 32u * (uint32_t)g;
+    return ALIAS ? (uint32_t)CW * (uint32_t)g : T_PT + (uint32_t)(CW / 2) * (uint32_t)g;
   }
 };
 
@@ -99,13 +118,14 @@ __device__ __forceinline__ float d_of(const BwdArgs& a, int bh, int q) {
   return q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
 }
 
-template <int D, bool F16>
-__global__ void __launch_bounds__(320, 1)
+template <int D, bool F16, int NG>
+__global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, NG>;
   constexpr int NS = L::NS;
+  constexpr int kProd = L::NCW, kMma = L::NCW + 1;  // producer and MMA warps
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,18 +156,18 @@ __global__ void __launch_bounds__(320, 1)
   // barrier, already issues the copies that need no wait (K_j, V_j and the
   // first NS query tiles' Q, dO), so that their latency overlaps the TMEM
   // allocation.  The statistics of those stages are staged after the barrier.
-  const bool producer = (warp == 8 && lane == 0);
+  const bool producer = (warp == kProd && lane == 0);
   int pre = 0;  // producer lane: query-tile stages already being copied
   if (producer) {
     mbar_init(bar_kv, 1);
     mbar_init(bar_s_full, 1);
     mbar_init(bar_dp_full, 1);
-    mbar_init(bar_dp_free, 8);
-    mbar_init(bar_p_full, 8);
-    mbar_init(bar_ds_full, 8);
+    mbar_init(bar_dp_free, L::NCW);
+    mbar_init(bar_p_full, L::NCW);
+    mbar_init(bar_ds_full, L::NCW);
     mbar_init(bar_ds_free, 1);
     mbar_init(bar_dq_full, 1);
-    mbar_init(bar_dq_free, 8);
+    mbar_init(bar_dq_free, L::NCW);
     mbar_init(bar_done, 1);
     mbar_init(bar_pt_free, 1);
     for (int s = 0; s < NS; ++s) {
@@ -175,7 +195,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   }
-  if (warp == 9) {
+  if (warp == kMma) {
     tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
     tmem_relinquish();
   }
@@ -184,7 +204,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
 
-  if (warp == 8) {
+  if (warp == kProd) {
     // ------------------------------------------------------------ producer
     // Lane 0 issues the TMA copies; every lane also stages four rows of the
     // query tile's statistics into the ring stage, so that the stage's full
@@ -227,7 +247,7 @@ __global__ void __launch_bounds__(320, 1)
         if (n > 0) mbar_drain(w, bar_qf(s), (n - 1) & 1);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMma) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop converged (waits are warp-uniform); one
     // elected lane issues each MMA and commit.
@@ -356,17 +376,18 @@ __global__ void __launch_bounds__(320, 1)
     // Software-pipelined per query tile i:  dS_i | P_{i+1} | dQ_i, so that the
     // exponentials of the next tile run while the tensor core computes dK_i,
     // dQ_i and dP^T_{i+1}.
-    const int g = warp >> 2;                 // 0: query columns 0-63, 1: 64-127
+    constexpr int CW = L::CW;
+    const int g = warp >> 2;                 // query columns [CW g, CW g + CW)
     const int r = (warp & 3) * 32 + lane;    // key row in the tile = TMEM lane
     const int key = kt * kTile + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint64_t c2p = f2pack(a.scale_log2, a.scale_log2);
     const bool rows_out = __any_sync(0xffffffffu, key >= a.N);  // a tail key tile
-    // dQ staging: this warp's 4 KiB, laid out as the 128-byte-swizzled box
-    // {32 columns, 32 rows} of tmdQ.  Each warp reduces its own box, so no warp
+    // dQ staging: this warp's box {DQC columns, 32 rows} of the dQ accumulator
+    // map, with that map's swizzle.  Each warp reduces its own box, so no warp
     // waits for another.  The TMA reduce reads the box asynchronously; the box
     // is released lazily, when it is about to be written again.
-    const uint32_t stg = sb + L::STG + (uint32_t)g * (kTile * 128) + (uint32_t)(warp & 3) * 4096u;
+    const uint32_t stg = sb + L::STG + (uint32_t)warp * L::BOXB;
     bool pend = false;  // a reduce may still be reading the box
     auto stg_acquire = [&]() {
       if (pend) {
@@ -378,7 +399,7 @@ __global__ void __launch_bounds__(320, 1)
     auto stat = [&](int it) {
       return reinterpret_cast<const float*>(smem + L::STAT) + (it % NS) * 256;
     };
-    float p[64];
+    float p[CW];
     // S^T -> P^T: fp32 in p[] for dS, 16-bit into TMEM for dV; then p_full
     auto p_phase = [&](int it, int qtile) -> bool {
       // the stage's statistics (staged by the producer with Q and dO)
@@ -386,17 +407,17 @@ __global__ void __launch_bounds__(320, 1)
       if (!warp_wait(w, bar_s_full, it & 1)) return false;
       tc_fence_after();
       {
-        uint32_t u[64];
-        tmem_ld64(tmem + L::T_S + lane_off + 64 * g, u);
+        uint32_t u[CW];
+        tmem_ld_n<CW>(tmem + L::T_S + lane_off + CW * g, u);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(u[c]);
+        for (int c = 0; c < CW; ++c) p[c] = __uint_as_float(u[c]);
       }
-      const float4* nl4 = reinterpret_cast<const float4*>(stat(it) + 64 * g);  // -LSE*log2(e)
-      const int q0 = qtile * kTile + 64 * g;
+      const float4* nl4 = reinterpret_cast<const float4*>(stat(it) + CW * g);  // -LSE*log2(e)
+      const int q0 = qtile * kTile + CW * g;
       const bool diag = a.m.causal && qtile == kt;
-      uint32_t pk[32];
+      uint32_t pk[CW / 2];
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
+      for (int c = 0; c < CW; c += 4) {
         const float4 nl = nl4[c / 4];
         float x0, x1, x2, x3;
         f2unpack(ffma2(f2pack(p[c], p[c + 1]), c2p, f2pack(nl.x, nl.y)), x0, x1);
@@ -408,11 +429,11 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (rows_out || diag) {  // warp-uniform: only tail and diagonal tiles mask
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < CW; ++c)
           if (key >= a.N || (diag && q0 + c < key)) p[c] = 0.f;
       }
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
+      for (int c = 0; c < CW; c += 2) pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
       if constexpr (!L::ALIAS) {
         // d = 64: P^T has one buffer; dV of the previous tile must be done with it
         // (at d = 128 P^T goes over S^T, which s_full already orders after dV)
@@ -421,7 +442,7 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
         }
       }
-      tmem_st32(tmem + L::pt_write_col(g) + lane_off, pk);
+      tmem_st_n<CW / 2>(tmem + L::pt_write_col(g) + lane_off, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -437,16 +458,16 @@ __global__ void __launch_bounds__(320, 1)
       // ---- dS_i = P_i * (dP_i - D)
       if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
       tc_fence_after();
-      uint32_t pk[32];
+      uint32_t pk[CW / 2];
       {
-        uint32_t u[64];
-        tmem_ld64(tmem + L::T_DP + lane_off + 64 * g, u);
+        uint32_t u[CW];
+        tmem_ld_n<CW>(tmem + L::T_DP + lane_off + CW * g, u);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_dp_free);
-        const float4* nd4 = reinterpret_cast<const float4*>(stat(it) + 128 + 64 * g);  // -D
+        const float4* nd4 = reinterpret_cast<const float4*>(stat(it) + 128 + CW * g);  // -D
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < CW; c += 4) {
           const float4 nd = nd4[c / 4];
           float y0, y1, y2, y3;
           f2unpack(fmul2(f2pack(p[c], p[c + 1]),
@@ -463,8 +484,8 @@ __global__ void __launch_bounds__(320, 1)
       // at d = 128 the last dQ reduction must have finished reading this region
       if (!L::STG_SEP) stg_acquire();
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        st_shared_v4(sb + L::DST + sw128_chunk_offset(r, 8 * g + ch, kTile), pk[ch * 4 + 0],
+      for (int ch = 0; ch < CW / 8; ++ch)
+        st_shared_v4(sb + L::DST + sw128_chunk_offset(r, (CW / 8) * g + ch, kTile), pk[ch * 4 + 0],
                      pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
       fence_async_smem();
       tc_fence_before();
@@ -477,27 +498,27 @@ __global__ void __launch_bounds__(320, 1)
       // ---- dQ_i (TMEM lane = query row) -> fp32 accumulator by TMA reduce-add
       if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
       tc_fence_after();
-      uint32_t dq[D / 2];
-      if constexpr (D == 64) {
-        tmem_ld32(tmem + L::T_DQ + lane_off + g * (D / 2), *reinterpret_cast<uint32_t(*)[32]>(dq));
-      } else {
-        tmem_ld64(tmem + L::T_DQ + lane_off + g * (D / 2), *reinterpret_cast<uint32_t(*)[64]>(dq));
-      }
+      uint32_t dq[L::DQG];
+      tmem_ld_n<L::DQG>(tmem + L::T_DQ + lane_off + g * L::DQG, dq);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_free);
 #pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+      for (int c0 = 0; c0 < L::DQG; c0 += L::DQC) {
         stg_acquire();
-        // row `lane` of this warp's 32, 16-byte chunk x at x ^ (row & 7)
+        // row `lane` of this warp's 32: with 128-byte rows, 16-byte chunk x at
+        // x ^ (row mod 8); with 64-byte rows, at x ^ ((row / 2) mod 4) (the two
+        // swizzles of the map, address bits 4-6 or 4-5 xor bits 7-9 or 7-8)
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
-          st_shared_v4(stg + (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16), dq[c0 + 4 * x],
-                       dq[c0 + 4 * x + 1], dq[c0 + 4 * x + 2], dq[c0 + 4 * x + 3]);
+        for (int x = 0; x < L::DQC / 4; ++x) {
+          const uint32_t off = (L::DQC == 32) ? (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16)
+                                              : (uint32_t)lane * 64u + (uint32_t)((x ^ ((lane >> 1) & 3)) * 16);
+          st_shared_v4(stg + off, dq[c0 + 4 * x], dq[c0 + 4 * x + 1], dq[c0 + 4 * x + 2], dq[c0 + 4 * x + 3]);
+        }
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&tmdQ, stg, g * (D / 2) + c0, qt * kTile + (warp & 3) * 32, bh);
+          tma_reduce_add_3d(&tmdQ, stg, g * L::DQG + c0, qt * kTile + (warp & 3) * 32, bh);
           bulk_commit_group();
         }
         pend = true;
@@ -517,23 +538,24 @@ __global__ void __launch_bounds__(320, 1)
     // `ok`/`have` is warp-uniform); only the stores are predicated on the row
     if (ok) {
       const bool store = key < a.N;
-      uint16_t* dVrow = reinterpret_cast<uint16_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * (D / 2);
-      uint16_t* dKrow = reinterpret_cast<uint16_t*>(a.dK) + ((size_t)bh * a.N + key) * D + g * (D / 2);
+      constexpr int EC = L::DQG < 32 ? L::DQG : 32;  // columns per TMEM load
+      uint16_t* dVrow = reinterpret_cast<uint16_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * L::DQG;
+      uint16_t* dKrow = reinterpret_cast<uint16_t*>(a.dK) + ((size_t)bh * a.N + key) * D + g * L::DQG;
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which == 0 ? L::T_DV : L::T_DK) + g * (D / 2);
+        const uint32_t col = (which == 0 ? L::T_DV : L::T_DK) + g * L::DQG;
         const float mul = which == 0 ? 1.f : a.scale;
         uint16_t* dst = which == 0 ? dVrow : dKrow;
 #pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t u[32];
+        for (int c0 = 0; c0 < L::DQG; c0 += EC) {
+          uint32_t u[EC];
           if (have) {
-            tmem_ld32(tmem + col + lane_off + c0, u);
+            tmem_ld_n<EC>(tmem + col + lane_off + c0, u);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = 0u;
+            for (int i = 0; i < EC; ++i) u[i] = 0u;
           }
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int v = 0; v < EC / 8; ++v) {
             uint4 pq;
             pq.x = pack2<F16>(__uint_as_float(u[v * 8 + 0]) * mul, __uint_as_float(u[v * 8 + 1]) * mul);
             pq.y = pack2<F16>(__uint_as_float(u[v * 8 + 2]) * mul, __uint_as_float(u[v * 8 + 3]) * mul);
@@ -548,7 +570,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMma) {
     tc_fence_after();
     tmem_dealloc(tmem, L::TMEM_COLS);
   }
@@ -556,13 +578,20 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, bool F16>
 cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
-  using L = BwdLayout<D>;
-  auto kern = bwd_tc_kernel<D, F16>;
+  // four compute warpgroups at d = 64; two at d = 128, where the dQ staging
+  // shares the dS^T buffer: with two, the dS^T rows a warp writes are exactly
+  // its own staging box (so waiting for its own reduce to finish reading is
+  // enough); with four they would fall into other warps' boxes
+  constexpr int NG = (D == 64) ? 4 : 2;
+  using L = BwdLayout<D, NG>;
+  auto kern = bwd_tc_kernel<D, F16, NG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   // the first a.direct key tiles, one CTA each (the rest, if any, go to the
   // persistent kernel)
-  kern<<<(unsigned)a.direct, 320, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], a);
+  // the dQ accumulator map whose box matches the staging: {32, 32} with the
+  // 128-byte swizzle (tm[4]) or {16, 32} with the 64-byte swizzle (tm[5])
+  kern<<<(unsigned)a.direct, L::NT, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], tm[L::DQC == 32 ? 4 : 5], a);
   return cudaGetLastError();
 }
 

@@ -156,9 +156,10 @@ fa_status encode_bhnd(CUtensorMap* m, const void* ptr, const fa_params* p) {
 }
 
 // The fp32 dQ accumulator [B*H][N][d] as a 3-D TMA map {d, N, B*H}; box
-// {32, 32, 1} (128-byte rows, one warp's slice), 128-byte swizzle; rows past N
-// are not written.
-fa_status encode_dqacc(CUtensorMap* m, const float* ptr, const fa_params* p) {
+// {cols, 32, 1} (one warp's slice of 32 rows): 32 columns (128-byte rows) with
+// the 128-byte swizzle or 16 columns (64-byte rows) with the 64-byte swizzle;
+// rows past N are not written.
+fa_status encode_dqacc(CUtensorMap* m, const float* ptr, const fa_params* p, int cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_err("cuTensorMapEncodeTiled is not available from the driver");
@@ -166,10 +167,11 @@ fa_status encode_dqacc(CUtensorMap* m, const float* ptr, const fa_params* p) {
   }
   const cuuint64_t dims[3] = {(cuuint64_t)p->d, (cuuint64_t)p->N, (cuuint64_t)p->B * p->H};
   const cuuint64_t strides[2] = {(cuuint64_t)p->d * 4, (cuuint64_t)p->N * p->d * 4};
-  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t box[3] = {(cuuint32_t)cols, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_err("cuTensorMapEncodeTiled (dQ accumulator) failed (CUresult %d)", (int)r);
@@ -617,12 +619,13 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
   a.dK = dK;
   a.dV = dV;
   a.rep = make_report(st);
-  CUtensorMap tm[5];
+  CUtensorMap tm[6];
   FA_TRY(encode_bhnd(&tm[0], Q, p));
   FA_TRY(encode_bhnd(&tm[1], K, p));
   FA_TRY(encode_bhnd(&tm[2], V, p));
   FA_TRY(encode_bhnd(&tm[3], dO, p));
-  FA_TRY(encode_dqacc(&tm[4], a.dQacc, p));
+  FA_TRY(encode_dqacc(&tm[4], a.dQacc, p, 32));
+  FA_TRY(encode_dqacc(&tm[5], a.dQacc, p, 16));
   cudaError_t e = cudaSuccess;
   if (a.direct > 0) e = launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess && a.G > 0)
