@@ -20,6 +20,18 @@ Functions and the passages they follow:
   the definition ("Passe arrière : recalculer au lieu de stocker" only says that
   P is recomputed from the saved statistics; the formulas are calculus).
 
+* ``philox4x32_10`` / ``dropout_keep`` -- the counter-based generator that
+  decides which attention weights dropout keeps (Salmon et al., SC 2011; the
+  pages fuse dropout into the kernel -- "Fusão de Kernels", reading guide -- and
+  pass ``dropout_p`` to the attention call -- "L'intégration est de huit
+  lignes", marketmaker.cc -- but name no generator).
+
+Dropout (``dropout_p`` > 0): each weight P_ij of head bh = b * H + h is kept
+and scaled by 1 / (1 - p) when word (j mod 4) of Philox4x32-10 with counter
+(j // 4, i, bh, offset) and key (seed mod 2^32, seed // 2^32) is at least
+floor(p * 2^32), else set to 0; m, l and LSE stay those of the undropped
+softmax.
+
 Masks: ``mask`` is a uint8 array of shape [T, T] (shared by every batch and
 head) or [B, H, T, T], with T = ceil(N / mask_block); entry [i // mb, j // mb]
 keeps (1) or hides (0) the pair (query i, key j) ("Extensão: Block-Sparse
@@ -62,16 +74,22 @@ def _load():
     Dd = ctypes.c_double
     F = ctypes.c_float
     lib.orc_num_threads.restype = I
-    lib.orc_fwd.argtypes = [I, I, I, I, P, P, P, Dd, I, P, I, LL, LL, P, P]
-    lib.orc_fwd_rows.argtypes = [I, I, P, P, P, Dd, I, P, I, I, P, P, P]
+    U64 = ctypes.c_ulonglong
+    U32 = ctypes.c_uint
+    lib.orc_fwd.argtypes = [I, I, I, I, P, P, P, Dd, I, P, I, LL, LL, P, P, Dd, U64, U32]
+    lib.orc_fwd_rows.argtypes = [I, I, P, P, P, Dd, I, P, I, I, P, P, P, Dd, U64, U32, I]
     lib.orc_fwd_blockwise_f64.argtypes = [I, I, I, I, P, P, P, Dd, I, P, I, LL, LL,
                                           I, I, I, P, P]
     lib.orc_fwd_blockwise_f32.argtypes = [I, I, I, I, P, P, P, F, I, P, I, LL, LL,
                                           I, I, I, P, P]
-    lib.orc_bwd.argtypes = [I, I, I, I, P, P, P, P, Dd, I, P, I, LL, LL, P, P, P]
-    lib.orc_bwd_rows.argtypes = [I, I, P, P, P, P, Dd, I, P, I, I, P, P, I, P, P, P]
+    lib.orc_bwd.argtypes = [I, I, I, I, P, P, P, P, Dd, I, P, I, LL, LL, P, P, P, Dd, U64, U32]
+    lib.orc_bwd_rows.argtypes = [I, I, P, P, P, P, Dd, I, P, I, I, P, P, I, P, P, P, Dd, U64,
+                                 U32, I]
+    lib.orc_philox4x32_10.argtypes = [P, P, P]
+    lib.orc_dropout_keep.argtypes = [I, I, I, Dd, U64, U32, P]
     for f in ("orc_fwd", "orc_fwd_rows", "orc_fwd_blockwise_f64",
-              "orc_fwd_blockwise_f32", "orc_bwd", "orc_bwd_rows"):
+              "orc_fwd_blockwise_f32", "orc_bwd", "orc_bwd_rows", "orc_philox4x32_10",
+              "orc_dropout_keep"):
         getattr(lib, f).restype = None
     _lib = lib
     return lib
@@ -118,7 +136,32 @@ def _head_mask(mask, b, h, N, mask_block):
     return np.ascontiguousarray(m)
 
 
-def attention_fwd(q, k, v, scale, causal=False, mask=None, mask_block=128):
+def _drop(dropout_p, seed, offset):
+    p = float(dropout_p)
+    if not 0.0 <= p < 1.0:
+        raise ValueError(f"dropout_p {p} is not in [0, 1)")
+    return p, int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """Philox4x32-10 of one counter (4 uint32) under one key (2 uint32) -> 4 uint32."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32).reshape(4))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(2))
+    out = np.zeros(4, dtype=np.uint32)
+    _load().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def dropout_keep(B, H, N, dropout_p, seed=0, offset=0) -> np.ndarray:
+    """Dropout's keep decisions [B,H,N,N] (uint8, 1 = kept) for every (query, key)."""
+    p, seed, offset = _drop(dropout_p, seed, offset)
+    keep = np.zeros((B, H, N, N), dtype=np.uint8)
+    _load().orc_dropout_keep(B, H, N, p, seed, offset, _ptr(keep))
+    return keep
+
+
+def attention_fwd(q, k, v, scale, causal=False, mask=None, mask_block=128, dropout_p=0.0,
+                  seed=0, offset=0):
     """Direct forward over whole [B,H,N,d] tensors -> (O [B,H,N,d], LSE [B,H,N]), fp64."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
@@ -126,12 +169,15 @@ def attention_fwd(q, k, v, scale, causal=False, mask=None, mask_block=128):
     LSE = np.zeros((B, H, N), dtype=np.float64)
     mp, keep, sb, sh = _mask_args(mask, B, H, N, mask_block)
     _load().orc_fwd(B, H, N, d, _ptr(q), _ptr(k), _ptr(v), float(scale), int(bool(causal)),
-                    mp, int(mask_block), sb, sh, _ptr(O), _ptr(LSE))
+                    mp, int(mask_block), sb, sh, _ptr(O), _ptr(LSE),
+                    *_drop(dropout_p, seed, offset))
     return O, LSE
 
 
-def attention_fwd_rows(qh, kh, vh, rows, scale, causal=False, mask_h=None, mask_block=128):
-    """Direct forward of selected query rows of one head ([N,d] tensors).
+def attention_fwd_rows(qh, kh, vh, rows, scale, causal=False, mask_h=None, mask_block=128,
+                       dropout_p=0.0, seed=0, offset=0, bh=0):
+    """Direct forward of selected query rows of one head ([N,d] tensors; bh = b * H + h
+    is the head's index, which dropout's counter uses).
 
     Returns (O_rows [len(rows), d], LSE_rows [len(rows)]).
     """
@@ -143,7 +189,7 @@ def attention_fwd_rows(qh, kh, vh, rows, scale, causal=False, mask_h=None, mask_
     m = None if mask_h is None else np.ascontiguousarray(np.asarray(mask_h, dtype=np.uint8))
     _load().orc_fwd_rows(N, d, _ptr(qh), _ptr(kh), _ptr(vh), float(scale), int(bool(causal)),
                          None if m is None else _ptr(m), int(mask_block), len(rows),
-                         _ptr(rows), _ptr(O), _ptr(L))
+                         _ptr(rows), _ptr(O), _ptr(L), *_drop(dropout_p, seed, offset), int(bh))
     return O, L
 
 
@@ -164,7 +210,8 @@ def attention_fwd_blockwise(q, k, v, scale, Br, Bc, causal=False, mask=None, mas
     return O, LSE
 
 
-def attention_bwd(q, k, v, do, scale, causal=False, mask=None, mask_block=128):
+def attention_bwd(q, k, v, do, scale, causal=False, mask=None, mask_block=128, dropout_p=0.0,
+                  seed=0, offset=0):
     """Gradients (dQ, dK, dV) of sum(dO * O) over whole [B,H,N,d] tensors, fp64."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, d = q.shape
@@ -172,12 +219,12 @@ def attention_bwd(q, k, v, do, scale, causal=False, mask=None, mask_block=128):
     mp, keep, sb, sh = _mask_args(mask, B, H, N, mask_block)
     _load().orc_bwd(B, H, N, d, _ptr(q), _ptr(k), _ptr(v), _ptr(do), float(scale),
                     int(bool(causal)), mp, int(mask_block), sb, sh,
-                    _ptr(dQ), _ptr(dK), _ptr(dV))
+                    _ptr(dQ), _ptr(dK), _ptr(dV), *_drop(dropout_p, seed, offset))
     return dQ, dK, dV
 
 
 def attention_bwd_rows(qh, kh, vh, doh, qrows, krows, scale, causal=False, mask_h=None,
-                       mask_block=128):
+                       mask_block=128, dropout_p=0.0, seed=0, offset=0, bh=0):
     """Gradients of selected rows of one head: dQ[qrows], dK[krows], dV[krows]."""
     qh, kh, vh, doh = _f64(qh), _f64(kh), _f64(vh), _f64(doh)
     N, d = qh.shape
@@ -189,7 +236,8 @@ def attention_bwd_rows(qh, kh, vh, doh, qrows, krows, scale, causal=False, mask_
     m = None if mask_h is None else np.ascontiguousarray(np.asarray(mask_h, dtype=np.uint8))
     _load().orc_bwd_rows(N, d, _ptr(qh), _ptr(kh), _ptr(vh), _ptr(doh), float(scale),
                          int(bool(causal)), None if m is None else _ptr(m), int(mask_block),
-                         len(qr), _ptr(qr), _ptr(dQ), len(kr), _ptr(kr), _ptr(dK), _ptr(dV))
+                         len(qr), _ptr(qr), _ptr(dQ), len(kr), _ptr(kr), _ptr(dK), _ptr(dV),
+                         *_drop(dropout_p, seed, offset), int(bh))
     return dQ, dK, dV
 
 

@@ -31,15 +31,90 @@
  *   - a row whose allowed set is empty has O_i = 0 and LSE_i = -inf, and it
  *     contributes nothing to any gradient;
  *   - the backward formulas are the derivative of the definition (the pages only
- *     say that S and P are recomputed from Q, K, V and the saved statistics).
+ *     say that S and P are recomputed from Q, K, V and the saved statistics);
+ *   - dropout ("Fusão de Kernels" among the "Ideias centrais" of the reading
+ *     guide fuses it into the same kernel; the integration code of "L'intégration
+ *     est de huit lignes", marketmaker.cc, passes dropout_p to the attention
+ *     call) acts on the attention weights after the softmax: each weight P_ij is
+ *     kept with probability 1 - p and scaled by 1/(1 - p), or set to 0.  The
+ *     statistics m, l and LSE stay those of the undropped softmax.  The pages
+ *     name no random-number generator; the keep decisions come from the
+ *     counter-based generator Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+ *     "Parallel random numbers: as easy as 1, 2, 3", SC 2011), so that a
+ *     backward pass regenerates them instead of storing them: for head bh,
+ *     query row i and key j, the word (j mod 4) of Philox4x32-10 with counter
+ *     (floor(j / 4), i, bh, offset) and key (seed mod 2^32, floor(seed / 2^32))
+ *     keeps the weight when it is at least t = floor(p * 2^32).
  */
 #include <math.h>
 #include <stddef.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10, written from its definition in Salmon et al. (SC 2011): a    */
+/* counter of four 32-bit words and a key of two go through ten rounds of      */
+/*   (x0, x1, x2, x3) -> (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1,  */
+/*                        lo(M0 x0))                                           */
+/* with M0 = 0xD2511F53, M1 = 0xCD9E8D57 and hi/lo the halves of the 64-bit    */
+/* product; the key is bumped by the Weyl constants (0x9E3779B9, 0xBB67AE85)   */
+/* before every round but the first.                                           */
+/* ------------------------------------------------------------------------ */
+static void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        uint64_t p0 = (uint64_t)0xD2511F53u * (uint64_t)x0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint64_t)x2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t n0 = hi1 ^ x1 ^ k0, n2 = hi0 ^ x3 ^ k1;
+        x0 = n0;
+        x1 = lo1;
+        x2 = n2;
+        x3 = lo0;
+    }
+    out[0] = x0;
+    out[1] = x1;
+    out[2] = x2;
+    out[3] = x3;
+}
+
+void orc_philox4x32_10(const uint32_t *ctr, const uint32_t *key, uint32_t *out)
+{
+    philox4x32_10(ctr, key, out);
+}
+
+/* Dropout of one call: off when p == 0. */
+typedef struct {
+    int on;
+    uint32_t t;     /* keep when the word is >= t = floor(p * 2^32) */
+    double z;       /* 1 / (1 - p) */
+    uint32_t key[2];
+    uint32_t offset;
+} drop_cfg;
+
+static drop_cfg make_drop(double p, unsigned long long seed, unsigned int offset)
+{
+    drop_cfg g;
+    g.on = p > 0.0;
+    double t = floor(p * 4294967296.0);
+    g.t = t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
+    g.z = g.on ? 1.0 / (1.0 - p) : 1.0;
+    g.key[0] = (uint32_t)(seed & 0xFFFFFFFFull);
+    g.key[1] = (uint32_t)(seed >> 32);
+    g.offset = offset;
+    return g;
+}
 
 typedef struct {
     int N, d;
@@ -48,12 +123,46 @@ typedef struct {
     const unsigned char *mask; /* this head's block mask, or NULL */
     int mask_block;            /* tokens per mask entry */
     int mask_cols;             /* ceil(N / mask_block) */
+    drop_cfg drop;
+    int bh;                    /* b * H + h, part of the dropout counter */
 } head_cfg;
+
+/* The factor dropout applies to weight (i, j) of this head: 1 without dropout,
+ * else 1 / (1 - p) or 0. */
+static double drop_factor(const head_cfg *c, int i, int j)
+{
+    if (!c->drop.on)
+        return 1.0;
+    uint32_t ctr[4] = {(uint32_t)j >> 2, (uint32_t)i, (uint32_t)c->bh, c->drop.offset};
+    uint32_t w[4];
+    philox4x32_10(ctr, c->drop.key, w);
+    return w[j & 3] >= c->drop.t ? c->drop.z : 0.0;
+}
+
+/* Keep decisions of every (b, h, i, j) as bytes [B][H][N][N] (1 = kept). */
+void orc_dropout_keep(int B, int H, int N, double p, unsigned long long seed,
+                      unsigned int offset, unsigned char *keep)
+{
+    drop_cfg g = make_drop(p, seed, offset);
+    const long long rows = (long long)B * H * N;
+#pragma omp parallel for schedule(static)
+    for (long long r = 0; r < rows; ++r) {
+        int bh = (int)(r / N), i = (int)(r % N);
+        for (int j = 0; j < N; ++j) {
+            uint32_t ctr[4] = {(uint32_t)j >> 2, (uint32_t)i, (uint32_t)bh, g.offset};
+            uint32_t w[4];
+            philox4x32_10(ctr, g.key, w);
+            keep[(size_t)r * N + j] = (unsigned char)(!g.on || w[j & 3] >= g.t);
+        }
+    }
+}
 
 static head_cfg make_cfg(int N, int d, double scale, int causal,
                          const unsigned char *mask_h, int mask_block)
 {
     head_cfg c;
+    c.drop = make_drop(0.0, 0, 0);
+    c.bh = 0;
     c.N = N;
     c.d = d;
     c.scale = scale;
@@ -91,7 +200,7 @@ static double dot(const double *a, const double *b, int d)
 /*   s_j = scale * q_i . k_j          (j in A_i)                               */
 /*   m   = max_j s_j                                                           */
 /*   l   = sum_j exp(s_j - m)                                                  */
-/*   O_i = sum_j exp(s_j - m) / l * v_j                                        */
+/*   O_i = sum_j exp(s_j - m) / l * z_ij * v_j   (z: the dropout factor)       */
 /*   LSE = m + ln l                                                            */
 /* s is caller scratch of N doubles.                                           */
 /* ------------------------------------------------------------------------ */
@@ -121,7 +230,7 @@ static void fwd_row(const head_cfg *c, const double *Qh, const double *Kh,
     for (int j = 0; j < N; ++j) {
         if (!allowed(c, i, j))
             continue;
-        double w = exp(s[j] - m) / l;
+        double w = exp(s[j] - m) / l * drop_factor(c, i, j);
         const double *v = Vh + (size_t)j * d;
         for (int k = 0; k < d; ++k)
             o[k] += w * v[k];
@@ -151,8 +260,10 @@ static const unsigned char *head_mask(const unsigned char *mask, long long sb,
 void orc_fwd(int B, int H, int N, int d, const double *Q, const double *K,
              const double *V, double scale, int causal,
              const unsigned char *mask, int mask_block, long long sb,
-             long long sh, double *O, double *LSE)
+             long long sh, double *O, double *LSE, double drop_p,
+             unsigned long long seed, unsigned int offset)
 {
+    const drop_cfg g = make_drop(drop_p, seed, offset);
     const long long rows = (long long)B * H * N;
 #pragma omp parallel
     {
@@ -163,6 +274,8 @@ void orc_fwd(int B, int H, int N, int d, const double *Q, const double *K,
             int b = bh / H, h = bh % H;
             head_cfg c = make_cfg(N, d, scale, causal,
                                   head_mask(mask, sb, sh, b, h), mask_block);
+            c.drop = g;
+            c.bh = bh;
             size_t base = (size_t)bh * N * d;
             fwd_row(&c, Q + base, K + base, V + base, i, s,
                     O + base + (size_t)i * d, LSE + (size_t)bh * N + i);
@@ -171,14 +284,18 @@ void orc_fwd(int B, int H, int N, int d, const double *Q, const double *K,
     }
 }
 
-/* Forward of selected query rows of one head (the head's tensors are [N][d]).
+/* Forward of selected query rows of one head (the head's tensors are [N][d];
+ * bh is the head's index b * H + h, used by dropout only).
  * O_rows is [nrows][d], LSE_rows is [nrows]. */
 void orc_fwd_rows(int N, int d, const double *Qh, const double *Kh,
                   const double *Vh, double scale, int causal,
                   const unsigned char *mask_h, int mask_block, int nrows,
-                  const int *rows, double *O_rows, double *LSE_rows)
+                  const int *rows, double *O_rows, double *LSE_rows, double drop_p,
+                  unsigned long long seed, unsigned int offset, int bh)
 {
     head_cfg c = make_cfg(N, d, scale, causal, mask_h, mask_block);
+    c.drop = make_drop(drop_p, seed, offset);
+    c.bh = bh;
 #pragma omp parallel
     {
         double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
@@ -311,10 +428,10 @@ DEFINE_BLOCKWISE(orc_fwd_blockwise_f32, float, expf, logf)
 /* derivative of O = softmax(scale * Q K^T) V with respect to Q, K and V for   */
 /* the loss whose gradient at O is dO):                                        */
 /*   P_ij  = exp(s_ij - LSE_i)                (0 when j is not in A_i)         */
-/*   dV_j  = sum_i P_ij dO_i                                                   */
-/*   dP_ij = dO_i . v_j                                                        */
-/*   D_i   = sum_j P_ij dP_ij                                                  */
-/*   dS_ij = P_ij (dP_ij - D_i)                                                */
+/*   dV_j  = sum_i P_ij z_ij dO_i             (z: the dropout factor, 1        */
+/*   dP_ij = dO_i . v_j                        without dropout)                */
+/*   D_i   = sum_j P_ij z_ij dP_ij            (= dO_i . O_i)                   */
+/*   dS_ij = P_ij (z_ij dP_ij - D_i)                                           */
 /*   dQ_i  = scale * sum_j dS_ij k_j                                           */
 /*   dK_j  = scale * sum_i dS_ij q_i                                           */
 /* Pass 1 walks query rows (LSE_i, D_i and dQ_i); pass 2 walks key rows (dK_j  */
@@ -355,7 +472,7 @@ static void bwd_row_stats(const head_cfg *c, const double *Qh, const double *Kh,
             continue;
         double P = exp(s[j] - lse);
         double dP = dot(g, Vh + (size_t)j * d, d);
-        D += P * dP;
+        D += P * drop_factor(c, i, j) * dP;
     }
     *lse_out = lse;
     *D_out = D;
@@ -366,7 +483,7 @@ static void bwd_row_stats(const head_cfg *c, const double *Qh, const double *Kh,
             continue;
         double P = exp(s[j] - lse);
         double dP = dot(g, Vh + (size_t)j * d, d);
-        double dS = P * (dP - D);
+        double dS = P * (drop_factor(c, i, j) * dP - D);
         const double *kr = Kh + (size_t)j * d;
         for (int k = 0; k < d; ++k)
             dq[k] += c->scale * dS * kr[k];
@@ -390,10 +507,11 @@ static void bwd_key_row(const head_cfg *c, const double *Qh, const double *Kh,
         const double *q = Qh + (size_t)i * d, *g = dOh + (size_t)i * d;
         double sij = c->scale * dot(q, kr, d);
         double P = exp(sij - LSE[i]);
+        double z = drop_factor(c, i, j);
         double dP = dot(g, vr, d);
-        double dS = P * (dP - Dv[i]);
+        double dS = P * (z * dP - Dv[i]);
         for (int k = 0; k < d; ++k) {
-            dv[k] += P * g[k];
+            dv[k] += P * z * g[k];
             dk[k] += c->scale * dS * q[k];
         }
     }
@@ -402,8 +520,10 @@ static void bwd_key_row(const head_cfg *c, const double *Qh, const double *Kh,
 void orc_bwd(int B, int H, int N, int d, const double *Q, const double *K,
              const double *V, const double *dO, double scale, int causal,
              const unsigned char *mask, int mask_block, long long sb,
-             long long sh, double *dQ, double *dK, double *dV)
+             long long sh, double *dQ, double *dK, double *dV, double drop_p,
+             unsigned long long seed, unsigned int offset)
 {
+    const drop_cfg g = make_drop(drop_p, seed, offset);
     const long long rows = (long long)B * H * N;
     double *LSE = (double *)malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1));
     double *Dv = (double *)malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1));
@@ -416,6 +536,8 @@ void orc_bwd(int B, int H, int N, int d, const double *Q, const double *K,
             head_cfg c = make_cfg(N, d, scale, causal,
                                   head_mask(mask, sb, sh, bh / H, bh % H),
                                   mask_block);
+            c.drop = g;
+            c.bh = bh;
             size_t base = (size_t)bh * N * d;
             bwd_row_stats(&c, Q + base, K + base, V + base, dO + base, i, s,
                           LSE + r, Dv + r, dQ + base + (size_t)i * d);
@@ -428,6 +550,8 @@ void orc_bwd(int B, int H, int N, int d, const double *Q, const double *K,
         head_cfg c = make_cfg(N, d, scale, causal,
                               head_mask(mask, sb, sh, bh / H, bh % H),
                               mask_block);
+        c.drop = g;
+        c.bh = bh;
         size_t base = (size_t)bh * N * d;
         bwd_key_row(&c, Q + base, K + base, V + base, dO + base,
                     LSE + (size_t)bh * N, Dv + (size_t)bh * N, j,
@@ -444,9 +568,12 @@ void orc_bwd_rows(int N, int d, const double *Qh, const double *Kh,
                   const double *Vh, const double *dOh, double scale, int causal,
                   const unsigned char *mask_h, int mask_block, int nq,
                   const int *qrows, double *dQ_rows, int nk, const int *krows,
-                  double *dK_rows, double *dV_rows)
+                  double *dK_rows, double *dV_rows, double drop_p,
+                  unsigned long long seed, unsigned int offset, int bh)
 {
     head_cfg c = make_cfg(N, d, scale, causal, mask_h, mask_block);
+    c.drop = make_drop(drop_p, seed, offset);
+    c.bh = bh;
     double *LSE = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     double *Dv = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     int need_all = nk > 0;
