@@ -65,6 +65,9 @@ def parse():
                     help="time separately launched kernels instead of one CUDA graph per step")
     ap.add_argument("--fwd-splits", type=int, default=0,
                     help="key-range slices of the forward (0: the library's choice for this GPU)")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="dropout probability of the attention weights (0: none, the workloads' "
+                         "own setting); the FLOP count is unchanged")
     return ap.parse_args()
 
 
@@ -162,7 +165,7 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def oracle_sample(w, inp, heads: int):
+def oracle_sample(w, inp, heads: int, dropout: float = 0.0):
     """fp64 oracle forward + backward on the first `heads` heads; returns (flops, s, threads)."""
     import oracle
     B, H = w.B, w.H
@@ -176,9 +179,9 @@ def oracle_sample(w, inp, heads: int):
         mh = oracle.head_mask(inp["mask"], b, h, w.N, w.mask_block)
         for c in w.causal:
             oracle.attention_fwd(sl("q"), sl("k"), sl("v"), w.scale, causal=c, mask=mh,
-                                 mask_block=w.mask_block)
+                                 mask_block=w.mask_block, dropout_p=dropout, seed=1)
             oracle.attention_bwd(sl("q"), sl("k"), sl("v"), sl("do"), w.scale, causal=c, mask=mh,
-                                 mask_block=w.mask_block)
+                                 mask_block=w.mask_block, dropout_p=dropout, seed=1)
             total += (flops[c]["fwd"] + flops[c]["bwd"]) / (B * H)
     return total, time.perf_counter() - t, oracle.num_threads()
 
@@ -193,9 +196,10 @@ def heads_for_seconds(w, target_s: float) -> int:
     return max(1, min(n, w.B * w.H))
 
 
-def config_of(w, fwd_splits=None):
+def config_of(w, fwd_splits=None, dropout=0.0):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
             "causal": list(w.causal), "block_mask_p": w.mask_p, "fwd_splits": fwd_splits,
+            "dropout_p": dropout,
             "passes": "fwd+bwd per causal setting",
             "l2": "flushed between steps (256 MiB write outside the timed events)"}
 
@@ -208,10 +212,10 @@ def run_reference(args, w, rank):
     # the whole reference run stays within a few minutes whatever K is
     heads = heads_for_seconds(w, min(1.5, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(w, inp, max(1, heads // 4))
+        oracle_sample(w, inp, max(1, heads // 4), args.dropout)
     tot_f, tot_s, cores = 0.0, 0.0, 1
     for _ in range(args.steps):
-        f, s, cores = oracle_sample(w, inp, heads)
+        f, s, cores = oracle_sample(w, inp, heads, args.dropout)
         tot_f += f
         tot_s += s
     value = tot_f / tot_s / 1e12
@@ -222,7 +226,7 @@ def run_reference(args, w, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * tot_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, dropout=args.dropout),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -357,7 +361,7 @@ def main():
 
     runs = []
     for c in w.causal:
-        p, keep = fa.make_params(q, w.scale, c, mask, w.mask_block)
+        p, keep = fa.make_params(q, w.scale, c, mask, w.mask_block, args.dropout, seed=1)
         ws = torch.empty(int(lib.fa_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8,
                          device=dev)
         splits = args.fwd_splits if args.fwd_splits > 0 else fa.num_splits(p)
@@ -500,7 +504,7 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         heads = heads_for_seconds(w, 15.0)
-        f, s, cores = oracle_sample(w, inp, heads)
+        f, s, cores = oracle_sample(w, inp, heads, args.dropout)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"fp64 oracle forward + backward of {heads} of {w.B * w.H} heads "
                          f"(causal settings {list(w.causal)}), {s:.1f} s"}
@@ -511,7 +515,7 @@ def main():
             "steps": K, "warmup": W, "ms_per_step": 1000.0 * total_s / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
-            "config": dict(config_of(w, [r["splits"] for r in runs]),
+            "config": dict(config_of(w, [r["splits"] for r in runs], args.dropout),
                            launch=("one CUDA graph per step, the causal settings as concurrent "
                                    "branches" if len(runs) > 1 else "one CUDA graph per step")
                            if graph is not None else "kernels launched one by one"),

@@ -45,6 +45,8 @@ class FaParams(ctypes.Structure):
         ("dtype", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int),
         ("block_mask", ctypes.c_void_p), ("mask_block", ctypes.c_int),
         ("mask_stride_b", ctypes.c_longlong), ("mask_stride_h", ctypes.c_longlong),
+        ("dropout_p", ctypes.c_float), ("dropout_seed", ctypes.c_ulonglong),
+        ("dropout_offset", ctypes.c_uint),
     ]
 
 
@@ -120,13 +122,15 @@ def _dtype_code(t) -> int:
 
 
 def make_params(q, scale: Optional[float] = None, causal: bool = False, block_mask=None,
-                mask_block: int = 128) -> tuple[FaParams, object]:
+                mask_block: int = 128, dropout_p: float = 0.0, seed: int = 0,
+                offset: int = 0) -> tuple[FaParams, object]:
     """fa_params for [B,H,N,d] tensors; returns (params, mask tensor kept alive)."""
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     p = FaParams(B, H, N, d, _dtype_code(q), float(scale), int(bool(causal)), None,
-                 int(mask_block), 0, 0)
+                 int(mask_block), 0, 0, float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
+                 int(offset) & 0xFFFFFFFF)
     keep = None
     if block_mask is not None:
         import torch
@@ -164,12 +168,12 @@ def _check_tensor(t, name, like):
 
 
 def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, mask_block=128,
-                  out=None, lse=None, stream=None):
+                  out=None, lse=None, stream=None, dropout_p=0.0, seed=0, offset=0):
     """O, LSE = fa_fwd(Q, K, V); tensors [B,H,N,d] on the current device."""
     import torch
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_tensor(t, n, q)
-    p, keep = make_params(q, scale, causal, block_mask, mask_block)
+    p, keep = make_params(q, scale, causal, block_mask, mask_block, dropout_p, seed, offset)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -189,13 +193,14 @@ def split_workspace_bytes(p: FaParams, splits: int) -> int:
 
 
 def attention_fwd_split(q, k, v, scale=None, causal=False, block_mask=None, mask_block=128,
-                        splits=None, out=None, lse=None, workspace=None, stream=None):
+                        splits=None, out=None, lse=None, workspace=None, stream=None,
+                        dropout_p=0.0, seed=0, offset=0):
     """O, LSE = fa_fwd_split(Q, K, V): the key range cut into ``splits`` slices
     (None: fa_fwd_num_splits for the current device)."""
     import torch
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_tensor(t, n, q)
-    p, keep = make_params(q, scale, causal, block_mask, mask_block)
+    p, keep = make_params(q, scale, causal, block_mask, mask_block, dropout_p, seed, offset)
     lib = load()
     if splits is None:
         splits = int(lib.fa_fwd_num_splits(ctypes.byref(p), 0))
@@ -223,12 +228,13 @@ def set_fwd_ctas(n: int) -> int:
 
 
 def attention_fwd_balanced(q, k, v, scale=None, causal=False, block_mask=None, mask_block=128,
-                           out=None, lse=None, workspace=None, stream=None):
+                           out=None, lse=None, workspace=None, stream=None, dropout_p=0.0,
+                           seed=0, offset=0):
     """O, LSE = fa_fwd_balanced(Q, K, V): persistent CTAs with equal shares."""
     import torch
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_tensor(t, n, q)
-    p, keep = make_params(q, scale, causal, block_mask, mask_block)
+    p, keep = make_params(q, scale, causal, block_mask, mask_block, dropout_p, seed, offset)
     lib = load()
     nbytes = int(lib.fa_fwd_balanced_workspace_size(ctypes.byref(p)))
     if workspace is None and nbytes > 0:
@@ -260,12 +266,14 @@ def workspace_bytes(q, scale=None, causal=False, block_mask=None, mask_block=128
 
 
 def attention_bwd(q, k, v, o, do, lse, scale=None, causal=False, block_mask=None,
-                  mask_block=128, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV = fa_bwd(Q, K, V, O, dO, LSE)."""
+                  mask_block=128, dq=None, dk=None, dv=None, workspace=None, stream=None,
+                  dropout_p=0.0, seed=0, offset=0):
+    """dQ, dK, dV = fa_bwd(Q, K, V, O, dO, LSE); with dropout, the same dropout_p, seed
+    and offset as the forward call that produced O."""
     import torch
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check_tensor(t, n, q)
-    p, keep = make_params(q, scale, causal, block_mask, mask_block)
+    p, keep = make_params(q, scale, causal, block_mask, mask_block, dropout_p, seed, offset)
     lib = load()
     nbytes = int(lib.fa_bwd_workspace_size(ctypes.byref(p)))
     if workspace is None:

@@ -142,7 +142,7 @@ static __device__ __noinline__ bool next_piece(const Sched& sc, int c, long long
   return sched_next(sc, c, g, g_end, first, sg);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(320, 1)
     bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -544,6 +544,10 @@ __global__ void __launch_bounds__(320, 1)
       return reinterpret_cast<const float*>(smem + L::STAT + (it % NQ) * L::STAT_STRIDE);
     };
     float p[64];
+    // dropout keep bits of this key row for the tile's 64 queries (bit c of
+    // kbits[c / 32] for query q0 + c): drawn with P, used again for dS
+    uint32_t kbits[2] = {~0u, ~0u};
+    auto keep = [&](int c) -> bool { return (kbits[c >> 5] >> (c & 31)) & 1u; };
     // S^T -> P^T of tile it: fp32 in p[] for dS, 16-bit into TMEM for dV; then p_full
     auto p_phase = [&](int it) -> bool {
       // the stage's statistics and coordinates (staged by the producer with Q and dO)
@@ -551,6 +555,12 @@ __global__ void __launch_bounds__(320, 1)
       const int4 ia = info_a(it);
       const int kt = ia.x, qtile = ia.z;
       const int key = kt * kTile + r;
+      if constexpr (DROP) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          kbits[i] = drop_keep_col<8>(a.drop, (uint32_t)key, (uint32_t)(qtile * kTile + 64 * g + 32 * i),
+                                      (uint32_t)ia.y);
+      }
       // a tail key tile: some row of this warp's 32 lies past N (warp-uniform)
       const bool rows_out = kt * kTile + (warp & 3) * 32 + 31 >= a.N;
       if (!warp_wait(w, bar_s_full, it & 1)) return false;
@@ -581,8 +591,14 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 64; ++c)
           if (key >= a.N || (diag && q0 + c < key)) p[c] = 0.f;
       }
+      // P^T for dV: with dropout the kept weights times 1 / (1 - p), else 0
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
+      for (int c = 0; c < 64; c += 2) {
+        if constexpr (DROP)
+          pk[c / 2] = pack2<F16>(keep(c) ? p[c] * a.drop.z : 0.f, keep(c + 1) ? p[c + 1] * a.drop.z : 0.f);
+        else
+          pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
+      }
       if constexpr (!L::ALIAS) {
         // d = 64: P^T has one buffer; dV of the previous tile must be done with it
         // (at d = 128 P^T goes over S^T, which s_full already orders after dV)
@@ -672,6 +688,11 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dp_free);
+          if constexpr (DROP) {  // dS = P (z dP - D)
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              u[c] = __float_as_uint(keep(c) ? __uint_as_float(u[c]) * a.drop.z : 0.f);
+          }
           const float4* nd4 = reinterpret_cast<const float4*>(stat(it) + 128 + 64 * g);  // -D
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
@@ -764,7 +785,7 @@ __global__ void __launch_bounds__(320, 1)
 template <int D, bool F16>
 cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   using L = BwdLayout<D>;
-  auto kern = bwd_persist_kernel<D, F16>;
+  auto kern = a.drop.on ? bwd_persist_kernel<D, F16, true> : bwd_persist_kernel<D, F16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;

@@ -118,7 +118,7 @@ __device__ __forceinline__ float d_of(const BwdArgs& a, int bh, int q) {
   return q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
 }
 
-template <int D, bool F16, int NG>
+template <int D, bool F16, int NG, bool DROP>
 __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -400,8 +400,20 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       return reinterpret_cast<const float*>(smem + L::STAT) + (it % NS) * 256;
     };
     float p[CW];
+    // dropout keep bits of this key row for the tile's CW queries (bit c of
+    // kbits[c / 32] for query q0 + c): drawn with P, used again for dS
+    uint32_t kbits[CW / 32];
+#pragma unroll
+    for (int i = 0; i < CW / 32; ++i) kbits[i] = ~0u;
+    auto keep = [&](int c) -> bool { return (kbits[c >> 5] >> (c & 31)) & 1u; };
     // S^T -> P^T: fp32 in p[] for dS, 16-bit into TMEM for dV; then p_full
     auto p_phase = [&](int it, int qtile) -> bool {
+      if constexpr (DROP) {  // drawn while the tile's S^T may still be in flight
+#pragma unroll
+        for (int i = 0; i < CW / 32; ++i)
+          kbits[i] = drop_keep_col<8>(a.drop, (uint32_t)key, (uint32_t)(qtile * kTile + CW * g + 32 * i),
+                                      (uint32_t)bh);
+      }
       // the stage's statistics (staged by the producer with Q and dO)
       if (!warp_wait(w, bar_qf(it % NS), (it / NS) & 1)) return false;
       if (!warp_wait(w, bar_s_full, it & 1)) return false;
@@ -432,8 +444,15 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         for (int c = 0; c < CW; ++c)
           if (key >= a.N || (diag && q0 + c < key)) p[c] = 0.f;
       }
+      // P^T for dV: with dropout the kept weights times 1 / (1 - p), else 0 (p[]
+      // keeps the undropped weights for dS)
 #pragma unroll
-      for (int c = 0; c < CW; c += 2) pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
+      for (int c = 0; c < CW; c += 2) {
+        if constexpr (DROP)
+          pk[c / 2] = pack2<F16>(keep(c) ? p[c] * a.drop.z : 0.f, keep(c + 1) ? p[c + 1] * a.drop.z : 0.f);
+        else
+          pk[c / 2] = pack2<F16>(p[c], p[c + 1]);
+      }
       if constexpr (!L::ALIAS) {
         // d = 64: P^T has one buffer; dV of the previous tile must be done with it
         // (at d = 128 P^T goes over S^T, which s_full already orders after dV)
@@ -455,7 +474,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     if (qt < n_tiles) ok = p_phase(0, qt);
     for (; ok && qt < n_tiles; ++it) {
       const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
-      // ---- dS_i = P_i * (dP_i - D)
+      // ---- dS_i = P_i * (dP_i - D), with dropout P_i * (z_i dP_i - D)
       if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
       tc_fence_after();
       uint32_t pk[CW / 2];
@@ -465,6 +484,11 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_dp_free);
+        if constexpr (DROP) {
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            u[c] = __float_as_uint(keep(c) ? __uint_as_float(u[c]) * a.drop.z : 0.f);
+        }
         const float4* nd4 = reinterpret_cast<const float4*>(stat(it) + 128 + CW * g);  // -D
 #pragma unroll
         for (int c = 0; c < CW; c += 4) {
@@ -584,7 +608,7 @@ cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   // enough); with four they would fall into other warps' boxes
   constexpr int NG = (D == 64) ? 4 : 2;
   using L = BwdLayout<D, NG>;
-  auto kern = bwd_tc_kernel<D, F16, NG>;
+  auto kern = a.drop.on ? bwd_tc_kernel<D, F16, NG, true> : bwd_tc_kernel<D, F16, NG, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   // the first a.direct key tiles, one CTA each (the rest, if any, go to the

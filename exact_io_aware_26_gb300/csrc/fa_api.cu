@@ -191,6 +191,23 @@ MaskArgs mask_args(const fa_params* p) {
   return m;
 }
 
+// The dropout arguments the kernels take: threshold floor(p * 2^32) on a
+// Philox word, keep scale 1 / (1 - p), the key and the counter's last word.
+DropArgs drop_args(const fa_params* p) {
+  DropArgs d;
+  std::memset(&d, 0, sizeof(d));
+  if (p->dropout_p > 0.f) {
+    const double t = std::floor((double)p->dropout_p * 4294967296.0);
+    d.on = 1;
+    d.t = t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
+    d.z = (float)(1.0 / (1.0 - (double)p->dropout_p));
+    d.key0 = (uint32_t)(p->dropout_seed & 0xFFFFFFFFull);
+    d.key1 = (uint32_t)(p->dropout_seed >> 32);
+    d.offset = p->dropout_offset;
+  }
+  return d;
+}
+
 BwdArgs bwd_args(const fa_params* p, void* ws) {
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -200,6 +217,7 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
   a.scale = p->scale;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.m = mask_args(p);
+  a.drop = drop_args(p);
   const size_t rows = (size_t)p->B * p->H * p->N;
   a.Dsum = static_cast<float*>(ws);
   a.dQacc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * 4));
@@ -326,8 +344,13 @@ fa_status fa_check(const fa_params* p, int for_backward) {
     set_err("the backward pass takes fp16 or bf16 tensors");
     return FA_ERR_UNSUPPORTED;
   }
+  if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f)) {
+    set_err("dropout_p must lie in [0, 1)");
+    return FA_ERR_INVALID;
+  }
   return FA_OK;
 }
+
 
 unsigned long long fa_set_wait_limit_ns(unsigned long long ns) {
   if (ns == 0) ns = 1;
@@ -355,6 +378,7 @@ fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V
   a.scale = p->scale;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.m = mask_args(p);
+  a.drop = drop_args(p);
   a.O = O;
   a.LSE = LSE;
   a.n_splits = 1;
@@ -477,6 +501,7 @@ fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const v
   a.scale = p->scale;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.m = mask_args(p);
+  a.drop = drop_args(p);
   a.O = O;
   a.LSE = LSE;
   a.n_splits = used;
@@ -502,7 +527,9 @@ namespace {
 long long fwd_iterations(const fa_params* p) {
   return make_sched((p->N + 127) / 128, p->B * p->H, p->causal ? 1 : 0, 1).T;
 }
-bool fwd_balanced_applies(const fa_params* p) { return p->dtype != FA_F32 && !p->block_mask; }
+bool fwd_balanced_applies(const fa_params* p) {
+  return p->dtype != FA_F32 && !p->block_mask && p->dropout_p == 0.f;
+}
 }  // namespace
 
 size_t fa_fwd_balanced_workspace_size(const fa_params* p) {
@@ -548,6 +575,7 @@ fa_status fa_fwd_balanced(const fa_params* p, const void* Q, const void* K, cons
   a.scale = p->scale;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.m = mask_args(p);
+  a.drop = drop_args(p);
   a.O = O;
   a.LSE = LSE;
   a.n_splits = 1;

@@ -7,10 +7,12 @@
 // do Softmax", FlashAttention reading guide), on 64 x 64 tiles staged in
 // shared memory: S = Q_i K_j^T with a 4 x 4 register block per thread, the
 // running max / sum per row (4 threads per row), then O = O e^(m-m') + P V_j.
-// O / l and LSE = m + ln l are written at the end.
+// O / l and LSE = m + ln l are written at the end.  With dropout, the weights
+// that enter P V_j are the kept ones times 1 / (1 - p) and the dropped ones 0
+// (Philox4x32-10 keep bits, as in the tensor-core kernels); l sums them all.
 #include <cmath>
 
-#include "internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 namespace {
@@ -111,11 +113,19 @@ __global__ void __launch_bounds__(NT) fwd_f32_kernel(const float* __restrict__ Q
     const float m_new = fmaxf(m, mx);
     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
     const float alpha = expf(m - m_use);
+    uint32_t kb16 = 0xFFFFu;  // dropout keep bits of this thread's 16 columns
+    if (a.drop.on) {
+      kb16 = 0;
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g)
+        kb16 |= drop_keep4(a.drop, (uint32_t)((k0 + part * 16) / 4 + g), (uint32_t)(q0 + sr), (uint32_t)bh)
+                << (4 * g);
+    }
     float sum = 0.f;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const float p = expf(srow[c] - m_use);
-      srow[c] = p;
+      srow[c] = a.drop.on ? (((kb16 >> c) & 1u) ? p * a.drop.z : 0.f) : p;
       sum += p;
     }
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);

@@ -19,11 +19,18 @@
 // same stale max, so the result is unchanged while most tiles skip the O
 // rescale.
 //
-// Per CTA the schedule is serial -- S_j, softmax, P~V_j, S_{j+1} -- because
-// P~ overwrites S in TMEM; two CTAs share each SM (256 TMEM columns and at
-// most 97 KiB of shared memory each), so one CTA's exponentials run on the
-// CUDA cores while the other's MMAs run on the tensor core ("FA3 : Mécanique
-// de la trémie", point 2, realised across CTAs).
+// At d = 64 P~ has TMEM columns of its own, so S_{j+1} is computed while the
+// softmax of tile j runs; at d = 128 P~ overwrites S and the schedule is
+// serial (S_j, softmax, P~V_j, S_{j+1}).  Two CTAs share each SM (256 TMEM
+// columns and at most 97 KiB of shared memory each), so one CTA's
+// exponentials run on the CUDA cores while the other's MMAs run on the tensor
+// core ("FA3 : Mécanique de la trémie", point 2, realised across CTAs).
+//
+// Dropout (a separate instantiation): after the exponentials of a tile, each
+// weight whose Philox4x32-10 word is below the threshold is replaced by 0 and
+// each other one is multiplied by 1 / (1 - p) before P~ V; l sums the undropped
+// weights, so O / l and LSE are those of the dropped-out attention and of the
+// undropped scores respectively.
 //
 // Warp roles (192 threads): warps 0-3 softmax (thread t owns query row t =
 // TMEM lane t); warp 4 TMA producer (Q once, K_j and V_j through a ring of
@@ -79,7 +86,7 @@ __device__ __forceinline__ int next_kept(const MaskArgs& m, int b, int h, int qt
   return kt;
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(192, 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -265,6 +272,20 @@ __global__ void __launch_bounds__(192, 2)
       // d = 128: S_j is complete, and so is every earlier MMA (P~ V_{j-1}
       // included), so O is stable and P~_{j-1} has been consumed.  d = 64 waits
       // for P~ V_{j-1} separately below.
+      // dropout: keep bits of the tile's 128 keys for this row (bit c of kb[c / 32]),
+      // drawn while S_j is still being computed
+      uint32_t kb[4] = {~0u, ~0u, ~0u, ~0u};
+      if constexpr (DROP) {
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          uint32_t m32 = 0;
+#pragma unroll 1
+          for (int g = 0; g < 8; ++g)
+            m32 |= drop_keep4(a.drop, (uint32_t)kt * (kTile / 4) + 8u * w4 + g, (uint32_t)row, (uint32_t)bh)
+                   << (4 * g);
+          kb[w4] = m32;
+        }
+      }
       if (!(ok = warp_wait(w, bar_s, it & 1))) break;
       tc_fence_after();
       float s[kTile];
@@ -317,8 +338,12 @@ __global__ void __launch_bounds__(192, 2)
       for (int c = 0; c < kTile; c += 2) {
         float x0, x1;
         f2unpack(ffma2(f2pack(s[c], s[c + 1]), c2p, mp), x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
+        float p0 = ex2(x0), p1 = ex2(x1);
         acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], f2pack(p0, p1));  // four independent sums
+        if constexpr (DROP) {  // l sums the undropped weights; P~ V takes the dropped ones
+          p0 = ((kb[c >> 5] >> (c & 31)) & 1u) ? p0 * a.drop.z : 0.f;
+          p1 = ((kb[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? p1 * a.drop.z : 0.f;
+        }
         if (c < 64)
           plo[c / 2] = pack2<F16>(p0, p1);
         else
@@ -433,7 +458,7 @@ __global__ void __launch_bounds__(192, 2)
 template <int D, bool F16>
 cudaError_t launch_t(const FwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   using L = FwdLayout<D>;
-  auto kern = fwd_tc_kernel<D, F16>;
+  auto kern = a.drop.on ? fwd_tc_kernel<D, F16, true> : fwd_tc_kernel<D, F16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;

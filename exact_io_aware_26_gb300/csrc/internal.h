@@ -35,6 +35,18 @@ struct MaskArgs {
   long long mask_sb, mask_sh;
 };
 
+// Dropout of the attention weights: weight (query i, key j) of head bh is kept
+// and scaled by z = 1 / (1 - p) when word (j mod 4) of Philox4x32-10 with
+// counter (j / 4, i, bh, offset) and key (key0, key1) is >= t = floor(p 2^32),
+// else dropped.  on = 0: no dropout (the kernels without it run).
+struct DropArgs {
+  uint32_t on;
+  uint32_t t;
+  float z;
+  uint32_t key0, key1;
+  uint32_t offset;
+};
+
 struct FwdArgs {
   int B, H, N;
   float scale;       // natural-units score scale
@@ -52,6 +64,7 @@ struct FwdArgs {
   // persistent forward: CTAs (the slots are 2 per CTA, each fp32 O [128][d]
   // then LSE [128])
   int G_fwd;
+  DropArgs drop;
   Report rep;
 };
 
@@ -76,6 +89,7 @@ struct BwdArgs {
   int G;
   int u0;
   float* slots;
+  DropArgs drop;
   Report rep;
 };
 

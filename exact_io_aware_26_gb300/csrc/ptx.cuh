@@ -416,6 +416,57 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef FA_R8
 #undef FA_W8
 
+// ----------------------------------------------------------------- dropout
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011): ten rounds of
+//   (x0, x1, x2, x3) -> (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0))
+// with the key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Keep bits of keys 4g .. 4g + 3 (bits 0-3) of query row i in head bh.
+__device__ __forceinline__ uint32_t drop_keep4(const DropArgs& dr, uint32_t g, uint32_t i, uint32_t bh) {
+  const uint4 w = philox4x32_10(make_uint4(g, i, bh, dr.offset), dr.key0, dr.key1);
+  return (uint32_t)(w.x >= dr.t) | ((uint32_t)(w.y >= dr.t) << 1) | ((uint32_t)(w.z >= dr.t) << 2) |
+         ((uint32_t)(w.w >= dr.t) << 3);
+}
+
+// Keep bits, for the key row of this lane (keys are consecutive across lanes, so
+// lanes 4a .. 4a + 3 share one key group), of the 4 n queries q0 .. q0 + 4n - 1:
+// bit c of the result for query q0 + c.  The four lanes of a group each draw the
+// Philox words of one query of every 4 and pass them round, so no word is drawn
+// twice.  All 32 lanes must call it together.
+template <int NQ4>
+__device__ __forceinline__ uint32_t drop_keep_col(const DropArgs& dr, uint32_t key, uint32_t q0,
+                                                  uint32_t bh) {
+  static_assert(NQ4 <= 8, "at most 32 queries per word");
+  const uint32_t lane = threadIdx.x & 31u, r = lane & 3u;
+  uint32_t bits = 0;
+#pragma unroll 1
+  for (int m = 0; m < NQ4; ++m) {
+    const uint4 wv = philox4x32_10(make_uint4(key >> 2, q0 + 4u * m + r, bh, dr.offset), dr.key0, dr.key1);
+#pragma unroll
+    for (uint32_t t = 0; t < 4; ++t) {
+      // offer word (r - t) mod 4 of this lane's draw; take from the lane whose
+      // draw is for query 4m + ((r + t) mod 4) the word of this lane's key
+      const uint32_t i = (r - t) & 3u;
+      const uint32_t offer = i == 0 ? wv.x : i == 1 ? wv.y : i == 2 ? wv.z : wv.w;
+      const uint32_t got = t == 0 ? offer : __shfl_sync(0xffffffffu, offer, (lane & ~3u) | ((r + t) & 3u));
+      bits |= (uint32_t)(got >= dr.t) << (4u * m + ((r + t) & 3u));
+    }
+  }
+  return bits;
+}
+
 // ----------------------------------------------------------------- math
 
 __device__ __forceinline__ float ex2(float x) {

@@ -69,8 +69,21 @@ typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
  *               Combined with `causal` by AND.  Hidden tiles are never loaded.
  *   mask_block  tokens per mask entry; a positive multiple of 128 when
  *               block_mask is set (ignored otherwise).
+ *   dropout_p   probability in [0, 1) of dropping each attention weight (the
+ *               softmax output, after masking); kept weights are scaled by
+ *               1 / (1 - p).  Dropout is fused into the kernels ("Fusão de
+ *               Kernels", reading guide, "Ideias centrais").  0 = none.
+ *   dropout_seed, dropout_offset
+ *               the keep decision of weight (query i, key j) of head
+ *               bh = b * H + h is word (j mod 4) of Philox4x32-10 (Salmon et
+ *               al., SC 2011) with counter (j / 4, i, bh, dropout_offset) and
+ *               key (seed mod 2^32, seed / 2^32): kept when the word is at
+ *               least floor(p * 2^32).  The backward regenerates the same
+ *               decisions from the same three values instead of storing them.
  * A query row whose allowed key set is empty gets O = 0 and LSE = -inf, and
- * contributes nothing to the gradients.
+ * contributes nothing to the gradients.  With dropout, O is the dropped and
+ * rescaled weights times V, while LSE stays the log-sum-exp of the undropped
+ * scores (it is what the backward recomputes the weights from).
  */
 typedef struct {
   int B, H, N, d;
@@ -80,6 +93,9 @@ typedef struct {
   const uint8_t* block_mask;
   int mask_block;
   long long mask_stride_b, mask_stride_h;
+  float dropout_p;
+  unsigned long long dropout_seed;
+  unsigned int dropout_offset;
 } fa_params;
 
 /* Host-only validation of `p` (no CUDA call).  for_backward selects the
@@ -110,7 +126,7 @@ fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V
  * O = sum_s exp(LSE_s - LSE) O_s.  `workspace`: device memory owned by the
  * caller, 256-byte aligned, at least fa_fwd_balanced_workspace_size(p) bytes
  * (else FA_ERR_WORKSPACE); its contents on entry do not matter.  With a block
- * mask or fp32 inputs this is fa_fwd (the workspace is not used).
+ * mask, fp32 inputs or dropout this is fa_fwd (the workspace is not used).
  */
 fa_status fa_fwd_balanced(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
                           float* LSE, void* workspace, size_t workspace_bytes, void* stream);
@@ -118,7 +134,7 @@ fa_status fa_fwd_balanced(const fa_params* p, const void* Q, const void* K, cons
 /* Bytes of workspace fa_fwd_balanced needs: two fp32 slots of 128 x d + 128
  * values per CTA, for min(320, iterations) CTAs, where iterations =
  * B*H*T^2 or B*H*T(T+1)/2 causal, T = ceil(N / 128); 0 when the call would
- * be fa_fwd (block mask, fp32) or p is invalid. */
+ * be fa_fwd (block mask, fp32, dropout) or p is invalid. */
 size_t fa_fwd_balanced_workspace_size(const fa_params* p);
 
 /* Upper bound on the CTAs of fa_fwd_balanced (0, the default: two per SM, at

@@ -54,6 +54,11 @@ def _p(**kw):
     ({"block_mask": 4096, "mask_block": 0}, fa.FA_ERR_INVALID),
     ({"block_mask": 4096, "mask_block": 256}, fa.FA_OK),
     ({"block_mask": 4096, "mask_stride_h": -1}, fa.FA_ERR_INVALID),
+    ({"dropout_p": 0.1, "dropout_seed": 2 ** 63 + 5, "dropout_offset": 7}, fa.FA_OK),
+    ({"dropout_p": 0.999}, fa.FA_OK),
+    ({"dropout_p": 1.0}, fa.FA_ERR_INVALID),
+    ({"dropout_p": -0.1}, fa.FA_ERR_INVALID),
+    ({"dropout_p": float("nan")}, fa.FA_ERR_INVALID),
 ])
 def test_check_params(lib, kw, expect):
     assert fa.check_params(_p(**kw)) == expect
@@ -183,3 +188,17 @@ def test_balanced_forward_workspace_and_fallbacks(lib):
     assert call(ok_ptr + 16, need) == fa.FA_ERR_WORKSPACE
     old = fa.set_fwd_ctas(9)
     assert fa.set_fwd_ctas(old) == 9
+
+
+def test_params_mirror_the_header_layout(lib):
+    """The dropout fields sit after the mask strides (float, 8-byte seed, 4-byte offset)."""
+    import ctypes
+    assert fa.FaParams.dropout_p.offset == fa.FaParams.mask_stride_h.offset + 8
+    assert fa.FaParams.dropout_seed.offset == fa.FaParams.dropout_p.offset + 8
+    assert fa.FaParams.dropout_offset.offset == fa.FaParams.dropout_seed.offset + 8
+    assert ctypes.sizeof(fa.FaParams) == fa.FaParams.dropout_offset.offset + 8
+
+
+def test_balanced_forward_with_dropout_is_the_plain_forward(lib):
+    assert fa.balanced_workspace_bytes(_p(N=1024, dropout_p=0.1)) == 0
+    assert fa.balanced_workspace_bytes(_p(N=1024)) > 0
