@@ -263,7 +263,24 @@ def fwd(fa, r, q, k, v, o, lse, stream):
         fa.fwd_raw(r["p"], q, k, v, o, lse, stream)
 
 
-def run_e2e(fa, inp, runs, flops, steps, dev, stream):
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest x over all ranks of the process group (x itself with one rank): a
+    multi-rank step takes as long as its slowest rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: every rank processes units_per_rank (weak scaling, one
+    replica of the workload per GPU) in at most `seconds` (the max over ranks)."""
+    return units_per_rank * world / seconds
+
+
+def run_e2e(fa, inp, runs, flops, steps, dev, stream, dist=None, world=1):
     """Same metric with host buffers.  Every step copies its inputs from pinned host
     memory, runs the path, and copies every output back to pinned host memory.  The
     copies run on their own streams with double-buffered device tensors, so step i's
@@ -318,12 +335,17 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream):
 
     run(2)
     torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
     t0 = time.perf_counter()
     run(steps)
     torch.cuda.synchronize()
     s = time.perf_counter() - t0
+    if dist:
+        dist.barrier()
+    s = max_over_ranks(s, dist, dev)
     step_flops = sum(f["fwd"] + f["bwd"] for f in flops.values())
-    return {"value": step_flops * steps / s / 1e12, "unit": "TFLOP/s",
+    return {"value": job_value(step_flops * steps, world, s) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "host clock around all steps, synchronised on both sides",
             "overlap": "copies on their own streams, double-buffered device tensors; one "
@@ -486,10 +508,7 @@ def main():
     launched_s = sum(a.elapsed_time(b) for a, b in ev_kstep) / 1000.0
     main_s = sum(a.elapsed_time(b) for row in ev_main for a, b in row) / 1000.0
     fwd_s = sum(a.elapsed_time(b) for row in ev_fwd for a, b in row) / 1000.0
-    if dist:
-        t = torch.tensor([total_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(total_s, dist, dev)
 
     peak, peak_src = read_peaks()
     launches = K * len(runs)
@@ -497,9 +516,9 @@ def main():
     fwd_flops = sum(flops[r["causal"]]["fwd"] for r in runs) * K
     achieved = bwd_flops / main_s / 1e12
     fwd_tflops = fwd_flops / fwd_s / 1e12
-    value = step_flops * K * world / total_s / 1e12
+    value = job_value(step_flops * K, world, total_s) / 1e12
 
-    e2e = run_e2e(fa, inp, runs, flops, args.e2e_steps, dev, stream)
+    e2e = run_e2e(fa, inp, runs, flops, args.e2e_steps, dev, stream, dist, world)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
