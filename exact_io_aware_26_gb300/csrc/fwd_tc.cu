@@ -277,14 +277,8 @@ __global__ void __launch_bounds__(192, 2)
       uint32_t kb[4] = {~0u, ~0u, ~0u, ~0u};
       if constexpr (DROP) {
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) {
-          uint32_t m32 = 0;
-#pragma unroll 1
-          for (int g = 0; g < 8; ++g)
-            m32 |= drop_keep4(a.drop, (uint32_t)kt * (kTile / 4) + 8u * w4 + g, (uint32_t)row, (uint32_t)bh)
-                   << (4 * g);
-          kb[w4] = m32;
-        }
+        for (int w4 = 0; w4 < 4; ++w4)
+          kb[w4] = drop_keep32(a.drop, (uint32_t)kt * (kTile / 32) + (uint32_t)w4, (uint32_t)row, (uint32_t)bh);
       }
       if (!(ok = warp_wait(w, bar_s, it & 1))) break;
       tc_fence_after();

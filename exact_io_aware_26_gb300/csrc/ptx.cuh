@@ -433,6 +433,45 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// The same for K counters at once, advanced round by round in lockstep: the
+// rounds of one counter depend on each other, so K independent counters keep
+// the multiply and logic pipes busy instead of waiting on one chain.
+template <int K>
+__device__ __forceinline__ void philox4x32_10_n(uint4 (&c)[K], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const uint32_t hi0 = __umulhi(0xD2511F53u, c[j].x), lo0 = 0xD2511F53u * c[j].x;
+      const uint32_t hi1 = __umulhi(0xCD9E8D57u, c[j].z), lo1 = 0xCD9E8D57u * c[j].z;
+      c[j] = make_uint4(hi1 ^ c[j].y ^ k0, lo1, hi0 ^ c[j].w ^ k1, lo0);
+    }
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
+__device__ __forceinline__ uint32_t keep_bits4(const uint4& w, uint32_t t) {
+  return (uint32_t)(w.x >= t) | ((uint32_t)(w.y >= t) << 1) | ((uint32_t)(w.z >= t) << 2) |
+         ((uint32_t)(w.w >= t) << 3);
+}
+
+// Keep bits of keys 32 w .. 32 w + 31 (bit c for key 32 w + c) of query row i in
+// head bh: eight counters drawn together.
+__device__ __forceinline__ uint32_t drop_keep32(const DropArgs& dr, uint32_t w, uint32_t i, uint32_t bh) {
+  uint32_t bits = 0;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {  // two batches of four counters
+    uint4 c[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) c[g] = make_uint4(8u * w + 4u * h + (uint32_t)g, i, bh, dr.offset);
+    philox4x32_10_n<4>(c, dr.key0, dr.key1);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) bits |= keep_bits4(c[g], dr.t) << (16 * h + 4 * g);
+  }
+  return bits;
+}
+
 // Keep bits of keys 4g .. 4g + 3 (bits 0-3) of query row i in head bh.
 __device__ __forceinline__ uint32_t drop_keep4(const DropArgs& dr, uint32_t g, uint32_t i, uint32_t bh) {
   const uint4 w = philox4x32_10(make_uint4(g, i, bh, dr.offset), dr.key0, dr.key1);
@@ -450,10 +489,14 @@ __device__ __forceinline__ uint32_t drop_keep_col(const DropArgs& dr, uint32_t k
                                                   uint32_t bh) {
   static_assert(NQ4 <= 8, "at most 32 queries per word");
   const uint32_t lane = threadIdx.x & 31u, r = lane & 3u;
+  uint4 c[NQ4];  // this lane's draws, all at once (see philox4x32_10_n)
+#pragma unroll
+  for (int m = 0; m < NQ4; ++m) c[m] = make_uint4(key >> 2, q0 + 4u * m + r, bh, dr.offset);
+  philox4x32_10_n<NQ4>(c, dr.key0, dr.key1);
   uint32_t bits = 0;
-#pragma unroll 1
+#pragma unroll
   for (int m = 0; m < NQ4; ++m) {
-    const uint4 wv = philox4x32_10(make_uint4(key >> 2, q0 + 4u * m + r, bh, dr.offset), dr.key0, dr.key1);
+    const uint4 wv = c[m];
 #pragma unroll
     for (uint32_t t = 0; t < 4; ++t) {
       // offer word (r - t) mod 4 of this lane's draw; take from the lane whose
