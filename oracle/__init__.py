@@ -26,11 +26,12 @@ Functions and the passages they follow:
   pass ``dropout_p`` to the attention call -- "L'intégration est de huit
   lignes", marketmaker.cc -- but name no generator).
 
-Dropout (``dropout_p`` > 0): each weight P_ij of head bh = b * H + h is kept
-and scaled by 1 / (1 - p) when word (j mod 4) of Philox4x32-10 with counter
-(j // 4, i, bh, offset) and key (seed mod 2^32, seed // 2^32) is at least
-floor(p * 2^32), else set to 0; m, l and LSE stay those of the undropped
-softmax.
+Dropout (``dropout_p`` > 0): weight P_ij of head bh = b * H + h is kept when
+the 16-bit half (low for even j, high for odd j) of word (j mod 8) // 2 of
+Philox4x32-10 with counter (j // 8, i, bh, offset) and key (seed mod 2^32,
+seed // 2^32) is at least t = floor(p * 2^16), else set to 0; kept weights are
+scaled by 2^16 / (2^16 - t) (``dropout_scale``), the inverse of the keep
+probability.  m, l and LSE stay those of the undropped softmax.
 
 Masks: ``mask`` is a uint8 array of shape [T, T] (shared by every batch and
 head) or [B, H, T, T], with T = ceil(N / mask_block); entry [i // mb, j // mb]
@@ -150,6 +151,12 @@ def philox4x32_10(counter, key) -> np.ndarray:
     out = np.zeros(4, dtype=np.uint32)
     _load().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
     return out
+
+
+def dropout_scale(dropout_p) -> float:
+    """The factor kept weights are multiplied by: 2^16 / (2^16 - floor(p * 2^16))."""
+    t = min(int(np.floor(float(dropout_p) * 65536.0)), 65535)
+    return 65536.0 / (65536.0 - t) if dropout_p > 0 else 1.0
 
 
 def dropout_keep(B, H, N, dropout_p, seed=0, offset=0) -> np.ndarray:

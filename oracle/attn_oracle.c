@@ -42,9 +42,12 @@
  *     counter-based generator Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
  *     "Parallel random numbers: as easy as 1, 2, 3", SC 2011), so that a
  *     backward pass regenerates them instead of storing them: for head bh,
- *     query row i and key j, the word (j mod 4) of Philox4x32-10 with counter
- *     (floor(j / 4), i, bh, offset) and key (seed mod 2^32, floor(seed / 2^32))
- *     keeps the weight when it is at least t = floor(p * 2^32).
+ *     query row i and key j, Philox4x32-10 with counter (floor(j / 8), i, bh,
+ *     offset) and key (seed mod 2^32, floor(seed / 2^32)) gives four words;
+ *     word floor((j mod 8) / 2), its low 16 bits for even j and its high 16
+ *     bits for odd j, keeps the weight when it is at least t = floor(p * 2^16).
+ *     A weight is then kept with probability 1 - t / 2^16 (p to within 2^-16)
+ *     and scaled by 2^16 / (2^16 - t), the inverse of that probability.
  */
 #include <math.h>
 #include <stddef.h>
@@ -97,8 +100,8 @@ void orc_philox4x32_10(const uint32_t *ctr, const uint32_t *key, uint32_t *out)
 /* Dropout of one call: off when p == 0. */
 typedef struct {
     int on;
-    uint32_t t;     /* keep when the word is >= t = floor(p * 2^32) */
-    double z;       /* 1 / (1 - p) */
+    uint32_t t;     /* keep when the 16-bit half is >= t = floor(p * 2^16) */
+    double z;       /* 2^16 / (2^16 - t) */
     uint32_t key[2];
     uint32_t offset;
 } drop_cfg;
@@ -107,9 +110,9 @@ static drop_cfg make_drop(double p, unsigned long long seed, unsigned int offset
 {
     drop_cfg g;
     g.on = p > 0.0;
-    double t = floor(p * 4294967296.0);
-    g.t = t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
-    g.z = g.on ? 1.0 / (1.0 - p) : 1.0;
+    double t = floor(p * 65536.0);
+    g.t = t >= 65535.0 ? 65535u : (uint32_t)t;
+    g.z = g.on ? 65536.0 / (65536.0 - (double)g.t) : 1.0;
     g.key[0] = (uint32_t)(seed & 0xFFFFFFFFull);
     g.key[1] = (uint32_t)(seed >> 32);
     g.offset = offset;
@@ -127,16 +130,23 @@ typedef struct {
     int bh;                    /* b * H + h, part of the dropout counter */
 } head_cfg;
 
+/* The 16-bit draw of weight (i, j) of head bh. */
+static uint32_t drop_draw(const drop_cfg *g, int bh, int i, int j)
+{
+    uint32_t ctr[4] = {(uint32_t)j >> 3, (uint32_t)i, (uint32_t)bh, g->offset};
+    uint32_t w[4];
+    philox4x32_10(ctr, g->key, w);
+    uint32_t word = w[(j & 7) >> 1];
+    return (j & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
 /* The factor dropout applies to weight (i, j) of this head: 1 without dropout,
- * else 1 / (1 - p) or 0. */
+ * else 2^16 / (2^16 - t) or 0. */
 static double drop_factor(const head_cfg *c, int i, int j)
 {
     if (!c->drop.on)
         return 1.0;
-    uint32_t ctr[4] = {(uint32_t)j >> 2, (uint32_t)i, (uint32_t)c->bh, c->drop.offset};
-    uint32_t w[4];
-    philox4x32_10(ctr, c->drop.key, w);
-    return w[j & 3] >= c->drop.t ? c->drop.z : 0.0;
+    return drop_draw(&c->drop, c->bh, i, j) >= c->drop.t ? c->drop.z : 0.0;
 }
 
 /* Keep decisions of every (b, h, i, j) as bytes [B][H][N][N] (1 = kept). */
@@ -148,12 +158,8 @@ void orc_dropout_keep(int B, int H, int N, double p, unsigned long long seed,
 #pragma omp parallel for schedule(static)
     for (long long r = 0; r < rows; ++r) {
         int bh = (int)(r / N), i = (int)(r % N);
-        for (int j = 0; j < N; ++j) {
-            uint32_t ctr[4] = {(uint32_t)j >> 2, (uint32_t)i, (uint32_t)bh, g.offset};
-            uint32_t w[4];
-            philox4x32_10(ctr, g.key, w);
-            keep[(size_t)r * N + j] = (unsigned char)(!g.on || w[j & 3] >= g.t);
-        }
+        for (int j = 0; j < N; ++j)
+            keep[(size_t)r * N + j] = (unsigned char)(!g.on || drop_draw(&g, bh, i, j) >= g.t);
     }
 }
 

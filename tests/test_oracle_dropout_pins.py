@@ -40,16 +40,19 @@ def test_philox_known_answer_vectors(ctr, key, expect):
 
 
 def test_keep_decisions_follow_the_documented_counter_layout():
-    """Word j mod 4 of the counter (j // 4, i, bh, offset) under key (seed lo, seed hi)."""
+    """Half j mod 2 of word (j mod 8) // 2 of the counter (j // 8, i, bh, offset) under
+    key (seed lo, seed hi), against floor(p 2^16)."""
     B, H, N, p, seed, off = 2, 3, 37, 0.35, 0x123456789ABCDEF0, 77
     keep = oracle.dropout_keep(B, H, N, p, seed, off)
-    t = int(np.floor(p * 2.0 ** 32))
+    t = int(np.floor(p * 2.0 ** 16))
     key = [seed & 0xFFFFFFFF, seed >> 32]
     rng = np.random.default_rng(0)
     for _ in range(200):
         b, h, i, j = (int(rng.integers(0, n)) for n in (B, H, N, N))
-        w = oracle.philox4x32_10([j // 4, i, b * H + h, off], key)[j % 4]
-        assert keep[b, h, i, j] == (1 if int(w) >= t else 0)
+        w = int(oracle.philox4x32_10([j // 8, i, b * H + h, off], key)[(j % 8) // 2])
+        half = (w >> 16) if j % 2 else (w & 0xFFFF)
+        assert keep[b, h, i, j] == (1 if half >= t else 0)
+    assert oracle.dropout_scale(p) == 65536.0 / (65536.0 - t)
 
 
 def test_p0_is_plain_attention():
@@ -71,8 +74,10 @@ def test_keep_fraction_is_one_minus_p(p):
     keep = oracle.dropout_keep(B, H, N, p, seed=11, offset=3)
     n = keep.size
     frac = keep.mean()
-    sigma = np.sqrt(p * (1 - p) / n)
-    assert abs(frac - (1 - p)) <= 5 * sigma, (frac, 1 - p, sigma)
+    q = 1.0 / oracle.dropout_scale(p)  # the keep probability, 1 - p to within 2^-16
+    assert abs(q - (1 - p)) <= 2.0 ** -16
+    sigma = np.sqrt(q * (1 - q) / n)
+    assert abs(frac - q) <= 5 * sigma, (frac, q, sigma)
 
 
 def test_masks_differ_across_seeds_offsets_and_heads_and_repeat_for_equal_ones():
@@ -112,7 +117,7 @@ def _torch_dropout_attention(q, k, v, do, scale, causal, z):
 def test_forward_and_gradients_match_torch_with_the_same_mask(causal):
     B, H, N, d, p, seed, off = 2, 2, 45, 16, 0.25, 99, 4
     q, k, v, do = (_rand((B, H, N, d), s) for s in (11, 12, 13, 14))
-    z = oracle.dropout_keep(B, H, N, p, seed, off).astype(np.float64) / (1 - p)
+    z = oracle.dropout_keep(B, H, N, p, seed, off).astype(np.float64) * oracle.dropout_scale(p)
     O_t, dq_t, dk_t, dv_t = _torch_dropout_attention(q, k, v, do, 0.25, causal, z)
     O, L = oracle.attention_fwd(q, k, v, 0.25, causal=causal, dropout_p=p, seed=seed, offset=off)
     O_plain, L_plain = oracle.attention_fwd(q, k, v, 0.25, causal=causal)
