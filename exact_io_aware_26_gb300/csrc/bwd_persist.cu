@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(320, 1)
       if constexpr (DROP) {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-          kbits[i] = drop_keep_col<8>(a.drop, (uint32_t)key, (uint32_t)(qtile * kTile + 64 * g + 32 * i),
+          kbits[i] = drop_keep_col32(a.drop, (uint32_t)key, (uint32_t)(qtile * kTile + 64 * g + 32 * i),
                                       (uint32_t)ia.y);
       }
       // a tail key tile: some row of this warp's 32 lies past N (warp-uniform)

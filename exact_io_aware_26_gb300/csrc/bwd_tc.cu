@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       if constexpr (DROP) {  // drawn while the tile's S^T may still be in flight
 #pragma unroll
         for (int i = 0; i < CW / 32; ++i)
-          kbits[i] = drop_keep_col<8>(a.drop, (uint32_t)key, (uint32_t)(qtile * kTile + CW * g + 32 * i),
+          kbits[i] = drop_keep_col32(a.drop, (uint32_t)key, (uint32_t)(qtile * kTile + CW * g + 32 * i),
                                       (uint32_t)bh);
       }
       // the stage's statistics (staged by the producer with Q and dO)

@@ -191,16 +191,17 @@ MaskArgs mask_args(const fa_params* p) {
   return m;
 }
 
-// The dropout arguments the kernels take: threshold floor(p * 2^32) on a
-// Philox word, keep scale 1 / (1 - p), the key and the counter's last word.
+// The dropout arguments the kernels take: threshold t = floor(p * 2^16) on a
+// 16-bit half of a Philox word, keep scale 2^16 / (2^16 - t) (the inverse of the
+// keep probability), the key and the counter's last word.
 DropArgs drop_args(const fa_params* p) {
   DropArgs d;
   std::memset(&d, 0, sizeof(d));
   if (p->dropout_p > 0.f) {
-    const double t = std::floor((double)p->dropout_p * 4294967296.0);
+    const double t = std::floor((double)p->dropout_p * 65536.0);
     d.on = 1;
-    d.t = t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
-    d.z = (float)(1.0 / (1.0 - (double)p->dropout_p));
+    d.t = t >= 65535.0 ? 65535u : (uint32_t)t;
+    d.z = (float)(65536.0 / (65536.0 - (double)d.t));
     d.key0 = (uint32_t)(p->dropout_seed & 0xFFFFFFFFull);
     d.key1 = (uint32_t)(p->dropout_seed >> 32);
     d.offset = p->dropout_offset;

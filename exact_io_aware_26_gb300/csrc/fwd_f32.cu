@@ -115,14 +115,12 @@ __global__ void __launch_bounds__(NT) fwd_f32_kernel(const float* __restrict__ Q
     const float alpha = expf(m - m_use);
     uint32_t kb16 = 0xFFFFu;  // dropout keep bits of this thread's 16 columns
     if (a.drop.on) {
-      uint4 c[4];
+      uint4 c[2];
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
-        c[g] = make_uint4((uint32_t)((k0 + part * 16) / 4 + g), (uint32_t)(q0 + sr), (uint32_t)bh, a.drop.offset);
-      philox4x32_10_n<4>(c, a.drop.key0, a.drop.key1);
-      kb16 = 0;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) kb16 |= keep_bits4(c[g], a.drop.t) << (4 * g);
+      for (int g = 0; g < 2; ++g)
+        c[g] = make_uint4((uint32_t)((k0 + part * 16) / 8 + g), (uint32_t)(q0 + sr), (uint32_t)bh, a.drop.offset);
+      philox4x32_10_n<2>(c, a.drop.key0, a.drop.key1);
+      kb16 = keep_bits8(c[0], a.drop.t) | (keep_bits8(c[1], a.drop.t) << 8);
     }
     float sum = 0.f;
 #pragma unroll

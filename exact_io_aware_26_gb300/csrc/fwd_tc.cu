@@ -276,9 +276,15 @@ __global__ void __launch_bounds__(192, 2)
       // drawn while S_j is still being computed
       uint32_t kb[4] = {~0u, ~0u, ~0u, ~0u};
       if constexpr (DROP) {
+        // one 32-key word at a time (four counters in flight), written by
+        // selects so that kb stays in registers
+#pragma unroll 1
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const uint32_t bits =
+              drop_keep32(a.drop, (uint32_t)kt * (kTile / 32) + (uint32_t)w4, (uint32_t)row, (uint32_t)bh);
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4)
-          kb[w4] = drop_keep32(a.drop, (uint32_t)kt * (kTile / 32) + (uint32_t)w4, (uint32_t)row, (uint32_t)bh);
+          for (int i = 0; i < 4; ++i) kb[i] = (w4 == i) ? bits : kb[i];
+        }
       }
       if (!(ok = warp_wait(w, bar_s, it & 1))) break;
       tc_fence_after();

@@ -36,9 +36,10 @@ struct MaskArgs {
 };
 
 // Dropout of the attention weights: weight (query i, key j) of head bh is kept
-// and scaled by z = 1 / (1 - p) when word (j mod 4) of Philox4x32-10 with
-// counter (j / 4, i, bh, offset) and key (key0, key1) is >= t = floor(p 2^32),
-// else dropped.  on = 0: no dropout (the kernels without it run).
+// and scaled by z = 2^16 / (2^16 - t) when the 16-bit half (j mod 2: low, high)
+// of word (j mod 8) / 2 of Philox4x32-10 with counter (j / 8, i, bh, offset) and
+// key (key0, key1) is >= t = floor(p 2^16), else dropped.  on = 0: no dropout
+// (the kernels without it run).
 struct DropArgs {
   uint32_t on;
   uint32_t t;

@@ -420,22 +420,9 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
 // easy as 1, 2, 3", SC 2011): ten rounds of
 //   (x0, x1, x2, x3) -> (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0))
-// with the key bumped by the Weyl constants between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
-  }
-  return c;
-}
-
-// The same for K counters at once, advanced round by round in lockstep: the
-// rounds of one counter depend on each other, so K independent counters keep
-// the multiply and logic pipes busy instead of waiting on one chain.
+// with the key bumped by the Weyl constants between rounds.  K counters are
+// advanced round by round in lockstep: the rounds of one counter depend on each
+// other, so independent counters keep the multiply and logic pipes busy.
 template <int K>
 __device__ __forceinline__ void philox4x32_10_n(uint4 (&c)[K], uint32_t k0, uint32_t k1) {
 #pragma unroll
@@ -451,60 +438,55 @@ __device__ __forceinline__ void philox4x32_10_n(uint4 (&c)[K], uint32_t k0, uint
   }
 }
 
-__device__ __forceinline__ uint32_t keep_bits4(const uint4& w, uint32_t t) {
-  return (uint32_t)(w.x >= t) | ((uint32_t)(w.y >= t) << 1) | ((uint32_t)(w.z >= t) << 2) |
-         ((uint32_t)(w.w >= t) << 3);
-}
-
-// Keep bits of keys 32 w .. 32 w + 31 (bit c for key 32 w + c) of query row i in
-// head bh: eight counters drawn together.
-__device__ __forceinline__ uint32_t drop_keep32(const DropArgs& dr, uint32_t w, uint32_t i, uint32_t bh) {
+// The eight keep decisions of one draw: bit b (for key 8 g + b of the counter
+// (g, ...)) from the 16-bit half b mod 2 (low, high) of word b / 2.
+__device__ __forceinline__ uint32_t keep_bits8(const uint4& w, uint32_t t) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
   uint32_t bits = 0;
-#pragma unroll 1
-  for (int h = 0; h < 2; ++h) {  // two batches of four counters
-    uint4 c[4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) c[g] = make_uint4(8u * w + 4u * h + (uint32_t)g, i, bh, dr.offset);
-    philox4x32_10_n<4>(c, dr.key0, dr.key1);
-#pragma unroll
-    for (int g = 0; g < 4; ++g) bits |= keep_bits4(c[g], dr.t) << (16 * h + 4 * g);
-  }
+  for (int k = 0; k < 4; ++k)
+    bits |= ((uint32_t)((v[k] & 0xFFFFu) >= t) << (2 * k)) | ((uint32_t)((v[k] >> 16) >= t) << (2 * k + 1));
   return bits;
 }
 
-// Keep bits of keys 4g .. 4g + 3 (bits 0-3) of query row i in head bh.
-__device__ __forceinline__ uint32_t drop_keep4(const DropArgs& dr, uint32_t g, uint32_t i, uint32_t bh) {
-  const uint4 w = philox4x32_10(make_uint4(g, i, bh, dr.offset), dr.key0, dr.key1);
-  return (uint32_t)(w.x >= dr.t) | ((uint32_t)(w.y >= dr.t) << 1) | ((uint32_t)(w.z >= dr.t) << 2) |
-         ((uint32_t)(w.w >= dr.t) << 3);
+// Keep bits of keys 32 w .. 32 w + 31 (bit c for key 32 w + c) of query row i in
+// head bh: four counters (w * 4 .. w * 4 + 3, i, bh, offset) drawn together.
+__device__ __forceinline__ uint32_t drop_keep32(const DropArgs& dr, uint32_t w, uint32_t i, uint32_t bh) {
+  uint4 c[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) c[g] = make_uint4(4u * w + (uint32_t)g, i, bh, dr.offset);
+  philox4x32_10_n<4>(c, dr.key0, dr.key1);
+  uint32_t bits = 0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) bits |= keep_bits8(c[g], dr.t) << (8 * g);
+  return bits;
 }
 
 // Keep bits, for the key row of this lane (keys are consecutive across lanes, so
-// lanes 4a .. 4a + 3 share one key group), of the 4 n queries q0 .. q0 + 4n - 1:
-// bit c of the result for query q0 + c.  The four lanes of a group each draw the
-// Philox words of one query of every 4 and pass them round, so no word is drawn
-// twice.  All 32 lanes must call it together.
-template <int NQ4>
-__device__ __forceinline__ uint32_t drop_keep_col(const DropArgs& dr, uint32_t key, uint32_t q0,
-                                                  uint32_t bh) {
-  static_assert(NQ4 <= 8, "at most 32 queries per word");
-  const uint32_t lane = threadIdx.x & 31u, r = lane & 3u;
-  uint4 c[NQ4];  // this lane's draws, all at once (see philox4x32_10_n)
+// lanes 8a .. 8a + 7 share one key group), of the 32 queries q0 .. q0 + 31: bit c
+// for query q0 + c.  The eight lanes of a group each draw the counter of one
+// query of every 8 and pass the words round, so no counter is drawn twice.  All
+// 32 lanes must call it together.
+__device__ __forceinline__ uint32_t drop_keep_col32(const DropArgs& dr, uint32_t key, uint32_t q0,
+                                                    uint32_t bh) {
+  const uint32_t lane = threadIdx.x & 31u, r = lane & 7u;
+  uint4 c[4];
 #pragma unroll
-  for (int m = 0; m < NQ4; ++m) c[m] = make_uint4(key >> 2, q0 + 4u * m + r, bh, dr.offset);
-  philox4x32_10_n<NQ4>(c, dr.key0, dr.key1);
+  for (int m = 0; m < 4; ++m) c[m] = make_uint4(key >> 3, q0 + 8u * m + r, bh, dr.offset);
+  philox4x32_10_n<4>(c, dr.key0, dr.key1);
+  const uint32_t sh = 16u * (r & 1u);  // this key's half of a word
   uint32_t bits = 0;
 #pragma unroll
-  for (int m = 0; m < NQ4; ++m) {
-    const uint4 wv = c[m];
+  for (int m = 0; m < 4; ++m) {
 #pragma unroll
-    for (uint32_t t = 0; t < 4; ++t) {
-      // offer word (r - t) mod 4 of this lane's draw; take from the lane whose
-      // draw is for query 4m + ((r + t) mod 4) the word of this lane's key
-      const uint32_t i = (r - t) & 3u;
-      const uint32_t offer = i == 0 ? wv.x : i == 1 ? wv.y : i == 2 ? wv.z : wv.w;
-      const uint32_t got = t == 0 ? offer : __shfl_sync(0xffffffffu, offer, (lane & ~3u) | ((r + t) & 3u));
-      bits |= (uint32_t)(got >= dr.t) << (4u * m + ((r + t) & 3u));
+    for (uint32_t t = 0; t < 8; ++t) {
+      // offer the word that lane (r - t) mod 8 of the group needs for its key; take
+      // from lane (r + t) mod 8, whose draw is for query 8m + ((r + t) mod 8), the
+      // word of this lane's key
+      const uint32_t k = ((r - t) & 7u) >> 1;
+      const uint32_t offer = k == 0 ? c[m].x : k == 1 ? c[m].y : k == 2 ? c[m].z : c[m].w;
+      const uint32_t got = t == 0 ? offer : __shfl_sync(0xffffffffu, offer, (lane & ~7u) | ((r + t) & 7u));
+      bits |= (uint32_t)(((got >> sh) & 0xFFFFu) >= dr.t) << (8u * m + ((r + t) & 7u));
     }
   }
   return bits;

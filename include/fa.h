@@ -70,16 +70,20 @@ typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
  *   mask_block  tokens per mask entry; a positive multiple of 128 when
  *               block_mask is set (ignored otherwise).
  *   dropout_p   probability in [0, 1) of dropping each attention weight (the
- *               softmax output, after masking); kept weights are scaled by
- *               1 / (1 - p).  Dropout is fused into the kernels ("Fusão de
- *               Kernels", reading guide, "Ideias centrais").  0 = none.
+ *               softmax output, after masking); kept weights are scaled by the
+ *               inverse of the keep probability.  Dropout is fused into the
+ *               kernels ("Fusão de Kernels", reading guide, "Ideias centrais").
+ *               0 = none.
  *   dropout_seed, dropout_offset
  *               the keep decision of weight (query i, key j) of head
- *               bh = b * H + h is word (j mod 4) of Philox4x32-10 (Salmon et
- *               al., SC 2011) with counter (j / 4, i, bh, dropout_offset) and
- *               key (seed mod 2^32, seed / 2^32): kept when the word is at
- *               least floor(p * 2^32).  The backward regenerates the same
- *               decisions from the same three values instead of storing them.
+ *               bh = b * H + h is the 16-bit half (low for even j, high for
+ *               odd j) of word (j mod 8) / 2 of Philox4x32-10 (Salmon et al.,
+ *               SC 2011) with counter (j / 8, i, bh, dropout_offset) and key
+ *               (seed mod 2^32, seed / 2^32): kept when the half is at least
+ *               t = floor(p * 2^16), i.e. with probability 1 - t / 2^16 (p to
+ *               within 2^-16), and then scaled by 2^16 / (2^16 - t).  The
+ *               backward regenerates the same decisions from the same three
+ *               values instead of storing them.
  * A query row whose allowed key set is empty gets O = 0 and LSE = -inf, and
  * contributes nothing to the gradients.  With dropout, O is the dropped and
  * rescaled weights times V, while LSE stays the log-sum-exp of the undropped
