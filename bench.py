@@ -28,7 +28,13 @@ sample of the workload on the host cores).
 
 Multi-GPU (torchrun, one process per GPU): every rank runs its own copy of the
 workload (independent batches: weak scaling, no collective on the data path);
-the reported time is the max over ranks.
+the reported time is the max over ranks (max_over_ranks) and the value counts
+every rank's work (job_value), for the device-timed and the end-to-end numbers.
+
+Options beyond the contract's: --fwd-splits S (key-range slices of the forward;
+0 lets the library choose), --no-graph (time separately launched kernels),
+--dropout P (dropout of the attention weights, off in the workloads; the FLOP
+count is unchanged), --no-cpu-baseline, --e2e-steps K.
 """
 from __future__ import annotations
 
