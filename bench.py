@@ -345,6 +345,7 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream, dist=None, world=1):
         dist.barrier()
     t0 = time.perf_counter()
     run(steps)
+    issued = time.perf_counter() - t0  # the host's time to enqueue the steps
     torch.cuda.synchronize()
     s = time.perf_counter() - t0
     if dist:
@@ -354,6 +355,7 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream, dist=None, world=1):
     return {"value": job_value(step_flops * steps, world, s) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "host clock around all steps, synchronised on both sides",
+            "host_issue_ms_per_step": 1000.0 * issued / steps,
             "overlap": "copies on their own streams, double-buffered device tensors; one "
                        "compute and one copy-back stream per causal setting"}
 
