@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 64; ++c)
           if (key >= a.N || (diag && q0 + c < key)) p[c] = 0.f;
       }
-      // P^T for dV: with dropout the kept weights times 1 / (1 - p), else 0
+      // P^T for dV: with dropout the kept weights times the keep scale z, else 0
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         if constexpr (DROP)

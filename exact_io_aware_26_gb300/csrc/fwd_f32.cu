@@ -8,7 +8,7 @@
 // shared memory: S = Q_i K_j^T with a 4 x 4 register block per thread, the
 // running max / sum per row (4 threads per row), then O = O e^(m-m') + P V_j.
 // O / l and LSE = m + ln l are written at the end.  With dropout, the weights
-// that enter P V_j are the kept ones times 1 / (1 - p) and the dropped ones 0
+// that enter P V_j are the kept ones times the keep scale and the dropped ones 0
 // (Philox4x32-10 keep bits, as in the tensor-core kernels); l sums them all.
 #include <cmath>
 

@@ -27,8 +27,8 @@
 // core ("FA3 : Mécanique de la trémie", point 2, realised across CTAs).
 //
 // Dropout (a separate instantiation): after the exponentials of a tile, each
-// weight whose Philox4x32-10 word is below the threshold is replaced by 0 and
-// each other one is multiplied by 1 / (1 - p) before P~ V; l sums the undropped
+// weight whose 16-bit Philox4x32-10 draw is below the threshold is replaced by 0 and
+// each other one is multiplied by the keep scale before P~ V; l sums the undropped
 // weights, so O / l and LSE are those of the dropped-out attention and of the
 // undropped scores respectively.
 //
