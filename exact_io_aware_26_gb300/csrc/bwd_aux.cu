@@ -144,6 +144,64 @@ __global__ void __launch_bounds__(256) bwd_finalize_fixup_kernel(const BwdArgs a
   }
 }
 
+// Query-split backward (qsplit > 1): block `part` of key tile `unit` adds its
+// slice of the unit's qsplit partial slots and writes that slice of dV and
+// dK (dK times the score scale).
+template <int D, bool F16>
+__device__ void qsplit_key_tile(const BwdArgs& a, int unit, int part) {
+  const int BH = a.B * a.H;
+  const int kt = unit / BH, bh = unit % BH;
+  constexpr int PER = 2 * 128 * D / 4;  // float4 per slot ([dV | dK])
+  constexpr int SLICE = PER / kFixupParts;
+  const float4* base = reinterpret_cast<const float4*>(a.slots) + (size_t)unit * a.qsplit * PER;
+  for (int e = part * SLICE + (int)threadIdx.x; e < (part + 1) * SLICE; e += blockDim.x) {
+    float4 acc = base[e];
+    for (int sp = 1; sp < a.qsplit; ++sp) {
+      const float4 v = base[(size_t)sp * PER + e];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int f = e * 4;              // first float of the four
+    const int which = f / (128 * D);  // 0: dV, 1: dK
+    const int row = (f / D) % 128;
+    const int col = f % D;
+    const int key = kt * 128 + row;
+    if (key >= a.N) continue;
+    const float mul = which == 0 ? 1.f : a.scale;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? a.dV : a.dK) + ((size_t)bh * a.N + key) * D + col;
+    uint2 o;
+    o.x = pack2<F16>(acc.x * mul, acc.y * mul);
+    o.y = pack2<F16>(acc.z * mul, acc.w * mul);
+    *reinterpret_cast<uint2*>(dst) = o;
+  }
+}
+
+// Blocks [0, dq_blocks) convert the dQ accumulator; blocks after them,
+// kFixupParts per key tile, add up a query-split backward's partial dK, dV.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_finalize_qsplit_kernel(const BwdArgs a, int dq_blocks) {
+  if ((int)blockIdx.x >= dq_blocks) {
+    const int k = (int)blockIdx.x - dq_blocks;
+    qsplit_key_tile<D, F16>(a, k / kFixupParts, k % kFixupParts);
+    return;
+  }
+  const long long n8 = (long long)a.B * a.H * a.N * D / 8;
+  const float4* acc = reinterpret_cast<const float4*>(a.dQacc);
+  uint4* dQ = reinterpret_cast<uint4*>(a.dQ);
+  const long long nthreads = (long long)dq_blocks * blockDim.x;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += nthreads) {
+    const float4 x = acc[2 * t], y = acc[2 * t + 1];
+    uint4 o;
+    o.x = pack2<F16>(x.x * a.scale, x.y * a.scale);
+    o.y = pack2<F16>(x.z * a.scale, x.w * a.scale);
+    o.z = pack2<F16>(y.x * a.scale, y.y * a.scale);
+    o.w = pack2<F16>(y.z * a.scale, y.w * a.scale);
+    dQ[t] = o;
+  }
+}
+
 __global__ void wait_selftest_kernel(Report rep) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_cta;
@@ -180,6 +238,13 @@ cudaError_t pre_t(const BwdArgs& a, cudaStream_t s) {
 }
 
 template <int D, bool F16>
+cudaError_t fin_qsplit_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
+  const int units = a.B * a.H * ((a.N + 127) / 128);
+  bwd_finalize_qsplit_kernel<D, F16><<<dq_blocks + units * kFixupParts, 256, 0, s>>>(a, dq_blocks);
+  return cudaGetLastError();
+}
+
+template <int D, bool F16>
 cudaError_t fin_fixup_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
   bwd_finalize_fixup_kernel<D, F16><<<dq_blocks + (a.G - 1) * kFixupParts, 256, 0, s>>>(a, dq_blocks);
   return cudaGetLastError();
@@ -195,6 +260,11 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_
 cudaError_t launch_bwd_finalize(const BwdArgs& a, int d, bool f16, cudaStream_t s) {
   const long long n8 = (long long)a.B * a.H * a.N * d / 8;
   const int grid = grid_for(n8, 256);
+  if (a.qsplit > 1) {
+    // query-split main kernel: the same launch adds up the partial dK, dV
+    if (d == 64) return f16 ? fin_qsplit_t<64, true>(a, grid, s) : fin_qsplit_t<64, false>(a, grid, s);
+    return f16 ? fin_qsplit_t<128, true>(a, grid, s) : fin_qsplit_t<128, false>(a, grid, s);
+  }
   if (a.G > 1) {
     // persistent main kernel: the same launch also finishes the shared key tiles
     if (d == 64) return f16 ? fin_fixup_t<64, true>(a, grid, s) : fin_fixup_t<64, false>(a, grid, s);

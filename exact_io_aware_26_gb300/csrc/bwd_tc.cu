@@ -118,7 +118,7 @@ __device__ __forceinline__ float d_of(const BwdArgs& a, int bh, int q) {
   return q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
 }
 
-template <int D, bool F16, int NG, bool DROP>
+template <int D, bool F16, int NG, bool DROP, bool QS>
 __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -132,10 +132,15 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
 
   const int BH = a.B * a.H;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const int kt = (int)(blockIdx.x / BH);  // causal: low key tiles see the most queries
-  const int bh = (int)(blockIdx.x % BH);
+  // QS (a query-split launch, qsplit = 2): CTAs 2u and 2u + 1 share key tile u
+  const int unit = QS ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int kt = unit / BH;  // causal: low key tiles see the most queries
+  const int bh = unit % BH;
   const int b = bh / a.H, h = bh % a.H;
-  const int qt_begin = a.m.causal ? kt : 0;
+  // this CTA's query tiles: [qt_begin, q_end) (all of them without QS)
+  const int q_half = (n_tiles + 1) / 2;
+  const int qt_begin = QS ? (int)(blockIdx.x & 1) * q_half : (a.m.causal ? kt : 0);
+  const int q_end = QS ? min(n_tiles, qt_begin + q_half) : n_tiles;
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
   const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_dp_full = bar(2), bar_dp_free = bar(3),
@@ -185,8 +190,8 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       tma_load_3d(sb + L::K + c * (kTile * 128), &tmK, bar_kv, c * 64, kt * kTile, bh);
       tma_load_3d(sb + L::V + c * (kTile * 128), &tmV, bar_kv, c * 64, kt * kTile, bh);
     }
-    for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles && pre < NS;
-         qt = next_q(a.m, b, h, qt + 1, kt, n_tiles), ++pre) {
+    for (int qt = next_q(a.m, b, h, qt_begin, kt, q_end); qt < q_end && pre < NS;
+         qt = next_q(a.m, b, h, qt + 1, kt, q_end), ++pre) {
       const uint32_t dst = sb + L::QS + (uint32_t)pre * 2u * L::TILE;
       mbar_arrive_expect_tx(bar_qf(pre), 2 * L::TILE);
       for (int c = 0; c < D / 64; ++c) {
@@ -211,8 +216,8 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     // barrier covers Q, dO and the statistics together.
     pre = __shfl_sync(0xffffffffu, pre, 0);
     int it = 0;
-    for (int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles); qt < n_tiles;
-         qt = next_q(a.m, b, h, qt + 1, kt, n_tiles)) {
+    for (int qt = next_q(a.m, b, h, qt_begin, kt, q_end); qt < q_end;
+         qt = next_q(a.m, b, h, qt + 1, kt, q_end)) {
       const int s = it % NS;
       if (it >= NS && !warp_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
       if (lane == 0 && it >= pre) {
@@ -292,8 +297,8 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         tc_mma_ss_elect(tDQ, dS_mn + mnmajor_step(kk), dK_mn + mnmajor_step(kk), idQ, kk > 0 ? 1u : 0u);
       };
       bool ok = warp_wait(w, bar_kv, 0);
-      int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
-      if (ok && qt < n_tiles && (ok = warp_wait(w, bar_qf(0), 0))) {
+      int qt = next_q(a.m, b, h, qt_begin, kt, q_end);
+      if (ok && qt < q_end && (ok = warp_wait(w, bar_qf(0), 0))) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
@@ -303,9 +308,9 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         tc_commit_elect(bar_s_full);
         tc_commit_elect(bar_dp_full);
       }
-      for (int it = 0; ok && qt < n_tiles; ++it) {
-        const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
-        const bool next = qn < n_tiles;
+      for (int it = 0; ok && qt < q_end; ++it) {
+        const int qn = next_q(a.m, b, h, qt + 1, kt, q_end);
+        const bool next = qn < q_end;
         // Within each group the MMA the compute warps wait for next goes first
         // (MMAs execute in issue order).
         if (!(ok = warp_wait(w, bar_p_full, it & 1))) break;
@@ -470,10 +475,10 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     };
     bool ok = true;
     int it = 0;
-    int qt = next_q(a.m, b, h, qt_begin, kt, n_tiles);
-    if (qt < n_tiles) ok = p_phase(0, qt);
-    for (; ok && qt < n_tiles; ++it) {
-      const int qn = next_q(a.m, b, h, qt + 1, kt, n_tiles);
+    int qt = next_q(a.m, b, h, qt_begin, kt, q_end);
+    if (qt < q_end) ok = p_phase(0, qt);
+    for (; ok && qt < q_end; ++it) {
+      const int qn = next_q(a.m, b, h, qt + 1, kt, q_end);
       // ---- dS_i = P_i * (dP_i - D), with dropout P_i * (z_i dP_i - D)
       if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
       tc_fence_after();
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       if (lane == 0) mbar_arrive(bar_ds_full);
 
       // ---- P of the next query tile, while dK_i, dQ_i, dP^T_{i+1} run
-      if (qn < n_tiles && !(ok = p_phase(it + 1, qn))) break;
+      if (qn < q_end && !(ok = p_phase(it + 1, qn))) break;
 
       // ---- dQ_i (TMEM lane = query row) -> fp32 accumulator by TMA reduce-add
       if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
@@ -560,7 +565,32 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     }
     // tcgen05.ld is .sync.aligned: every lane of the warp loads (the condition
     // `ok`/`have` is warp-uniform); only the stores are predicated on the row
-    if (ok) {
+    if constexpr (QS) {
+      if (ok) {
+        // half of the key tile's query tiles: fp32 partial sums, dK unscaled
+        float* slot = a.slots + (size_t)blockIdx.x * (2 * kTile * D);
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = (which == 0 ? L::T_DV : L::T_DK) + g * L::DQG;
+          float* dst = slot + (size_t)which * (kTile * D) + (size_t)r * D + g * L::DQG;
+          constexpr int EC = L::DQG < 32 ? L::DQG : 32;
+#pragma unroll
+          for (int c0 = 0; c0 < L::DQG; c0 += EC) {
+            uint32_t u[EC];
+            if (have) {
+              tmem_ld_n<EC>(tmem + col + lane_off + c0, u);
+            } else {
+#pragma unroll
+              for (int i = 0; i < EC; ++i) u[i] = 0u;
+            }
+#pragma unroll
+            for (int v = 0; v < EC / 4; ++v)
+              *reinterpret_cast<float4*>(dst + c0 + v * 4) =
+                  make_float4(__uint_as_float(u[4 * v]), __uint_as_float(u[4 * v + 1]),
+                              __uint_as_float(u[4 * v + 2]), __uint_as_float(u[4 * v + 3]));
+          }
+        }
+      }
+    } else if (ok) {
       const bool store = key < a.N;
       constexpr int EC = L::DQG < 32 ? L::DQG : 32;  // columns per TMEM load
       uint16_t* dVrow = reinterpret_cast<uint16_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * L::DQG;
@@ -608,7 +638,13 @@ cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   // enough); with four they would fall into other warps' boxes
   constexpr int NG = (D == 64) ? 4 : 2;
   using L = BwdLayout<D, NG>;
-  auto kern = a.drop.on ? bwd_tc_kernel<D, F16, NG, true> : bwd_tc_kernel<D, F16, NG, false>;
+  // query-split launches (two CTAs per key tile) exist at d = 64 only
+  if constexpr (D == 128) {
+    if (a.qsplit > 1) return cudaErrorInvalidValue;
+  }
+  constexpr bool kQs = (D == 64);
+  auto kern = a.qsplit > 1 ? (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, kQs> : bwd_tc_kernel<D, F16, NG, false, kQs>)
+                           : (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, false> : bwd_tc_kernel<D, F16, NG, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   // the first a.direct key tiles, one CTA each (the rest, if any, go to the

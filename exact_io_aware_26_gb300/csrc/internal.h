@@ -90,6 +90,11 @@ struct BwdArgs {
   int G;
   int u0;
   float* slots;
+  // qsplit = 2 (d = 64, non-causal, direct CTAs only): the direct grid has two
+  // CTAs per key tile, CTA 2u + s taking the s-th half of the query tiles and
+  // writing fp32 [dV | dK] partial sums (dK unscaled) to slot 2u + s; the
+  // finalize kernel adds them up.  1: one CTA per key tile.
+  int qsplit;
   DropArgs drop;
   Report rep;
 };
