@@ -214,10 +214,13 @@ fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V
  * preprocess: D = rowsum(dO * O) into the workspace, dQ accumulator zeroed.
  * main: recompute P tile by tile, accumulate dK, dV per key tile and add
  *       scale-free dQ contributions into the accumulator.  One CTA per key
- *       tile, whose dK, dV it writes; without a block mask and with fewer key
- *       tiles than SMs, persistent CTAs (about one per SM) split the
- *       (key tile, query tile) iterations evenly instead: a key tile whose
- *       iterations several CTAs share gets fp32 partial sums in the workspace.
+ *       tile, whose dK, dV it writes.  Without a block mask and with fewer key
+ *       tiles than SMs: at d = 64, non-causal, with at most half as many key
+ *       tiles as SMs, two CTAs per key tile, each with half of its query tiles
+ *       and fp32 partial dK, dV in the workspace; otherwise persistent CTAs
+ *       (about one per SM) that split the (key tile, query tile) iterations
+ *       evenly, a key tile whose iterations several CTAs share getting fp32
+ *       partial sums in the workspace.
  * finalize: dQ = scale * accumulator, converted to `dtype`, and dK, dV of the
  *       shared key tiles from their partial sums.  Must follow the main stage
  *       of the same call sequence (same p, workspace and fa_set_bwd_ctas). */
