@@ -231,29 +231,26 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
   a.u0 = (int)units;
   a.qsplit = 1;
   if (!p->block_mask) {
-    // ... unless that leaves SMs idle: with fewer key tiles than CTAs (one per
-    // SM, at most kBwdMaxCtas, or the cap set by fa_set_bwd_ctas) persistent
-    // stream-K CTAs take them all.  A cap also splits the last one to two
-    // waves' worth of a non-causal grid that would end in a partly filled wave
-    // (off by default: on GB300 the persistent kernel's slower tiles cancel
-    // what the fuller last wave gains).
+    // ... unless that leaves SMs idle, with fewer key tiles than CTAs (one per
+    // SM, at most kBwdMaxCtas, or the cap set by fa_set_bwd_ctas):
     long long G = device_sms();
     if (G > kBwdMaxCtas) G = kBwdMaxCtas;
     const int cap = g_bwd_ctas.load();
     if (cap > 0 && cap < G) G = cap;
-    long long u0 = -1;
-#ifndef FA_BWD_QSPLIT
-#define FA_BWD_QSPLIT 1
-#endif
-    if (FA_BWD_QSPLIT && p->d == 64 && !p->causal && 2 * units <= G && n >= 4) {
-      // d = 64, non-causal, at most half as many key tiles as CTAs: two CTAs
-      // per key tile, each with half of its query tiles, and the partial dK,
-      // dV added up by the finalize kernel (cheaper per (key tile, query tile)
-      // pair than the persistent CTAs, which pay for their piece changes)
+    if (p->d == 64 && !p->causal && 2 * units <= G && n >= 4) {
+      // - d = 64, non-causal, at most half as many key tiles as CTAs: two CTAs
+      //   per key tile, each with half of its query tiles, the partial dK, dV
+      //   added up by the finalize kernel (cheaper per (key tile, query tile)
+      //   pair than the persistent CTAs, which pay for their piece changes);
       a.qsplit = 2;
       a.direct = (int)(2 * units);
       return a;
     }
+    // - otherwise persistent stream-K CTAs take them all.  A cap also hands the
+    //   last one to two waves' worth of a non-causal grid that would end in a
+    //   partly filled wave to persistent CTAs (off by default: on GB300 the
+    //   persistent kernel's slower tiles cancel what the fuller last wave gains).
+    long long u0 = -1;
     if (units < G) {
       u0 = 0;
     } else if (cap > 0 && !p->causal && units % G != 0) {
