@@ -33,6 +33,14 @@ seed // 2^32) is at least t = floor(p * 2^16), else set to 0; kept weights are
 scaled by 2^16 / (2^16 - t) (``dropout_scale``), the inverse of the keep
 probability.  m, l and LSE stay those of the undropped softmax.
 
+* ``e4m3_encode`` / ``e4m3_decode`` / ``fp8_block_scale`` / ``hadamard_rotate`` /
+  ``fp8_quantize`` / ``fp8_attention_fwd`` -- the FP8 forward with incoherent
+  processing ("Trois idées pour FA3", marketmaker.cc, point 3: a random rotation
+  of the query and key vectors before block quantisation spreads outliers over the
+  coordinates); ``fp8_oracle.c`` states the readings taken where the page is silent
+  (randomised Sylvester-Hadamard rotation, power-of-two scale per 128-row block,
+  e4m3 round-to-nearest-even, P~ quantised as e4m3(256 P~) in the online loop).
+
 Masks: ``mask`` is a uint8 array of shape [T, T] (shared by every batch and
 head) or [B, H, T, T], with T = ceil(N / mask_block); entry [i // mb, j // mb]
 keeps (1) or hides (0) the pair (query i, key j) ("Extensão: Block-Sparse
@@ -48,16 +56,19 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRCS = (_SRC, os.path.join(_HERE, "fp8_oracle.c"))
 _SO = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile ``attn_oracle.c`` into ``liboracle.so`` next to it (gcc, OpenMP)."""
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+    """Compile ``attn_oracle.c`` and ``fp8_oracle.c`` into ``liboracle.so`` next to them
+    (gcc, OpenMP)."""
+    if force or not os.path.exists(_SO) or any(os.path.getmtime(_SO) < os.path.getmtime(f)
+                                               for f in _SRCS):
         tmp = _SO + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=gnu11", "-fopenmp", "-fPIC", "-shared",
-               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+               "-ffp-contract=off", "-o", tmp, *_SRCS, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _SO)
     return _SO
@@ -88,6 +99,16 @@ def _load():
                                  U32, I]
     lib.orc_philox4x32_10.argtypes = [P, P, P]
     lib.orc_dropout_keep.argtypes = [I, I, I, Dd, U64, U32, P]
+    lib.orc_e4m3_encode.argtypes = [LL, P, P]
+    lib.orc_e4m3_decode.argtypes = [LL, P, P]
+    lib.orc_fp8_block_scale.argtypes = [Dd]
+    lib.orc_fp8_block_scale.restype = Dd
+    lib.orc_hadamard_rotate.argtypes = [LL, I, P, P, Dd, P]
+    lib.orc_fp8_quantize.argtypes = [I, I, I, P, P, P, P, I, LL, P, P, P, P, P, P]
+    lib.orc_fp8_fwd.argtypes = [I, I, I, P, P, P, LL, P, P, P, I, Dd, I, P, I, P, P]
+    for f in ("orc_e4m3_encode", "orc_e4m3_decode", "orc_hadamard_rotate", "orc_fp8_quantize",
+              "orc_fp8_fwd"):
+        getattr(lib, f).restype = None
     for f in ("orc_fwd", "orc_fwd_rows", "orc_fwd_blockwise_f64",
               "orc_fwd_blockwise_f32", "orc_bwd", "orc_bwd_rows", "orc_philox4x32_10",
               "orc_dropout_keep"):
@@ -251,3 +272,83 @@ def attention_bwd_rows(qh, kh, vh, doh, qrows, krows, scale, causal=False, mask_
 def head_mask(mask, b, h, N, mask_block=128):
     """The [T,T] mask matrix that applies to head (b, h), or None."""
     return _head_mask(mask, b, h, N, mask_block)
+
+
+# ---------------------------------------------------------------------------
+# FP8 forward with incoherent processing (fp8_oracle.c)
+# ---------------------------------------------------------------------------
+
+def e4m3_encode(x) -> np.ndarray:
+    """e4m3 codes (uint8) of x: round to nearest, ties to even, saturating at +-448."""
+    a = _f64(x)
+    out = np.zeros(a.shape, dtype=np.uint8)
+    _load().orc_e4m3_encode(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (fp64) of e4m3 codes."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(c.shape, dtype=np.float64)
+    _load().orc_e4m3_decode(c.size, _ptr(c), _ptr(out))
+    return out
+
+
+def fp8_block_scale(amax: float) -> float:
+    """Smallest power of two sigma with amax / sigma <= 448 (1 for amax = 0)."""
+    return float(_load().orc_fp8_block_scale(float(amax)))
+
+
+def hadamard_rotate(x, signs, post=1.0) -> np.ndarray:
+    """Rows of x times diag(signs) H_d times post (H_d the Sylvester Hadamard matrix)."""
+    a = _f64(x)
+    d = a.shape[-1]
+    sg = _f64(signs).reshape(d)
+    out = np.zeros_like(a)
+    _load().orc_hadamard_rotate(a.size // d, d, _ptr(a), _ptr(sg), float(post), _ptr(out))
+    return out
+
+
+def fp8_vt_cols(N: int) -> int:
+    """Row length of the transposed V codes: N rounded up to a multiple of 16."""
+    return (N + 15) // 16 * 16
+
+
+def fp8_quantize(q, k, v, signs=None, block=128):
+    """Rotation (signs given) and block quantisation of [B,H,N,d] Q, K, V.
+
+    Returns a dict with q8, k8 [B,H,N,d] and vt8 [B,H,d,fp8_vt_cols(N)] (uint8 e4m3
+    codes; vt8 is V transposed, zero past N) and sq, sk, sv [B,H,ceil(N/block)] (fp64
+    powers of two), the layout the CUDA library's FP8 forward takes."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = q.shape
+    T = (N + block - 1) // block
+    ld = fp8_vt_cols(N)
+    r = {"q8": np.zeros((B, H, N, d), np.uint8), "k8": np.zeros((B, H, N, d), np.uint8),
+         "vt8": np.zeros((B, H, d, ld), np.uint8), "sq": np.zeros((B, H, T)),
+         "sk": np.zeros((B, H, T)), "sv": np.zeros((B, H, T))}
+    sg = None if signs is None else _f64(signs).reshape(d)
+    _load().orc_fp8_quantize(B * H, N, d, _ptr(q), _ptr(k), _ptr(v),
+                             None if sg is None else _ptr(sg), int(block), ld,
+                             _ptr(r["q8"]), _ptr(r["k8"]), _ptr(r["vt8"]), _ptr(r["sq"]),
+                             _ptr(r["sk"]), _ptr(r["sv"]))
+    return r
+
+
+def fp8_attention_fwd(t, scale, causal=False, mask=None, mask_block=128, block=128):
+    """The FP8 forward on the codes and scales of ``fp8_quantize`` -> (O, LSE), fp64."""
+    q8, k8, vt8 = (np.ascontiguousarray(t[n], dtype=np.uint8) for n in ("q8", "k8", "vt8"))
+    sq, sk, sv = (_f64(t[n]) for n in ("sq", "sk", "sv"))
+    B, H, N, d = q8.shape
+    O = np.zeros((B, H, N, d))
+    LSE = np.zeros((B, H, N))
+    m = None
+    if mask is not None:
+        m = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
+        T = (N + mask_block - 1) // mask_block
+        if m.shape != (T, T):
+            raise ValueError(f"mask shape {m.shape} != {(T, T)}")
+    _load().orc_fp8_fwd(B * H, N, d, _ptr(q8), _ptr(k8), _ptr(vt8), vt8.shape[-1], _ptr(sq),
+                        _ptr(sk), _ptr(sv), int(block), float(scale), int(bool(causal)),
+                        None if m is None else _ptr(m), int(mask_block), _ptr(O), _ptr(LSE))
+    return O, LSE

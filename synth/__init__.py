@@ -18,6 +18,13 @@ independent, drawn in the order Q, K, V, dO, then the block mask):
   off-diagonal entries 1 with probability ``mask_p``; one mask shared by every
   batch and head.
 
+* outliers (``outlier_p``): after the i.i.d. draw, each entry of Q, K and V is
+  replaced, with probability ``outlier_p``, by ``outlier_sd`` * N(0, 1) (one
+  ``random`` draw for the choice, then one ``standard_normal`` for the value,
+  per tensor) -- heavy coordinates of the kind that ruin naive FP8 attention.
+* rotation signs: ``rotation_signs(d, seed)``, d values in {-1, +1} from their own
+  generator (PCG64(seed)), the random diagonal the FP8 path rotates with.
+
 The five named workloads stand in for the pages' workloads (a trading day of
 23,400 one-second steps with 12 heads, the 8192-token fp16 single-head case, a
 block-sparse long sequence); no dataset is read.
@@ -97,10 +104,17 @@ def block_mask(rng: np.random.Generator, N: int, mask_block: int, p: float) -> n
     return m
 
 
+def rotation_signs(d: int, seed: int) -> torch.Tensor:
+    """d random signs (fp32 tensor of -1.0 / +1.0) from PCG64(seed)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return torch.from_numpy(np.where(rng.random(d) < 0.5, -1.0, 1.0).astype(np.float32))
+
+
 def make_inputs(B: int, H: int, N: int, d: int, dtype: str, seed: int, *,
                 qkv_scale: float = 1.0, ar1_rho: Optional[float] = None,
                 mask_p: Optional[float] = None, mask_block: int = 128,
-                backward: bool = True) -> dict:
+                backward: bool = True, outlier_p: float = 0.0,
+                outlier_sd: float = 10.0) -> dict:
     """Draw Q, K, V (and dO, and a block mask when mask_p is set) as CPU tensors.
 
     Returns a dict with torch tensors ``q, k, v`` (and ``do``) in the dtype,
@@ -115,6 +129,10 @@ def make_inputs(B: int, H: int, N: int, d: int, dtype: str, seed: int, *,
             x = _ar1(rng, shape, ar1_rho)
         else:
             x = _iid(rng, shape, qkv_scale)
+        if outlier_p > 0.0:
+            hit = rng.random(shape) < outlier_p
+            x = np.where(hit, np.float32(outlier_sd) * rng.standard_normal(shape, dtype=np.float32),
+                         x)
         out[name] = torch.from_numpy(x).to(td).contiguous()
     if backward:
         out["do"] = torch.from_numpy(_iid(rng, shape, 1.0)).to(td).contiguous()
