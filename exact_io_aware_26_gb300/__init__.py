@@ -90,6 +90,9 @@ def load() -> ctypes.CDLL:
         "fa_status_string": (ctypes.c_char_p, [I]),
         "fa_last_error": (ctypes.c_char_p, []),
         "fa_version": (I, []),
+        "fa_fp8_vt_cols": (I, [I]),
+        "fa_fp8_quantize": (I, [PP, P, P, P, P, P, P, P, P, P, P, P]),
+        "fa_fwd_fp8": (I, [PP, P, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(lib, name)
@@ -181,6 +184,74 @@ def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, mask_block
     _check(load().fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                          _stream(stream)), "fa_fwd")
     return out, lse
+
+
+def fp8_vt_cols(N: int) -> int:
+    """fa_fp8_vt_cols: row length of the transposed V codes (N rounded up to 16)."""
+    return int(load().fa_fp8_vt_cols(int(N)))
+
+
+def fp8_quantize(q, k, v, signs=None, stream=None) -> dict:
+    """fa_fp8_quantize: rotation (``signs``: d floats of +-1 on the device, or None) and
+    block quantisation of [B,H,N,d] Q, K, V.  Returns q8, k8 [B,H,N,d] and vt8
+    [B,H,d,fp8_vt_cols(N)] (uint8 e4m3 codes) and sq, sk, sv [B,H,ceil(N/128)] (fp32)."""
+    import torch
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(t, n, q)
+    B, H, N, d = q.shape
+    if signs is not None and not (signs.is_cuda and signs.dtype == torch.float32
+                                  and signs.is_contiguous() and signs.numel() == d):
+        raise ValueError(f"signs must be a contiguous cuda float32 tensor of {d} values")
+    T = (N + 127) // 128
+    u8 = dict(dtype=torch.uint8, device=q.device)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    t = {"q8": torch.empty((B, H, N, d), **u8), "k8": torch.empty((B, H, N, d), **u8),
+         "vt8": torch.empty((B, H, d, fp8_vt_cols(N)), **u8), "sq": torch.empty((B, H, T), **f32),
+         "sk": torch.empty((B, H, T), **f32), "sv": torch.empty((B, H, T), **f32)}
+    p, _ = make_params(q)
+    _check(load().fa_fp8_quantize(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(signs),
+                                  _ptr(t["q8"]), _ptr(t["k8"]), _ptr(t["vt8"]), _ptr(t["sq"]),
+                                  _ptr(t["sk"]), _ptr(t["sv"]), _stream(stream)),
+           "fa_fp8_quantize")
+    return t
+
+
+def attention_fwd_fp8_codes(t: dict, scale, causal=False, block_mask=None, mask_block=128,
+                            dtype=None, out=None, lse=None, stream=None):
+    """O, LSE = fa_fwd_fp8 on the codes and scales of ``fp8_quantize`` (same keys and
+    layout); O in ``dtype`` (default bf16)."""
+    import torch
+    q8 = t["q8"]
+    B, H, N, d = q8.shape
+    T = (N + 127) // 128
+    shapes = {"q8": (B, H, N, d), "k8": (B, H, N, d), "vt8": (B, H, d, fp8_vt_cols(N)),
+              "sq": (B, H, T), "sk": (B, H, T), "sv": (B, H, T)}
+    for n, shp in shapes.items():
+        x = t[n]
+        want = torch.uint8 if n.endswith("8") else torch.float32
+        if not (x.is_cuda and x.is_contiguous() and x.dtype == want and tuple(x.shape) == shp):
+            raise ValueError(f"{n} must be a contiguous cuda {want} tensor of shape {shp}")
+    dtype = torch.bfloat16 if dtype is None else dtype
+    p, keep = make_params(torch.empty((B, H, N, d), dtype=dtype, device="meta"), scale, causal,
+                          block_mask, mask_block)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=dtype, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    _check(load().fa_fwd_fp8(ctypes.byref(p), _ptr(t["q8"]), _ptr(t["k8"]), _ptr(t["vt8"]),
+                             _ptr(t["sq"]), _ptr(t["sk"]), _ptr(t["sv"]), _ptr(out), _ptr(lse),
+                             _stream(stream)), "fa_fwd_fp8")
+    return out, lse
+
+
+def attention_fwd_fp8(q, k, v, signs=None, scale=None, causal=False, block_mask=None,
+                      mask_block=128, stream=None):
+    """O, LSE of the FP8 forward: fa_fp8_quantize then fa_fwd_fp8 (O in q's dtype)."""
+    t = fp8_quantize(q, k, v, signs, stream)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return attention_fwd_fp8_codes(t, scale, causal, block_mask, mask_block, q.dtype,
+                                   stream=stream)
 
 
 def num_splits(p: FaParams, num_sms: int = 0) -> int:

@@ -18,8 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
-SOURCES = ["fa_api.cu", "fwd_tc.cu", "fwd_persist.cu", "fwd_f32.cu", "bwd_tc.cu", "bwd_persist.cu", "bwd_aux.cu", "fa_noalloc.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "bwd_sched.cuh"]
+SOURCES = ["fa_api.cu", "fwd_tc.cu", "fwd_persist.cu", "fwd_f32.cu", "bwd_tc.cu", "bwd_persist.cu", "bwd_aux.cu", "fa_noalloc.cu", "fwd_fp8.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "bwd_sched.cuh", "fp8.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "bwd_sched.cuh"
+#include "fp8.h"
 #include "internal.h"
 
 using namespace fa;
@@ -180,6 +181,29 @@ fa_status encode_dqacc(CUtensorMap* m, const float* ptr, const fa_params* p, int
   return FA_OK;
 }
 
+// An 8-bit tensor {x, y, z} (x contiguous) as a 3-D TMA map with box {bx, by, 1}
+// and the given swizzle; reads past the extents give zero.
+fa_status encode_u8(CUtensorMap* m, const void* ptr, uint64_t x, uint64_t y, uint64_t z, uint32_t bx,
+                    uint32_t by, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_err("cuTensorMapEncodeTiled is not available from the driver");
+    return FA_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)x, (cuuint64_t)y, (cuuint64_t)z};
+  const cuuint64_t strides[2] = {(cuuint64_t)x, (cuuint64_t)(x * y)};
+  const cuuint32_t box[3] = {bx, by, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_err("cuTensorMapEncodeTiled (8-bit operand) failed (CUresult %d)", (int)r);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 MaskArgs mask_args(const fa_params* p) {
   MaskArgs m;
   m.causal = p->causal ? 1 : 0;
@@ -299,6 +323,116 @@ fa_status need16(const void* ptr, const char* name) {
 extern "C" {
 
 int fa_version(void) { return 100; }
+
+int fa_fp8_vt_cols(int N) { return N < 1 ? 0 : (N + 15) / 16 * 16; }
+
+namespace {
+fa_status fp8_check(const fa_params* p) {
+  FA_TRY(fa_check(p, 0));
+  if (p->dtype == FA_F32) {
+    set_err("the FP8 path takes fp16 or bf16 tensors");
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (p->dropout_p > 0.f) {
+    set_err("the FP8 forward has no dropout");
+    return FA_ERR_UNSUPPORTED;
+  }
+  return FA_OK;
+}
+
+fa_status need_scales(const float* a, const float* b, const float* c) {
+  for (const float* x : {a, b, c})
+    if (!x || !aligned(x, 4)) {
+      set_err("a block-scale array is NULL or not 4-byte aligned");
+      return FA_ERR_INVALID;
+    }
+  return FA_OK;
+}
+}  // namespace
+
+fa_status fa_fp8_quantize(const fa_params* p, const void* Q, const void* K, const void* V,
+                          const float* signs, void* q8, void* k8, void* vt8, float* sq, float* sk,
+                          float* sv, void* stream) {
+  FA_TRY(fp8_check(p));
+  FA_TRY(need16(Q, "Q"));
+  FA_TRY(need16(K, "K"));
+  FA_TRY(need16(V, "V"));
+  FA_TRY(need16(q8, "q8"));
+  FA_TRY(need16(k8, "k8"));
+  FA_TRY(need16(vt8, "vt8"));
+  FA_TRY(need_scales(sq, sk, sv));
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  if (signs) {  // read by the kernel: it must be device memory
+    cudaPointerAttributes at{};
+    if (!aligned(signs, 4) || cudaPointerGetAttributes(&at, signs) != cudaSuccess ||
+        (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)) {
+      cudaGetLastError();
+      set_err("signs must be 4-byte aligned device memory (d floats) or NULL");
+      return FA_ERR_INVALID;
+    }
+  }
+  Fp8QuantArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.BH = p->B * p->H;
+  a.N = p->N;
+  a.T = (p->N + 127) / 128;
+  a.ld = fa_fp8_vt_cols(p->N);
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.signs = signs;
+  a.q8 = static_cast<uint8_t*>(q8);
+  a.k8 = static_cast<uint8_t*>(k8);
+  a.vt8 = static_cast<uint8_t*>(vt8);
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  const cudaError_t e = launch_fp8_quantize(a, p->d, p->dtype == FA_F16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 quantise launch");
+  return FA_OK;
+}
+
+fa_status fa_fwd_fp8(const fa_params* p, const void* q8, const void* k8, const void* vt8,
+                     const float* sq, const float* sk, const float* sv, void* O, float* LSE,
+                     void* stream) {
+  FA_TRY(fp8_check(p));
+  FA_TRY(need16(q8, "q8"));
+  FA_TRY(need16(k8, "k8"));
+  FA_TRY(need16(vt8, "vt8"));
+  FA_TRY(need16(O, "O"));
+  FA_TRY(need_scales(sq, sk, sv));
+  if (!LSE || !aligned(LSE, 4)) {
+    set_err("LSE is NULL or misaligned");
+    return FA_ERR_INVALID;
+  }
+  DevStatus* st = nullptr;
+  FA_TRY(device_ready(&st));
+  const uint64_t BH = (uint64_t)p->B * p->H, d = (uint64_t)p->d;
+  CUtensorMap tm[3];
+  const CUtensorMapSwizzle sw = p->d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  FA_TRY(encode_u8(&tm[0], q8, d, (uint64_t)p->N, BH, (uint32_t)d, 128, sw));
+  FA_TRY(encode_u8(&tm[1], k8, d, (uint64_t)p->N, BH, (uint32_t)d, 128, sw));
+  FA_TRY(encode_u8(&tm[2], vt8, (uint64_t)fa_fp8_vt_cols(p->N), d, BH, 128, (uint32_t)d,
+                   CU_TENSOR_MAP_SWIZZLE_128B));
+  Fp8FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = p->B;
+  a.H = p->H;
+  a.N = p->N;
+  a.T = (p->N + 127) / 128;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.m = mask_args(p);
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  a.O = O;
+  a.LSE = LSE;
+  a.rep = make_report(st);
+  const cudaError_t e = launch_fwd_fp8(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 forward launch");
+  return FA_OK;
+}
 
 const char* fa_last_error(void) { return g_err; }
 

@@ -295,6 +295,53 @@ const char* fa_last_error(void);
 /* Library interface version (major * 100 + minor). */
 int fa_version(void);
 
+/* ------------------------------------------------------------------------
+ * FP8 forward with incoherent processing ("Trois idées pour FA3",
+ * marketmaker.cc, point 3: naive FP8 attention suffers from outlier
+ * coordinates; rotating the query and key vectors at random before block
+ * quantisation spreads an outlier over all coordinates).  Two calls, so that
+ * the quantised operands can be produced once and reused:
+ *
+ *   fa_fp8_quantize  Q^ = Q D H / d and K^ = K D H, with H the d x d Sylvester
+ *                    Hadamard matrix (H_ab = (-1)^popcount(a & b)) and
+ *                    D = diag(signs); Q^ K^^T = Q K^T since H H^T = d I.  With
+ *                    signs = NULL there is no rotation (Q^ = Q, K^ = K).  V is
+ *                    not rotated.  Each block of 128 rows of one head of Q^, K^
+ *                    and V gets the smallest power-of-two scale sigma with
+ *                    max|x| / sigma <= 448 (1 for an all-zero block; 2^-126 at
+ *                    least), and its values become e4m3 codes of x / sigma
+ *                    (round to nearest even, saturating to +-448; the rotated
+ *                    values are formed in fp32).
+ *   fa_fwd_fp8       the forward on those codes: scores
+ *                    scale * sigma_q * sigma_k * (q8 . k8) accumulated in fp32
+ *                    on the tensor cores, the online softmax against the exact
+ *                    running max m, the weights P~ = exp(s - m) <= 1 quantised
+ *                    as e4m3(256 P~) for the P~ V product, the row sum l of the
+ *                    unquantised P~; O = sum sigma_v P~q V8 / (256 l) in the
+ *                    dtype of p, LSE = m + ln l (natural log, fp32).
+ *
+ * Buffers (device memory, owned by the caller, 16-byte aligned except the
+ * scales, which are 4-byte aligned):
+ *   q8, k8      uint8 [B*H][N][d]     e4m3 codes of Q^ and K^
+ *   vt8         uint8 [B*H][d][ld]    e4m3 codes of V transposed (row c holds
+ *                                     column c of V over the keys), ld =
+ *                                     fa_fp8_vt_cols(N); entries past N are 0
+ *   sq, sk, sv  float [B*H][ceil(N / 128)]  the block scales (powers of two)
+ *   signs       float [d]             +-1 (device memory), or NULL
+ * p: dtype FA_F16 or FA_BF16 (of Q, K, V and of O), d 64 or 128, causal and
+ * block masks as for fa_fwd; dropout and FA_F32 give FA_ERR_UNSUPPORTED.  Both
+ * calls are asynchronous on `stream`; validation errors return before any
+ * launch.  Codes made elsewhere (any e4m3 values with power-of-two scales in
+ * this layout) may be passed to fa_fwd_fp8.
+ * ------------------------------------------------------------------------ */
+int fa_fp8_vt_cols(int N);
+fa_status fa_fp8_quantize(const fa_params* p, const void* Q, const void* K, const void* V,
+                          const float* signs, void* q8, void* k8, void* vt8, float* sq, float* sk,
+                          float* sv, void* stream);
+fa_status fa_fwd_fp8(const fa_params* p, const void* q8, const void* k8, const void* vt8,
+                     const float* sq, const float* sk, const float* sv, void* O, float* LSE,
+                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif

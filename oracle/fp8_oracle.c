@@ -231,6 +231,17 @@ void orc_fp8_fwd(int BH, int N, int d, const uint8_t *q8, const uint8_t *k8, con
     const int Bc = 128;
     const int T = (N + block - 1) / block;
     const int Tm = mask ? (N + mask_block - 1) / mask_block : 0;
+    /* the operands' values, decoded once */
+    double *kd = (double *)malloc(sizeof(double) * (size_t)BH * N * d);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)BH * N * d); /* [bh][j][c] */
+#pragma omp parallel for schedule(static)
+    for (long long r = 0; r < (long long)BH * N; ++r) {
+        int bh = (int)(r / N), j = (int)(r % N);
+        for (int c = 0; c < d; ++c) {
+            kd[(size_t)r * d + c] = e4m3_value(k8[(size_t)r * d + c]);
+            vd[(size_t)r * d + c] = e4m3_value(vt8[((size_t)bh * d + c) * ld + j]);
+        }
+    }
 #pragma omp parallel
     {
         double *qd = (double *)malloc(sizeof(double) * d);
@@ -239,8 +250,7 @@ void orc_fp8_fwd(int BH, int N, int d, const uint8_t *q8, const uint8_t *k8, con
 #pragma omp for schedule(dynamic, 16)
         for (long long job = 0; job < (long long)BH * N; ++job) {
             int bh = (int)(job / N), i = (int)(job % N);
-            const uint8_t *k8h = k8 + (size_t)bh * N * d;
-            const uint8_t *vt8h = vt8 + (size_t)bh * d * ld;
+            const double *kh = kd + (size_t)bh * N * d, *vh = vd + (size_t)bh * N * d;
             for (int c = 0; c < d; ++c)
                 qd[c] = e4m3_value(q8[((size_t)bh * N + i) * d + c]);
             double m = -INFINITY, l = 0.0;
@@ -257,7 +267,7 @@ void orc_fp8_fwd(int BH, int N, int d, const uint8_t *q8, const uint8_t *k8, con
                     if (ok) {
                         double t = 0.0;
                         for (int c = 0; c < d; ++c)
-                            t += qd[c] * e4m3_value(k8h[(size_t)j * d + c]);
+                            t += qd[c] * kh[(size_t)j * d + c];
                         v = scale * sq[(size_t)bh * T + i / block] * sk[(size_t)bh * T + j / block] * t;
                     }
                     s[j - j0] = v;
@@ -279,7 +289,7 @@ void orc_fp8_fwd(int BH, int N, int d, const uint8_t *q8, const uint8_t *k8, con
                     double pq = e4m3_value(e4m3_code(256.0 * (double)(float)p)) / 256.0;
                     double w = pq * sv[(size_t)bh * T + j / block];
                     for (int c = 0; c < d; ++c)
-                        acc[c] += w * e4m3_value(vt8h[(size_t)c * ld + j]);
+                        acc[c] += w * vh[(size_t)j * d + c];
                 }
                 m = mn;
             }
@@ -292,4 +302,6 @@ void orc_fp8_fwd(int BH, int N, int d, const uint8_t *q8, const uint8_t *k8, con
         free(s);
         free(acc);
     }
+    free(kd);
+    free(vd);
 }

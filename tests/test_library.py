@@ -202,3 +202,28 @@ def test_params_mirror_the_header_layout(lib):
 def test_balanced_forward_with_dropout_is_the_plain_forward(lib):
     assert fa.balanced_workspace_bytes(_p(N=1024, dropout_p=0.1)) == 0
     assert fa.balanced_workspace_bytes(_p(N=1024)) > 0
+
+
+def test_fp8_calls_validate_before_any_launch(lib):
+    """The FP8 calls reject unsupported settings and bad pointers on the host."""
+    ok = 1 << 20  # never dereferenced
+    assert [lib.fa_fp8_vt_cols(n) for n in (0, 1, 16, 17, 2048, 23400)] == [0, 16, 16, 32, 2048, 23408]
+    q_args = [ok] * 3 + [None] + [ok] * 6 + [None]  # Q K V signs q8 k8 vt8 sq sk sv stream
+    f_args = [ok] * 8 + [None]                       # q8 k8 vt8 sq sk sv O LSE stream
+    for bad, code in (({"dtype": fa.FA_F32}, fa.FA_ERR_UNSUPPORTED), ({"d": 96}, fa.FA_ERR_UNSUPPORTED),
+                      ({"dropout_p": 0.1}, fa.FA_ERR_UNSUPPORTED), ({"N": 0}, fa.FA_ERR_INVALID)):
+        p = _p(**bad)
+        assert lib.fa_fp8_quantize(ctypes.byref(p), *q_args) == code
+        assert lib.fa_fwd_fp8(ctypes.byref(p), *f_args) == code
+    p = _p()
+    for i in range(3):  # q8, k8, vt8 null or misaligned
+        for v in (None, ok + 8):
+            a = list(f_args)
+            a[i] = v
+            assert lib.fa_fwd_fp8(ctypes.byref(p), *a) == fa.FA_ERR_INVALID
+    a = list(f_args)
+    a[3] = ok + 2  # a scale array off its 4-byte alignment
+    assert lib.fa_fwd_fp8(ctypes.byref(p), *a) == fa.FA_ERR_INVALID
+    a = list(q_args)
+    a[0] = None
+    assert lib.fa_fp8_quantize(ctypes.byref(p), *a) == fa.FA_ERR_INVALID
