@@ -31,7 +31,14 @@ workload (independent batches: weak scaling, no collective on the data path);
 the reported time is the max over ranks (max_over_ranks) and the value counts
 every rank's work (job_value), for the device-timed and the end-to-end numbers.
 
-Options beyond the contract's: --fwd-splits S (key-range slices of the forward;
+With --fp8 a step is the FP8 forward with incoherent processing instead: one
+fa_fp8_quantize of Q, K, V (randomised Hadamard rotation, power-of-two block
+scales, e4m3 codes) and one fa_fwd_fp8 per causal setting; the FLOPs are the
+forward's, the roofline kernel is fwd_fp8_kernel against the FP8 tensor peak
+(the measured bf16 peak times the nominal FP8/BF16 ratio 4.5/2.25 = 2), and the
+CPU baseline and the reference arm run the oracle's FP8 forward.
+
+Options beyond the contract's: --fp8, --fwd-splits S (key-range slices of the forward;
 0 lets the library choose), --no-graph (time separately launched kernels),
 --dropout P (dropout of the attention weights, off in the workloads; the FLOP
 count is unchanged), --no-cpu-baseline, --e2e-steps K.
@@ -71,6 +78,9 @@ def parse():
                     help="time separately launched kernels instead of one CUDA graph per step")
     ap.add_argument("--fwd-splits", type=int, default=0,
                     help="key-range slices of the forward (0: the library's choice for this GPU)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="measure the FP8 forward with incoherent processing (rotation + block "
+                         "quantisation + forward) instead of the 16-bit forward + backward")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout probability of the attention weights (0: none, the workloads' "
                          "own setting); the FLOP count is unchanged")
@@ -239,10 +249,14 @@ def run_reference(args, w, rank):
                 "d2h_bytes_per_step": 0}}), flush=True)
 
 
-def kernel_source_digest() -> str:
-    """Digest of the sources the backward main kernel is built from."""
+KERNEL_SOURCES = {"bwd_main": ("bwd_tc.cu", "ptx.cuh", "internal.h"),
+                  "fwd_fp8": ("fwd_fp8.cu", "fp8.h", "ptx.cuh", "internal.h")}
+
+
+def kernel_source_digest(kernel: str = "bwd_main") -> str:
+    """Digest of the sources a kernel is built from."""
     h = hashlib.sha256()
-    for f in ("bwd_tc.cu", "ptx.cuh", "internal.h"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "exact_io_aware_26_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -254,7 +268,7 @@ def measured_traffic(workload: str, kernel: str):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)[workload][kernel]
-        if t.get("source_digest") != kernel_source_digest():
+        if t.get("source_digest") != kernel_source_digest(kernel):
             return None
         return t["bytes_per_launch"]
     except Exception:
@@ -284,6 +298,247 @@ def job_value(units_per_rank: float, world: int, seconds: float) -> float:
     """Whole-job throughput: every rank processes units_per_rank (weak scaling, one
     replica of the workload per GPU) in at most `seconds` (the max over ranks)."""
     return units_per_rank * world / seconds
+
+
+FP8_METRIC = ("attention FP8 forward TFLOP/s (rotation + block quantisation + forward), "
+              "% of GB300 FP8 tensor peak")
+
+
+def read_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def oracle_fp8_sample(w, inp, heads: int, signs):
+    """The oracle's FP8 path (quantise + forward) on the first `heads` heads; returns
+    (forward flops, seconds, threads)."""
+    import oracle
+    sel = [(b, h) for b in range(w.B) for h in range(w.H)][:heads]
+    x = {n: inp[n].double().numpy() for n in ("q", "k", "v")}
+    flops = workload_flops(w, inp["mask"])
+    total = 0.0
+    t = time.perf_counter()
+    for (b, h) in sel:
+        sl = lambda n: x[n][b:b + 1, h:h + 1]
+        tq = oracle.fp8_quantize(sl("q"), sl("k"), sl("v"), signs)
+        mh = oracle.head_mask(inp["mask"], b, h, w.N, w.mask_block)
+        for c in w.causal:
+            oracle.fp8_attention_fwd(tq, w.scale, causal=c, mask=mh, mask_block=w.mask_block)
+            total += flops[c]["fwd"] / (w.B * w.H)
+    return total, time.perf_counter() - t, oracle.num_threads()
+
+
+def fp8_heads_for_seconds(w, target_s: float) -> int:
+    cores = os.cpu_count() or 8
+    per_head = sum(v["fwd"] for v in workload_flops(w, None).values()) / (w.B * w.H)
+    return max(1, min(int(target_s * cores * 2.0e9 / max(per_head, 1.0)), w.B * w.H))
+
+
+def fp8_config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+            "causal": list(w.causal), "block_mask_p": w.mask_p,
+            "passes": "fa_fp8_quantize once, then fa_fwd_fp8 per causal setting",
+            "rotation": "randomised Sylvester-Hadamard, signs PCG64(1)",
+            "quantisation": "e4m3, one power-of-two scale per 128-row block",
+            "l2": "flushed between steps (256 MiB write outside the timed events)"}
+
+
+def run_fp8(args, w, rank, world, local):
+    """The --fp8 measurement (see the module docstring)."""
+    import torch
+    import synth
+    signs_cpu = synth.rotation_signs(w.d, 1)
+    inp = synth.make_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, qkv_scale=w.qkv_scale,
+                            ar1_rho=w.ar1_rho, mask_p=w.mask_p, mask_block=w.mask_block,
+                            backward=False)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        heads = max(1, fp8_heads_for_seconds(w, min(1.5, 120.0 / max(1, args.steps + args.warmup))))
+        sg = signs_cpu.double().numpy()
+        for _ in range(args.warmup):
+            oracle_fp8_sample(w, inp, 1, sg)
+        tot_f = tot_s = 0.0
+        cores = 1
+        for _ in range(args.steps):
+            f, s_, cores = oracle_fp8_sample(w, inp, heads, sg)
+            tot_f += f
+            tot_s += s_
+        value = tot_f / tot_s / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": fp8_config(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"fp64 oracle FP8 quantise + forward of {heads} of "
+                                       f"{w.B * w.H} heads per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    import exact_io_aware_26_gb300 as fa
+    fa.load()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    signs = signs_cpu.to(dev)
+    mask = None if inp["mask"] is None else torch.as_tensor(inp["mask"]).to(dev)
+    flops = workload_flops(w, inp["mask"])
+    step_flops = sum(f["fwd"] for f in flops.values())
+    stream = torch.cuda.current_stream()
+    t8 = fa.fp8_quantize(q, k, v, signs, stream)
+    outs = {c: (torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device=dev))
+            for c in w.causal}
+
+    def quant(s):
+        fa.fp8_quantize(q, k, v, signs, s, out=t8)
+
+    def fwd8(c, s):
+        fa.attention_fwd_fp8_codes(t8, w.scale, causal=c, block_mask=mask, mask_block=w.mask_block,
+                                   dtype=q.dtype, out=outs[c][0], lse=outs[c][1], stream=s)
+
+    def step(s, evq=None, evf=None):
+        if evq is not None:
+            evq[0].record(s)
+        quant(s)
+        if evq is not None:
+            evq[1].record(s)
+        for i, c in enumerate(w.causal):
+            if evf is not None:
+                evf[i][0].record(s)
+            fwd8(c, s)
+            if evf is not None:
+                evf[i][1].record(s)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    W = max(args.warmup, 3)
+    for _ in range(W):
+        step(stream)
+    torch.cuda.synchronize()
+    if fa.get_status() != fa.FA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+    K = args.steps
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    ev_step = [(E(), E()) for _ in range(K)]
+    ev_q = [(E(), E()) for _ in range(K)]
+    ev_f = [[(E(), E()) for _ in w.causal] for _ in range(K)]
+    uuid = getattr(torch.cuda.get_device_properties(local), "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(0)
+    for i in range(K):  # per-kernel pass
+        flush.zero_()
+        step(stream, ev_q[i], ev_f[i])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    for i in range(K):  # timed pass: whole steps
+        flush.zero_()
+        ev_step[i][0].record(stream)
+        step(stream)
+        ev_step[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(1)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    if fa.get_status() != fa.FA_OK:
+        raise RuntimeError("device status not OK after the timed region")
+    total_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_step) / 1000.0, dist, dev)
+    q_s = sum(a.elapsed_time(b) for a, b in ev_q) / 1000.0
+    f_s = sum(a.elapsed_time(b) for row in ev_f for a, b in row) / 1000.0
+    value = job_value(step_flops * K, world, total_s) / 1e12
+    bf16_peak, peak_src = read_peaks()
+    peak = 2.0 * bf16_peak
+    hbm, hbm_src = read_hbm_peak()
+    fwd_tflops = step_flops * K / f_s / 1e12
+    elems = w.B * w.H * w.N * w.d
+    T = (w.N + 127) // 128
+    quant_bytes = 3 * elems * 2 + 3 * elems * 1 + 3 * w.B * w.H * T * 4  # read 16-bit, write e4m3 + scales
+    quant_gbs = quant_bytes * K / q_s / 1e9
+
+    # end to end: pinned host Q, K, V in, O and LSE out, every step
+    host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v")}
+    host_out = {c: (torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+                    torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()) for c in w.causal}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
+              for o, l in host_out.values())
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def e2e_steps(n):
+        for _ in range(n):
+            with torch.cuda.stream(s_in):
+                for nm, t in (("q", q), ("k", k), ("v", v)):
+                    t.copy_(host_in[nm], non_blocking=True)
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)  # the previous step's outputs have been copied out
+            step(stream)
+            s_out.wait_stream(stream)
+            s_in.wait_stream(stream)  # inputs are overwritten only after this step read them
+            with torch.cuda.stream(s_out):
+                for c in w.causal:
+                    host_out[c][0].copy_(outs[c][0], non_blocking=True)
+                    host_out[c][1].copy_(outs[c][1], non_blocking=True)
+
+    e2e_steps(2)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    e2e_steps(args.e2e_steps)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    e2e = {"value": job_value(step_flops * args.e2e_steps, world, e2e_s) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "timing": "host clock around all steps, synchronised on both sides",
+           "overlap": "input copies on one stream, output copies on another"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        heads = fp8_heads_for_seconds(w, 15.0)
+        f, s_, cores = oracle_fp8_sample(w, inp, heads, signs_cpu.double().numpy())
+        cpu = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"fp64 oracle FP8 quantise + forward of {heads} of {w.B * w.H} heads, "
+                         f"{s_:.1f} s"}
+    if rank == 0:
+        launches = K * len(w.causal)
+        print(json.dumps({
+            "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": 1000.0 * total_s / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 operands, fp32 accumulation; " + w.dtype + " in and out",
+            "data": "synthetic", "config": fp8_config(w),
+            "breakdown": {"fwd_fp8_tflops": fwd_tflops, "fwd_fp8_frac_of_fp8_peak": fwd_tflops / peak,
+                          "step_frac_of_fp8_peak": value / world / peak,
+                          "quantize_us": 1e6 * q_s / K, "quantize_gbs": quant_gbs,
+                          "quantize_frac_of_hbm": quant_gbs / hbm,
+                          "hbm_peak_gbs": hbm, "hbm_peak_source": hbm_src},
+            "roofline": {"kernel": "fwd_fp8_kernel", "bound": "tensor", "achieved": fwd_tflops,
+                         "peak": peak, "unit": "TFLOP/s", "frac": fwd_tflops / peak,
+                         "peak_source": ("measured bf16 burst x 2 (nominal FP8/BF16 ratio), "
+                                         "MEASURED_PEAKS.json" if peak_src == "measured"
+                                         else "fallback bf16 burst x 2"),
+                         "traffic": measured_traffic(w.name, "fwd_fp8"),
+                         "algorithmic_flops_per_launch": step_flops * K / launches},
+            "clocks": clk, "e2e": e2e,
+            "gpu_launches": K * (1 + len(w.causal)),
+            "cpu_baseline": cpu}), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 def run_e2e(fa, inp, runs, flops, steps, dev, stream, dist=None, world=1):
@@ -370,6 +625,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.fp8:
+        run_fp8(args, w, rank, world, local)
+        return
     if args.impl == "reference":
         run_reference(args, w, rank)
         return

@@ -191,10 +191,11 @@ def fp8_vt_cols(N: int) -> int:
     return int(load().fa_fp8_vt_cols(int(N)))
 
 
-def fp8_quantize(q, k, v, signs=None, stream=None) -> dict:
+def fp8_quantize(q, k, v, signs=None, stream=None, out=None) -> dict:
     """fa_fp8_quantize: rotation (``signs``: d floats of +-1 on the device, or None) and
     block quantisation of [B,H,N,d] Q, K, V.  Returns q8, k8 [B,H,N,d] and vt8
-    [B,H,d,fp8_vt_cols(N)] (uint8 e4m3 codes) and sq, sk, sv [B,H,ceil(N/128)] (fp32)."""
+    [B,H,d,fp8_vt_cols(N)] (uint8 e4m3 codes) and sq, sk, sv [B,H,ceil(N/128)] (fp32),
+    written into ``out`` (a dict of such tensors) when given."""
     import torch
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_tensor(t, n, q)
@@ -205,9 +206,17 @@ def fp8_quantize(q, k, v, signs=None, stream=None) -> dict:
     T = (N + 127) // 128
     u8 = dict(dtype=torch.uint8, device=q.device)
     f32 = dict(dtype=torch.float32, device=q.device)
-    t = {"q8": torch.empty((B, H, N, d), **u8), "k8": torch.empty((B, H, N, d), **u8),
-         "vt8": torch.empty((B, H, d, fp8_vt_cols(N)), **u8), "sq": torch.empty((B, H, T), **f32),
-         "sk": torch.empty((B, H, T), **f32), "sv": torch.empty((B, H, T), **f32)}
+    shapes = {"q8": (B, H, N, d), "k8": (B, H, N, d), "vt8": (B, H, d, fp8_vt_cols(N)),
+              "sq": (B, H, T), "sk": (B, H, T), "sv": (B, H, T)}
+    if out is None:
+        t = {n: torch.empty(shp, **(u8 if n.endswith("8") else f32)) for n, shp in shapes.items()}
+    else:
+        t = out
+        for n, shp in shapes.items():
+            want = torch.uint8 if n.endswith("8") else torch.float32
+            x = t[n]
+            if not (x.is_cuda and x.is_contiguous() and x.dtype == want and tuple(x.shape) == shp):
+                raise ValueError(f"out[{n!r}] must be a contiguous cuda {want} tensor of shape {shp}")
     p, _ = make_params(q)
     _check(load().fa_fp8_quantize(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(signs),
                                   _ptr(t["q8"]), _ptr(t["k8"]), _ptr(t["vt8"]), _ptr(t["sq"]),

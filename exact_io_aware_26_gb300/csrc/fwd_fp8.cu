@@ -127,7 +127,10 @@ __device__ __forceinline__ int next_kept(const MaskArgs& m, int b, int h, int qt
 // blockIdx.x = head * T + block, blockIdx.y = tensor (0 Q, 1 K, 2 V).  2d threads:
 // d / 8 lanes share a row, each holding 8 consecutive columns (one 16-byte load),
 // so a warp covers 256 / d rows per step and 8 steps cover its share of the
-// block's 128 rows.
+// block's 128 rows.  All eight loads of a thread are issued before any of them is
+// used.  V's codes go row-major into shared memory (8-byte stores), and each
+// 32-byte piece of a transposed row (32 keys of one column) is then gathered with
+// byte reads in which consecutive lanes take consecutive columns.
 template <int D, bool F16>
 __global__ void __launch_bounds__(2 * D) fp8_quant_kernel(const Fp8QuantArgs a) {
   constexpr int NT = 2 * D, NW = NT / 32;
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(2 * D) fp8_quant_kernel(const Fp8QuantArgs a) 
   constexpr int IT = RPW / RPI;    // steps
   static_assert(IT == 8, "eight steps of eight columns per thread");
   __shared__ float wmax[NW];
-  __shared__ __align__(16) uint8_t vt[D * kT];  // V block transposed: [column][row]
+  __shared__ __align__(16) uint8_t vrm[kT * D];  // V block codes, row-major [row][column]
 
   const int which = blockIdx.y;
   const int bh = blockIdx.x / a.T, t = blockIdx.x % a.T;
@@ -146,6 +149,14 @@ __global__ void __launch_bounds__(2 * D) fp8_quant_kernel(const Fp8QuantArgs a) 
   const uint16_t* src =
       static_cast<const uint16_t*>(which == 0 ? a.Q : which == 1 ? a.K : a.V) + (size_t)bh * a.N * D;
   const bool rotate = which < 2 && a.signs != nullptr;
+
+  uint4 raw[IT];
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const int r = t * kT + warp * RPW + it * RPI + rsub;
+    raw[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < a.N) raw[it] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)r * D + ch * 8));
+  }
   float sg[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) sg[e] = rotate ? a.signs[ch * 8 + e] : 1.f;
@@ -155,13 +166,10 @@ __global__ void __launch_bounds__(2 * D) fp8_quant_kernel(const Fp8QuantArgs a) 
   float amax = 0.f;
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
-    const int r = t * kT + warp * RPW + it * RPI + rsub;
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (r < a.N) raw = *reinterpret_cast<const uint4*>(src + (size_t)r * D + ch * 8);
     float v[8];
     {
-      const float2 p0 = unpack2<F16>(raw.x), p1 = unpack2<F16>(raw.y), p2 = unpack2<F16>(raw.z),
-                   p3 = unpack2<F16>(raw.w);
+      const float2 p0 = unpack2<F16>(raw[it].x), p1 = unpack2<F16>(raw[it].y),
+                   p2 = unpack2<F16>(raw[it].z), p3 = unpack2<F16>(raw[it].w);
       v[0] = p0.x, v[1] = p0.y, v[2] = p1.x, v[3] = p1.y, v[4] = p2.x, v[5] = p2.y, v[6] = p3.x, v[7] = p3.y;
     }
     if (rotate) {
@@ -222,21 +230,27 @@ __global__ void __launch_bounds__(2 * D) fp8_quant_kernel(const Fp8QuantArgs a) 
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
       const int rl = warp * RPW + it * RPI + rsub;  // row in the block (rows past N hold 0)
-      const uint32_t w0 = pack4_e4m3(x[it][0] * inv, x[it][1] * inv, x[it][2] * inv, x[it][3] * inv);
-      const uint32_t w1 = pack4_e4m3(x[it][4] * inv, x[it][5] * inv, x[it][6] * inv, x[it][7] * inv);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        vt[(ch * 8 + e) * kT + rl] = (uint8_t)(w0 >> (8 * e));
-        vt[(ch * 8 + 4 + e) * kT + rl] = (uint8_t)(w1 >> (8 * e));
-      }
+      uint2 w;
+      w.x = pack4_e4m3(x[it][0] * inv, x[it][1] * inv, x[it][2] * inv, x[it][3] * inv);
+      w.y = pack4_e4m3(x[it][4] * inv, x[it][5] * inv, x[it][6] * inv, x[it][7] * inv);
+      *reinterpret_cast<uint2*>(vrm + rl * D + ch * 8) = w;
     }
     __syncthreads();
+    // piece (c, k32): keys [32 k32, 32 k32 + 32) of column c; c runs fastest over the
+    // threads, so the byte reads of a warp hit consecutive bytes of one row
     uint8_t* dst = a.vt8 + (size_t)bh * D * a.ld;
-    for (int i = threadIdx.x; i < D * (kT / 16); i += NT) {
-      const int c = i / (kT / 16), k16 = i % (kT / 16);
-      const int col = t * kT + k16 * 16;
-      if (col < a.ld)
-        *reinterpret_cast<uint4*>(dst + (size_t)c * a.ld + col) = *reinterpret_cast<const uint4*>(vt + c * kT + k16 * 16);
+    for (int i = threadIdx.x; i < D * (kT / 32); i += NT) {
+      const int c = i % D, k32 = i / D;
+      const int col = t * kT + k32 * 32;
+      uint32_t wds[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint8_t* b = vrm + (k32 * 32 + q * 4) * D + c;
+        wds[q] = (uint32_t)b[0] | ((uint32_t)b[D] << 8) | ((uint32_t)b[2 * D] << 16) | ((uint32_t)b[3 * D] << 24);
+      }
+      uint8_t* out = dst + (size_t)c * a.ld + col;
+      if (col < a.ld) *reinterpret_cast<uint4*>(out) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+      if (col + 16 < a.ld) *reinterpret_cast<uint4*>(out + 16) = make_uint4(wds[4], wds[5], wds[6], wds[7]);
     }
   }
   if (threadIdx.x == 0) (which == 0 ? a.sq : which == 1 ? a.sk : a.sv)[(size_t)bh * a.T + t] = sigma;
