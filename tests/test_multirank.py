@@ -64,3 +64,23 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = argparse.Namespace(steps=1, warmup=0, gpus=2, dropout=0.0)
     assert bench.run_reference(args, synth.WORKLOADS["fp32_n256"], rank=1) is None
     assert capsys.readouterr().out == ""
+
+
+def test_fp8_reference_arm_line(capsys):
+    """bench.py --fp8 --impl reference: rank 0 times the oracle's FP8 path and prints one
+    line with the contract's keys; another rank prints nothing."""
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    import synth
+    w = synth.Workload("fp8_small", 1, 2, 256, 64, "bf16", 3, causal=(False, True))
+    args = argparse.Namespace(steps=1, warmup=0, gpus=1, impl="reference", fp8=True)
+    bench.run_fp8(args, w, rank=1, world=2, local=1)
+    assert capsys.readouterr().out == ""
+    bench.run_fp8(args, w, rank=0, world=1, local=0)
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "reference" and line["metric"] == bench.FP8_METRIC
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["config"]["causal"] == [False, True]
