@@ -227,3 +227,20 @@ def test_fp8_calls_validate_before_any_launch(lib):
     a = list(q_args)
     a[0] = None
     assert lib.fa_fp8_quantize(ctypes.byref(p), *a) == fa.FA_ERR_INVALID
+
+
+def test_fp8_binding_rejects_bad_tensors_before_the_library():
+    """The FP8 binding's checks run on the host: CPU tensors, wrong shapes or dtypes and
+    a malformed code dict raise before any library call."""
+    import torch
+    q = torch.zeros(1, 1, 130, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fp8_quantize(q, q, q)  # not cuda
+    T = 2
+    good = {"q8": torch.zeros(1, 1, 130, 64, dtype=torch.uint8),
+            "k8": torch.zeros(1, 1, 130, 64, dtype=torch.uint8),
+            "vt8": torch.zeros(1, 1, 64, 144, dtype=torch.uint8),
+            "sq": torch.ones(1, 1, T), "sk": torch.ones(1, 1, T), "sv": torch.ones(1, 1, T)}
+    with pytest.raises(ValueError):
+        fa.attention_fwd_fp8_codes(good, 0.125)  # not cuda
+    assert fa.fp8_vt_cols(130) == 144
