@@ -224,3 +224,22 @@ def test_rotation_lowers_fp8_error_on_outliers(outlier_p, gain):
     else:
         assert e_rot * gain < e_naive, (e_rot, e_naive)
     assert e_rot < 0.1 * float(np.sqrt(np.mean(O ** 2)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_with_one_scale_per_head_equals_exact_attention(causal):
+    """block >= N (one scale per head, the naive scaling): the same no-rounding
+    construction as above, with the scale arrays of one block per head."""
+    rng = np.random.default_rng(11 + causal)
+    B, H, N, d = 1, 2, 300, 64
+    t = _exact_codes(rng, B, H, N, d)
+    t["sq"] = np.ones((B, H, 1))
+    t["sk"] = np.ones((B, H, 1))
+    t["sv"] = 2.0 ** rng.integers(-6, 2, (B, H, 1)).astype(np.float64)
+    O8, L8 = oracle.fp8_attention_fwd(t, math.log(2.0), causal=causal, block=N)
+    q = oracle.e4m3_decode(t["q8"])
+    k = oracle.e4m3_decode(t["k8"])
+    v = np.swapaxes(oracle.e4m3_decode(t["vt8"][..., :N]), -1, -2) * t["sv"][..., None]
+    O, L = oracle.attention_fwd(q, k, v, math.log(2.0), causal=causal)
+    np.testing.assert_allclose(O8, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L8, L, rtol=0, atol=1e-12)
