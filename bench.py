@@ -520,7 +520,8 @@ def run_fp8(args, w, rank, world, local):
             "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": 1000.0 * total_s / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 operands, fp32 accumulation; " + w.dtype + " in and out",
+            "dtype": "e4m3",
+            "dtype_detail": f"e4m3 operands, fp32 accumulation; {w.dtype} in and out",
             "data": "synthetic", "config": fp8_config(w),
             "breakdown": {"fwd_fp8_tflops": fwd_tflops, "fwd_fp8_frac_of_fp8_peak": fwd_tflops / peak,
                           "step_frac_of_fp8_peak": value / world / peak,
