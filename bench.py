@@ -49,6 +49,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -61,19 +62,23 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("attention fwd/bwd TFLOP/s at N=2k–23.4k, d=64/128; "
           "% of GB300 BF16 tensor peak")
-DEFAULT_WORKLOAD = "bf16_b4h12_n2048"
+DEFAULT_WORKLOAD = "bf16_day_n23400"
 L2_FLUSH_BYTES = 256 << 20
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--min-timed-s", type=float, default=1.2,
+                    help="passes per step are chosen so that the timed region lasts at least this long")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per-kernel figures of the other workloads")
     ap.add_argument("--no-graph", action="store_true",
                     help="time separately launched kernels instead of one CUDA graph per step")
     ap.add_argument("--fwd-splits", type=int, default=0,
@@ -181,35 +186,62 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def oracle_sample(w, inp, heads: int, dropout: float = 0.0):
-    """fp64 oracle forward + backward on the first `heads` heads; returns (flops, s, threads)."""
+def prefix_flops(w, mask, n: int) -> float:
+    """FLOPs (fwd + bwd, every causal setting) of one head of the workload cut to its first
+    n tokens: the leading n x n block of the problem, itself a complete attention problem
+    of the same kind (causal rows see only earlier keys; a block mask keeps its leading
+    block)."""
+    sub = None
+    if mask is not None:
+        t = (n + w.mask_block - 1) // w.mask_block
+        sub = mask[:t, :t]
+    dense = 4.0 * n * n * w.d
+    return sum(3.5 * dense * kept_fraction(sub, c) for c in w.causal)
+
+
+def oracle_sample(w, inp, heads: int, n: int = 0, dropout: float = 0.0):
+    """fp64 oracle forward + backward of the first `heads` heads, each cut to its first n
+    tokens (0: the whole sequence); returns (flops, seconds, threads)."""
     import oracle
-    B, H = w.B, w.H
-    sel = [(b, h) for b in range(B) for h in range(H)][:heads]
-    x = {n: inp[n].double().numpy() for n in ("q", "k", "v", "do")}
-    flops = workload_flops(w, inp["mask"])
+    n = w.N if n <= 0 else min(n, w.N)
+    sel = [(b, h) for b in range(w.B) for h in range(w.H)][:heads]
+    x = {nm: inp[nm][:, :, :n].double().numpy() for nm in ("q", "k", "v", "do")}
     total = 0.0
     t = time.perf_counter()
     for (b, h) in sel:
-        sl = lambda n: x[n][b:b + 1, h:h + 1]
+        sl = lambda nm: x[nm][b:b + 1, h:h + 1]
         mh = oracle.head_mask(inp["mask"], b, h, w.N, w.mask_block)
+        if mh is not None:
+            tt = (n + w.mask_block - 1) // w.mask_block
+            mh = mh[:tt, :tt]
         for c in w.causal:
             oracle.attention_fwd(sl("q"), sl("k"), sl("v"), w.scale, causal=c, mask=mh,
                                  mask_block=w.mask_block, dropout_p=dropout, seed=1)
             oracle.attention_bwd(sl("q"), sl("k"), sl("v"), sl("do"), w.scale, causal=c, mask=mh,
                                  mask_block=w.mask_block, dropout_p=dropout, seed=1)
-            total += (flops[c]["fwd"] + flops[c]["bwd"]) / (B * H)
+        total += prefix_flops(w, inp["mask"], n)
     return total, time.perf_counter() - t, oracle.num_threads()
 
 
-def heads_for_seconds(w, target_s: float) -> int:
-    """Heads that keep the oracle near target_s (it runs at roughly 1 GFLOP/s per core
-    on this convention's FLOPs)."""
-    cores = os.cpu_count() or 8
-    f = workload_flops(w, None)
-    per_head = sum(v["fwd"] + v["bwd"] for v in f.values()) / (w.B * w.H)
-    n = int(target_s * cores * 1.0e9 / max(per_head, 1.0))
-    return max(1, min(n, w.B * w.H))
+def oracle_plan(w, inp, seconds: float, dropout: float = 0.0):
+    """A sample of the workload that keeps the oracle near `seconds`: (heads, n).  Whole
+    heads while one head fits, else one head cut to the longest prefix that fits (a
+    multiple of 128 tokens).  The rate comes from a short calibration run."""
+    n0 = min(w.N, 1024)
+    f, s, _ = oracle_sample(w, inp, 1, n0, dropout)
+    rate = f / max(s, 1e-6)
+    budget = seconds * rate
+    per_head = prefix_flops(w, inp["mask"], w.N)
+    if per_head <= budget:
+        return max(1, min(w.B * w.H, int(budget // per_head))), w.N
+    n = int((budget / per_head) ** 0.5 * w.N) // 128 * 128
+    return 1, max(128, min(n, w.N))
+
+
+def sample_text(w, heads: int, n: int) -> str:
+    cut = "the whole sequence" if n >= w.N else f"each cut to its first {n} of {w.N} tokens"
+    return (f"fp64 oracle forward + backward of {heads} of {w.B * w.H} heads, {cut} "
+            f"({w.name}, causal settings {list(w.causal)})")
 
 
 def config_of(w, fwd_splits=None, dropout=0.0):
@@ -225,18 +257,19 @@ def run_reference(args, w, rank):
     if rank != 0:
         return
     inp = synth.workload_inputs(w)
-    # the whole reference run stays within a few minutes whatever K is
-    heads = heads_for_seconds(w, min(1.5, 120.0 / max(1, args.steps + args.warmup)))
+    # each step one bounded sample, so that the whole run stays within a few minutes
+    # whatever K is
+    per_step = max(0.2, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
+    heads, n = oracle_plan(w, inp, per_step, args.dropout)
     for _ in range(args.warmup):
-        oracle_sample(w, inp, max(1, heads // 4), args.dropout)
+        oracle_sample(w, inp, heads, n, args.dropout)
     tot_f, tot_s, cores = 0.0, 0.0, 1
     for _ in range(args.steps):
-        f, s, cores = oracle_sample(w, inp, heads, args.dropout)
+        f, s, cores = oracle_sample(w, inp, heads, n, args.dropout)
         tot_f += f
         tot_s += s
     value = tot_f / tot_s / 1e12
-    sample = (f"fp64 oracle, forward + backward of {heads} of {w.B * w.H} heads per step "
-              f"({w.name}, causal settings {list(w.causal)})")
+    sample = sample_text(w, heads, n) + " per step"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -250,7 +283,9 @@ def run_reference(args, w, rank):
 
 
 KERNEL_SOURCES = {"bwd_main": ("bwd_tc.cu", "ptx.cuh", "internal.h"),
+                  "fwd": ("fwd_tc.cu", "ptx.cuh", "internal.h"),
                   "fwd_fp8": ("fwd_fp8.cu", "fp8.h", "ptx.cuh", "internal.h")}
+TRAFFIC_KEY = {"main": "bwd_main", "fwd": "fwd", "fwd_fp8": "fwd_fp8", "bwd_main": "bwd_main"}
 
 
 def kernel_source_digest(kernel: str = "bwd_main") -> str:
@@ -262,13 +297,17 @@ def kernel_source_digest(kernel: str = "bwd_main") -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str, kernel: str):
+def measured_traffic(workload: str, kind: str):
     """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) recorded in
-    profiles/traffic.json for this workload and this exact kernel source; None otherwise."""
+    profiles/traffic.json for this workload and this exact kernel source; None otherwise
+    (no capture, or the kernel has changed since)."""
+    key = TRAFFIC_KEY.get(kind)
+    if key is None:
+        return None
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            t = json.load(f)[workload][kernel]
-        if t.get("source_digest") != kernel_source_digest(kernel):
+            t = json.load(f)[workload][key]
+        if t.get("source_digest") != kernel_source_digest(key):
             return None
         return t["bytes_per_launch"]
     except Exception:
@@ -616,6 +655,154 @@ def run_e2e(fa, inp, runs, flops, steps, dev, stream, dist=None, world=1):
                        "compute and one copy-back stream per causal setting"}
 
 
+def make_runs(fa, lib, w, inp, dev, fwd_splits=0, dropout=0.0):
+    """Device tensors of a workload and one run (parameters, outputs, workspaces) per
+    causal setting; the library allocates nothing, so these are all the buffers."""
+    import torch
+    t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
+    mask = None if inp["mask"] is None else torch.as_tensor(inp["mask"]).to(dev)
+    q = t["q"]
+    runs = []
+    for c in w.causal:
+        p, keep = fa.make_params(q, w.scale, c, mask, w.mask_block, dropout, seed=1)
+        ws = torch.empty(int(lib.fa_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8,
+                         device=dev)
+        splits = fwd_splits if fwd_splits > 0 else fa.num_splits(p)
+        fws = None
+        if splits > 1:
+            fws = torch.empty(fa.split_workspace_bytes(p, splits), dtype=torch.uint8, device=dev)
+        runs.append(dict(causal=c, p=p, keep=keep, splits=splits, fws=fws, o=torch.empty_like(q),
+                         lse=torch.empty(q.shape[:3], dtype=torch.float32, device=dev),
+                         dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
+                         ws=ws))
+    return t, mask, runs
+
+
+def run_one(fa, t, r, s, ev=None):
+    """One causal setting of the path: forward, then the three backward stages.  With
+    `ev` (a dict of event pairs) each launch is bracketed by events."""
+    def mark(name, i):
+        if ev is not None:
+            ev[name][i].record(s)
+    mark("fwd", 0)
+    fwd(fa, r, t["q"], t["k"], t["v"], r["o"], r["lse"], s)
+    mark("fwd", 1)
+    mark("pre", 0)
+    fa.bwd_preprocess(r["p"], r["o"], t["do"], r["ws"], s)
+    mark("pre", 1)
+    mark("main", 0)
+    fa.bwd_main(r["p"], t["q"], t["k"], t["v"], t["do"], r["lse"], r["dk"], r["dv"], r["ws"], s)
+    mark("main", 1)
+    mark("fin", 0)
+    fa.bwd_finalize(r["p"], r["dq"], r["dk"], r["dv"], r["ws"], s)
+    mark("fin", 1)
+
+
+def launches_per_pass(runs) -> int:
+    return sum(4 + (r["splits"] > 1) for r in runs)
+
+
+def kernel_pass(fa, t, runs, stream, flush, iters: int):
+    """Launch the path `iters` times kernel by kernel, L2 flushed before each pass,
+    every launch between CUDA events; returns seconds per launch kind and causal
+    setting, summed over the iterations."""
+    import torch
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [[{k: (E(), E()) for k in ("fwd", "pre", "main", "fin")} for _ in runs]
+           for _ in range(iters)]
+    for i in range(iters):
+        flush.zero_()
+        for j, r in enumerate(runs):
+            run_one(fa, t, r, stream, evs[i][j])
+    torch.cuda.synchronize()
+    out = [{k: 0.0 for k in ("fwd", "pre", "main", "fin")} for _ in runs]
+    for i in range(iters):
+        for j in range(len(runs)):
+            for k, (a, b) in evs[i][j].items():
+                out[j][k] += a.elapsed_time(b) / 1000.0
+    return out
+
+
+KERNEL_NAMES = {"fwd": "fwd_tc_kernel", "main": "bwd_tc_kernel / bwd_persist_kernel",
+                "pre": "bwd_preprocess_kernel", "fin": "bwd_finalize_kernel"}
+
+
+def algorithmic_bytes(w, kind: str) -> float:
+    """HBM bytes a launch must move at least: forward reads Q, K, V and writes O and LSE;
+    backward main reads Q, K, V, dO, LSE, D and writes dK, dV (the fp32 dQ accumulator is
+    reduced in L2 and counted with the finalize stage)."""
+    e = 4 if w.dtype == "f32" else 2
+    nd, n = w.B * w.H * w.N * w.d, w.B * w.H * w.N
+    return {"fwd": 4.0 * nd * e + 4.0 * n,
+            "main": 6.0 * nd * e + 8.0 * n,
+            "pre": 2.0 * nd * e + 4.0 * n + 4.0 * nd,
+            "fin": 4.0 * nd + nd * e}[kind]
+
+
+def measure_workload(fa, lib, name, dev, stream, flush, peak, hbm_peak, iters=5, warm=3,
+                     fwd_splits=0, dropout=0.0):
+    """Per-kernel TFLOP/s, fraction of the bf16 peak, HBM GB/s (measured DRAM bytes from
+    profiles/traffic.json where captured for this kernel source, and algorithmic bytes)
+    and the memory check of one workload, its kernels launched one by one."""
+    import torch
+    import synth
+    w = synth.WORKLOADS[name]
+    inp = synth.workload_inputs(w)
+    t, mask, runs = make_runs(fa, lib, w, inp, dev, fwd_splits, dropout)
+    flops = workload_flops(w, inp["mask"])
+    for _ in range(warm):
+        for r in runs:
+            run_one(fa, t, r, stream)
+    torch.cuda.synchronize()
+    # memory: nothing may be allocated while the path runs (the library allocates no
+    # device memory; every buffer above is the caller's)
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    for r in runs:
+        run_one(fa, t, r, stream)
+    torch.cuda.synchronize()
+    extra = torch.cuda.max_memory_allocated(dev) - base
+    tensors = sum(x.numel() * x.element_size() for x in t.values())
+    tensors += sum(r[k].numel() * r[k].element_size() for r in runs
+                   for k in ("o", "lse", "dq", "dk", "dv", "ws"))
+    tensors += sum(r["fws"].numel() for r in runs if r["fws"] is not None)
+    n2 = 2.0 * w.B * w.H * w.N * w.N
+    if extra > (1 << 20):
+        raise RuntimeError(f"{name}: {extra} bytes allocated while the path ran")
+    sec = kernel_pass(fa, t, runs, stream, flush, iters)
+    if fa.get_status() != fa.FA_OK:
+        raise RuntimeError(f"{name}: device status not OK")
+    out = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+           "causal": list(w.causal), "block_mask_p": w.mask_p,
+           "fwd_splits": [r["splits"] for r in runs]}
+    for kind in ("fwd", "main", "pre", "fin"):
+        s = sum(x[kind] for x in sec) / iters  # per pass, all causal settings
+        launches = len(runs)
+        d = {"us_per_launch": 1e6 * s / launches}
+        if kind in ("fwd", "main"):
+            fl = sum(flops[r["causal"]]["fwd" if kind == "fwd" else "bwd"] for r in runs)
+            d["tflops"] = fl / s / 1e12
+            d["frac_of_bf16_peak"] = d["tflops"] / peak
+        alg = algorithmic_bytes(w, kind)
+        d["algorithmic_hbm_gbs"] = alg * launches / s / 1e9
+        tr = measured_traffic(name, kind)
+        if tr is not None:
+            d["dram_bytes_per_launch"] = tr
+            d["achieved_hbm_gbs"] = tr * launches / s / 1e9
+            d["hbm_frac"] = d["achieved_hbm_gbs"] / hbm_peak
+        out[kind] = d
+    steps_s = sum(sum(x.values()) for x in sec) / iters
+    out["step_tflops_launched"] = sum(f["fwd"] + f["bwd"] for f in flops.values()) / steps_s / 1e12
+    out["memory"] = {"buffers_bytes": tensors, "allocated_during_calls_bytes": extra,
+                     "unfused_fp16_scores_bytes": n2, "buffers_vs_scores": tensors / n2}
+    del t, runs
+    torch.cuda.empty_cache()
+    return out
+
+
+PER_WORKLOAD = ("bf16_b4h12_n2048", "fp16_n8192", "bf16_day_n23400", "bf16_sparse_n16384")
+
+
 def main():
     args = parse()
     import torch
@@ -643,59 +830,26 @@ def main():
 
     inp = synth.workload_inputs(w)
     dev = torch.device("cuda", local)
-    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
-    mask = None if inp["mask"] is None else torch.as_tensor(inp["mask"]).to(dev)
+    t, mask, runs = make_runs(fa, lib, w, inp, dev, args.fwd_splits, args.dropout)
     flops = workload_flops(w, inp["mask"])
     step_flops = sum(f["fwd"] + f["bwd"] for f in flops.values())
-
-    runs = []
-    for c in w.causal:
-        p, keep = fa.make_params(q, w.scale, c, mask, w.mask_block, args.dropout, seed=1)
-        ws = torch.empty(int(lib.fa_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8,
-                         device=dev)
-        splits = args.fwd_splits if args.fwd_splits > 0 else fa.num_splits(p)
-        fws = None
-        if splits > 1:
-            fws = torch.empty(fa.split_workspace_bytes(p, splits), dtype=torch.uint8, device=dev)
-        runs.append(dict(causal=c, p=p, keep=keep, splits=splits, fws=fws, o=torch.empty_like(q),
-                         lse=torch.empty(q.shape[:3], dtype=torch.float32, device=dev),
-                         dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
-                         ws=ws))
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def run_one(i, r, s, ev_main=None, ev_fwd=None):
-        if ev_fwd is not None:
-            ev_fwd[i][0].record(s)
-        fwd(fa, r, q, k, v, r["o"], r["lse"], s)
-        if ev_fwd is not None:
-            ev_fwd[i][1].record(s)
-        fa.bwd_preprocess(r["p"], r["o"], do, r["ws"], s)
-        if ev_main is not None:
-            ev_main[i][0].record(s)
-        fa.bwd_main(r["p"], q, k, v, do, r["lse"], r["dk"], r["dv"], r["ws"], s)
-        if ev_main is not None:
-            ev_main[i][1].record(s)
-        fa.bwd_finalize(r["p"], r["dq"], r["dk"], r["dv"], r["ws"], s)
-
-    def step(s, ev_main=None, ev_fwd=None):
-        for i, r in enumerate(runs):
-            run_one(i, r, s, ev_main, ev_fwd)
-
-    def step_branches(s):
+    def pass_branches(s):
         # the causal settings are independent (same inputs, separate outputs and
         # workspaces): one branch each, forked from and joined to `s`
         if len(runs) == 1:
-            run_one(0, runs[0], s)
+            run_one(fa, t, runs[0], s)
             return
         fork = torch.cuda.Event()
         fork.record(s)
         side_streams = [torch.cuda.Stream(dev) for _ in runs[1:]]
         for b in side_streams:
             b.wait_event(fork)
-        run_one(0, runs[0], s)
-        for i, (r, b) in enumerate(zip(runs[1:], side_streams), start=1):
-            run_one(i, r, b)
+        run_one(fa, t, runs[0], s)
+        for r, b in zip(runs[1:], side_streams):
+            run_one(fa, t, r, b)
         for b in side_streams:
             join = torch.cuda.Event()
             join.record(b)
@@ -703,14 +857,14 @@ def main():
 
     W = max(args.warmup, 3)
     for _ in range(W):
-        step(stream)
+        for r in runs:
+            run_one(fa, t, r, stream)
     torch.cuda.synchronize()
     if fa.get_status() != fa.FA_OK:
         raise RuntimeError("device status not OK after warm-up")
 
-    # The step as one CUDA graph (its kernels launched back to back, without
-    # the host in between); the per-kernel breakdown comes from a pass of
-    # separately launched, separately timed kernels.
+    # One pass of the path as one CUDA graph (its kernels launched back to back,
+    # without the host in between).
     graph = None
     if not args.no_graph:
         try:
@@ -718,7 +872,7 @@ def main():
             side = torch.cuda.Stream(dev)
             side.wait_stream(stream)
             with torch.cuda.graph(graph, stream=side):
-                step_branches(torch.cuda.current_stream())
+                pass_branches(torch.cuda.current_stream())
             stream.wait_stream(side)
             graph.replay()
             torch.cuda.synchronize()
@@ -728,12 +882,28 @@ def main():
             print(f"# CUDA graph capture failed ({e}); timing launched steps", file=sys.stderr)
             graph = None
 
-    K = args.steps
+    def one_pass(s):
+        if graph is not None:
+            graph.replay()
+        else:
+            for r in runs:
+                run_one(fa, t, r, s)
+
+    # Passes per step: a step of K is R passes over the same batch, R chosen so that the
+    # timed region lasts at least a second (so that the clock record covers a sustained
+    # load) -- from the time of one pass measured here.
     E = lambda: torch.cuda.Event(enable_timing=True)
-    ev_step = [(E(), E()) for _ in range(K)]
-    ev_kstep = [(E(), E()) for _ in range(K)]
-    ev_main = [[(E(), E()) for _ in runs] for _ in range(K)]
-    ev_fwd = [[(E(), E()) for _ in runs] for _ in range(K)]
+    e0, e1 = E(), E()
+    e0.record(stream)
+    for _ in range(3):
+        one_pass(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_pass = e0.elapsed_time(e1) / 3000.0
+    K = args.steps
+    R = max(1, int(math.ceil(args.min_timed_s / max(K * t_pass, 1e-9))))
+    R = int(max_over_ranks(R, dist, dev))
+
     uuid = getattr(torch.cuda.get_device_properties(local), "uuid", None)
     clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
     clocks.start()
@@ -741,25 +911,14 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    ev_step = [(E(), E()) for _ in range(K)]
     clocks.mark(0)
-    # per-kernel pass
-    for i in range(K):
-        flush.zero_()
-        ev_kstep[i][0].record(stream)
-        step(stream, ev_main[i], ev_fwd[i])
-        ev_kstep[i][1].record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    # timed pass: the whole step
     wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()
         ev_step[i][0].record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            step(stream)
+        for _ in range(R):
+            one_pass(stream)
         ev_step[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -770,57 +929,76 @@ def main():
     status = fa.get_status()
     if status != fa.FA_OK:
         raise RuntimeError(f"device status {status} after the timed region")
-
     total_s = sum(a.elapsed_time(b) for a, b in ev_step) / 1000.0
-    launched_s = sum(a.elapsed_time(b) for a, b in ev_kstep) / 1000.0
-    main_s = sum(a.elapsed_time(b) for row in ev_main for a, b in row) / 1000.0
-    fwd_s = sum(a.elapsed_time(b) for row in ev_fwd for a, b in row) / 1000.0
     total_s = max_over_ranks(total_s, dist, dev)
+    value = job_value(step_flops * R * K, world, total_s) / 1e12
 
+    # the dominant kernel, timed launch by launch over K passes
     peak, peak_src = read_peaks()
-    launches = K * len(runs)
+    hbm_peak, hbm_src = read_hbm_peak()
+    sec = kernel_pass(fa, t, runs, stream, flush, K)
+    main_s = sum(x["main"] for x in sec)
+    fwd_s = sum(x["fwd"] for x in sec)
+    launched_s = sum(sum(x.values()) for x in sec)
     bwd_flops = sum(flops[r["causal"]]["bwd"] for r in runs) * K
     fwd_flops = sum(flops[r["causal"]]["fwd"] for r in runs) * K
     achieved = bwd_flops / main_s / 1e12
     fwd_tflops = fwd_flops / fwd_s / 1e12
-    value = job_value(step_flops * K, world, total_s) / 1e12
+    launches = K * len(runs)
+    traffic = measured_traffic(w.name, "main")
+    hbm_main = None if traffic is None else traffic * launches / main_s / 1e9
 
     e2e = run_e2e(fa, inp, runs, flops, args.e2e_steps, dev, stream, dist, world)
 
+    per_workload = {}
+    if rank == 0 and not args.no_per_workload:
+        for name in PER_WORKLOAD:
+            per_workload[name] = measure_workload(fa, lib, name, dev, stream, flush, peak, hbm_peak,
+                                                  dropout=args.dropout)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        heads = heads_for_seconds(w, 15.0)
-        f, s, cores = oracle_sample(w, inp, heads, args.dropout)
+        heads, n = oracle_plan(w, inp, 15.0, args.dropout)
+        f, s, cores = oracle_sample(w, inp, heads, n, args.dropout)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"fp64 oracle forward + backward of {heads} of {w.B * w.H} heads "
-                         f"(causal settings {list(w.causal)}), {s:.1f} s"}
+               "sample": sample_text(w, heads, n) + f", {s:.1f} s"}
 
     if rank == 0:
+        l2 = (f"inputs larger than L2 (the pass's buffers: {sum(x.numel() * x.element_size() for x in t.values()) / 1e6:.0f} MB of inputs) "
+              "and flushed between steps (256 MiB write outside the timed events)")
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": 1000.0 * total_s / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": dict(config_of(w, [r["splits"] for r in runs], args.dropout),
-                           launch=("one CUDA graph per step, the causal settings as concurrent "
-                                   "branches" if len(runs) > 1 else "one CUDA graph per step")
+                           passes_per_step=R,
+                           passes=f"a step is {R} passes of fwd+bwd over the batch, back to back",
+                           l2=l2,
+                           launch=("one CUDA graph per pass, the causal settings as concurrent "
+                                   "branches" if len(runs) > 1 else "one CUDA graph per pass")
                            if graph is not None else "kernels launched one by one"),
             "breakdown": {
                 "fwd_tflops": fwd_tflops, "bwd_main_tflops": achieved,
                 "fwd_frac_of_bf16_peak": fwd_tflops / peak,
                 "bwd_main_frac_of_bf16_peak": achieved / peak,
                 "step_frac_of_bf16_peak": value / world / peak,
+                "bf16_peak_tflops": peak,
                 "wall_s_timed_region": wall,
-                "ms_per_step_launched_one_by_one": 1000.0 * launched_s / K},
-            "roofline": {"kernel": "bwd_tc_kernel (backward main)", "bound": "tensor",
+                "ms_per_pass_graph": 1000.0 * total_s / (K * R),
+                "ms_per_pass_launched_one_by_one": 1000.0 * launched_s / K,
+                "per_workload": per_workload},
+            "roofline": {"kernel": "backward main (bwd_tc_kernel)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "peak_source": ("measured bf16 burst, MEASURED_PEAKS.json"
                                          if peak_src == "measured" else "fallback bf16 burst"),
-                         "traffic": measured_traffic(w.name, "bwd_main"),
-                         "algorithmic_flops_per_launch": bwd_flops / launches},
+                         "traffic": traffic,
+                         "algorithmic_flops_per_launch": bwd_flops / launches,
+                         "achieved_hbm_gbs": hbm_main,
+                         "hbm_peak_gbs": hbm_peak, "hbm_peak_source": hbm_src},
             "clocks": clk, "e2e": e2e,
-            "gpu_launches": K * sum(4 + (r["splits"] > 1) for r in runs),
+            "gpu_launches": K * R * launches_per_pass(runs),
             "cpu_baseline": cpu}), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -9,8 +9,12 @@
 // fp32 scratch (D = rowsum(dO * O) and the dQ accumulator) from the array
 // below.  The array is part of the library image, so every GPU that loads the
 // library holds FA_NOALLOC_SCRATCH_BYTES of device memory for it until the
-// process exits.  Nothing in this file calls cudaMalloc, cudaFree or any other
-// allocating routine.
+// process exits.  With the runtime's default lazy module loading, the driver
+// commits that memory when this file's module is first used on a device, i.e. at
+// the first fa_bwd_noalloc call's address lookup (with eager loading, at context
+// creation): callers should make that first call during set-up.  Nothing in this
+// file calls cudaMalloc, cudaFree or any other allocating routine.  The cached
+// address is the primary context's; other driver contexts are not supported.
 #include <mutex>
 
 #include "internal.h"
@@ -69,7 +73,9 @@ extern "C" fa_status fa_bwd_noalloc(const fa_params* p, const void* Q, const voi
   void* scratch = nullptr;
   if ((s = scratch_address(&scratch)) != FA_OK) return s;
   // fa_bwd's first stage rewrites D and zeroes the dQ accumulator before the
-  // main kernel reads either, so the array's previous contents never matter
+  // main kernel reads either, and the main stage stores every partial-sum slot
+  // of a shared key tile in full before the finalize stage reads it (no slot is
+  // accumulated into), so the array's previous contents never matter
   return fa_bwd(p, Q, K, V, O, dO, LSE, dQ, dK, dV, scratch, (size_t)FA_NOALLOC_SCRATCH_BYTES,
                 stream);
 }

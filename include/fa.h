@@ -188,7 +188,11 @@ size_t fa_fwd_split_workspace_size(const fa_params* p, int num_splits);
  * FA_F32, 0 on invalid p.  Host-only when num_sms > 0. */
 int fa_fwd_num_splits(const fa_params* p, int num_sms);
 
-/* Bytes of device workspace fa_bwd needs, each part 256-byte aligned: fp32
+/* Bytes of device workspace fa_bwd needs, each part 256-byte aligned.  The
+ * backward of "Passe arrière : recalculer au lieu de stocker" (marketmaker.cc)
+ * keeps only O and the per-row statistic of the forward and recomputes the rest;
+ * what it needs besides is linear in N ("Análise de Complexidade", reading
+ * guide: O(N) extra memory): fp32
  * D = rowsum(dO * O) [B*H*N], the fp32 dQ accumulator [B*H*N*d] and, without a
  * block mask, the fp32 partial-sum slots of the persistent main kernel
  * (2 x 2 x 128 x d values for each of up to min(160, iterations) CTAs, where
@@ -197,7 +201,12 @@ int fa_fwd_num_splits(const fa_params* p, int num_sms);
 size_t fa_bwd_workspace_size(const fa_params* p);
 
 /*
- * Backward of the forward above for the loss whose gradient at O is dO:
+ * Backward of the forward above for the loss whose gradient at O is dO, as
+ * "Passe arrière : recalculer au lieu de stocker" (marketmaker.cc) and the
+ * recomputation bullet of "Ideias centrais" (reading guide) describe it: the
+ * score and probability tiles are recomputed block by block from Q, K and the
+ * saved LSE instead of being stored.  The formulas (the pages give none) are the
+ * derivative of the definition:
  *   P = exp(scale * S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
  *   dS = P * (dP - D), dQ = scale * dS K, dK = scale * dS^T Q.
  * Q, K, V, O, LSE must be those of the forward call (same params).  dQ, dK, dV
@@ -263,10 +272,18 @@ int fa_set_bwd_ctas(int n);
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any stream
- * capture.  Every call, on every stream, shares the one array: calls that can
- * overlap on the GPU race on it and must be serialised by the caller.  Each
- * call rewrites all the scratch it reads (D, and the dQ accumulator, which it
- * zeroes first), so nothing left by an earlier call affects its results.
+ * capture.  Under the CUDA runtime's default lazy module loading the driver
+ * commits the array's device memory at that first lookup (under eager loading,
+ * when the context is created), so that first call is where an out-of-memory
+ * error can appear: make it during set-up, not on the execution path.  The
+ * cached address is that of the runtime's primary context on each device;
+ * callers that run the library under another driver context are not served.
+ * Every call, on every stream, shares the one array: calls that can overlap on
+ * the GPU race on it and must be serialised by the caller.  Each call rewrites
+ * all the scratch it reads: D and the dQ accumulator (zeroed first) in the first
+ * stage, and the fp32 partial-sum slots of key tiles that several CTAs share,
+ * each stored in full by the main stage before the finalize stage reads it.  So
+ * nothing left by an earlier call affects a call's results.
  */
 fa_status fa_bwd_noalloc(const fa_params* p, const void* Q, const void* K, const void* V,
                          const void* O, const void* dO, const float* LSE, void* dQ, void* dK,
@@ -274,7 +291,11 @@ fa_status fa_bwd_noalloc(const fa_params* p, const void* Q, const void* K, const
 
 /* Synchronises `stream`, returns the device-side status recorded since the
  * previous call (FA_OK or FA_ERR_TIMEOUT) and clears it; FA_ERR_CUDA if the
- * synchronisation itself fails. */
+ * synchronisation itself fails.  The pages have no counterpart: it reports the
+ * library's own failure detection (every on-chip barrier wait of every kernel is
+ * bounded in time, so a kernel that cannot proceed gives up and records the
+ * error instead of hanging), which guards the custom low-level CUDA that
+ * "Limitações e questões em aberto" (reading guide) names as the method's cost. */
 fa_status fa_get_status(void* stream);
 
 /* Upper bound, in nanoseconds, on any single barrier wait inside the kernels

@@ -160,14 +160,18 @@ def test_bwd_workload_fp16_n8192_full_and_no_score_matrix(cuda_lib):
     check_grads((dq, dk, dv), _ref(inp), "f16")
 
 
-def _sampled(w, heads, nq, nk, seed):
+def _sampled(w, heads, nq, nk, seed, always=()):
+    """Gradients of whole workloads at full size against the oracle on sampled rows of
+    the listed heads: nq random query rows and nk random key rows, plus rows 0 and N - 1
+    and every row in `always` (as query and as key rows)."""
     inp = synth.workload_inputs(w)
     causal = w.causal[0]
     dq, dk, dv = _run(inp, causal, inp["mask"], w.mask_block)
     rng = np.random.default_rng(seed)
+    fixed = np.asarray([0, w.N - 1, *always], dtype=np.int64)
     for (b, h) in heads:
-        qr = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, nq)])).astype(np.int32)
-        kr = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, nk)])).astype(np.int32)
+        qr = np.unique(np.concatenate([fixed, rng.integers(0, w.N, nq)])).astype(np.int32)
+        kr = np.unique(np.concatenate([fixed, rng.integers(0, w.N, nk)])).astype(np.int32)
         o = oracle_inputs({n: inp[n][b, h] for n in ("q", "k", "v", "do")})
         mh = oracle.head_mask(inp["mask"], b, h, w.N, w.mask_block)
         rq, rk, rv = oracle.attention_bwd_rows(o["q"], o["k"], o["v"], o["do"], qr, kr, w.scale,
@@ -179,8 +183,14 @@ def _sampled(w, heads, nq, nk, seed):
 
 
 def test_bwd_workload_trading_day_n23400_sampled(cuda_lib):
-    _sampled(synth.WORKLOADS["bf16_day_n23400"], [(0, 5)], 256, 256, 44)
+    """First, a middle and the last head; every row of the last, partial 104-row tile
+    (rows 23296-23399) as query and as key rows."""
+    w = synth.WORKLOADS["bf16_day_n23400"]
+    _sampled(w, [(0, 0), (0, 5), (0, 11)], 256, 256, 44, always=range(23296, 23400))
 
 
 def test_bwd_workload_block_sparse_n16384_sampled(cuda_lib):
-    _sampled(synth.WORKLOADS["bf16_sparse_n16384"], [(1, 3)], 256, 256, 55)
+    """First, a middle and the last head (of 32); the first and last 128-row tiles in full."""
+    w = synth.WORKLOADS["bf16_sparse_n16384"]
+    _sampled(w, [(0, 0), (1, 3), (1, 15)], 256, 256, 55,
+             always=[*range(0, 128), *range(w.N - 128, w.N)])

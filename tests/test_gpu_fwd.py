@@ -141,14 +141,15 @@ def test_fwd_workload_fp16_n8192_full_and_no_score_matrix(cuda_lib):
     check_fwd(O, L, *_ref(inp), "f16")
 
 
-def _sampled_rows(w, heads, rows_per_head, seed):
+def _sampled_rows(w, heads, rows_per_head, seed, always=()):
     inp = synth.workload_inputs(w)
     causal = w.causal[0]
     O, L = _run(inp, causal, inp["mask"], w.mask_block)
     rng = np.random.default_rng(seed)
     for (b, h) in heads:
         rows = np.unique(np.concatenate([
-            [0, 1, w.N - 1, w.N - 2], rng.integers(0, w.N, rows_per_head)])).astype(np.int32)
+            [0, 1, w.N - 1, w.N - 2], np.asarray(list(always), dtype=np.int64),
+            rng.integers(0, w.N, rows_per_head)])).astype(np.int32)
         o = oracle_inputs({n: inp[n][b, h] for n in "qkv"})
         mh = oracle.head_mask(inp["mask"], b, h, w.N, w.mask_block)
         O_ref, L_ref = oracle.attention_fwd_rows(o["q"], o["k"], o["v"], rows, w.scale,
@@ -158,13 +159,14 @@ def _sampled_rows(w, heads, rows_per_head, seed):
 
 
 def test_fwd_workload_trading_day_n23400_sampled(cuda_lib):
+    """First, a middle and the last head; every row of the last, partial 104-row tile."""
     w = synth.WORKLOADS["bf16_day_n23400"]
-    _sampled_rows(w, [(0, 0), (0, 11)], 600, 4)
+    _sampled_rows(w, [(0, 0), (0, 5), (0, 11)], 600, 4, always=range(23296, 23400))
 
 
 def test_fwd_workload_block_sparse_n16384_sampled(cuda_lib):
     w = synth.WORKLOADS["bf16_sparse_n16384"]
-    _sampled_rows(w, [(0, 0), (1, 15)], 400, 5)
+    _sampled_rows(w, [(0, 0), (1, 3), (1, 15)], 400, 5, always=range(w.N - 128, w.N))
 
 
 # ------------------------------------------------------------------ failure detection
