@@ -29,6 +29,7 @@ FA_ERR_CUDA = -3
 FA_ERR_TIMEOUT = -4
 FA_ERR_WORKSPACE = -5
 FA_ERR_DEVICE = -6
+FA_ERR_BOUNDS = -7
 FA_F32, FA_F16, FA_BF16 = 0, 1, 2
 
 
@@ -53,9 +54,21 @@ class FaParams(ctypes.Structure):
 _lib = None
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile libfa.so (debug=True: libfa_debug.so, whose kernels check their indices
+    and report FA_ERR_BOUNDS through get_status()); returns the library's path."""
     from . import _builder as _b
-    return _b.build(force=force, verbose=verbose)
+    return _b.build(force=force, verbose=verbose, debug=debug)
+
+
+def use_library(path: str) -> str:
+    """Make the calls of this module go to the library at `path` (e.g. the debug
+    build) from the next call on; returns the path in use before."""
+    global LIB_PATH, _lib
+    old = LIB_PATH
+    LIB_PATH = path
+    _lib = None
+    return old
 
 
 def load() -> ctypes.CDLL:

@@ -281,6 +281,13 @@ __global__ void __launch_bounds__(320, 1)
     while (ok && live) {
       // this tile, and whether another follows (in this piece or the next)
       const int kt = sg.kt, bh = sg.bh, slot = sg.slot;
+      // debug build: the piece the schedule handed out lies inside the problem and
+      // its slot inside the workspace's slots (two per CTA)
+      if (!(ok = __all_sync(0xffffffffu, dbg_check(w, kt >= 0 && kt < n_tiles && bh >= 0 && bh < BH &&
+                                                        qt >= sg.q_first && qt < sg.q_end &&
+                                                        sg.q_end <= n_tiles && slot >= -1 &&
+                                                        slot < 2 * (a.G > 0 ? a.G : 1)))))
+        break;
       const int qn = next_q(a.m, bh / a.H, bh % a.H, qt + 1, kt, sg.q_end);
       const bool last = qn >= sg.q_end;
       const bool first = at_start;

@@ -1,4 +1,5 @@
-// bwd_sched.cuh -- how the backward main kernel splits its work over CTAs.
+// bwd_sched.cuh -- how the backward main kernel splits its work over CTAs, and
+// the head-group grid order of the one-CTA-per-tile launches of both passes.
 //
 // A unit is one key tile of one head; the units are numbered key-tile-major,
 // u = kt * (B*H) + bh, and each unit's iterations are its visited query tiles
@@ -86,6 +87,21 @@ __host__ __device__ inline void sched_locate(const Sched& s, long long g, int& b
   const int v = sched_visited(k, s.n, s.causal);
   bh = (int)(rem / v);
   j = (int)(rem - (long long)bh * v);
+}
+
+// Grid order of a one-CTA-per-tile launch (both passes): CTA t of a grid over
+// `tiles` tiles of each of BH heads, the heads taken in groups of `group` (the
+// last group may be smaller) and the tiles of a group tile-major, so that the
+// CTAs running at any moment share the streamed operands of one group of heads.
+// Returns the tile index ti (0 first: the caller maps it to its heaviest tile)
+// and the head bh.  group = BH is plain tile-major order over all heads.
+__host__ __device__ inline void group_order(int t, int tiles, int BH, int group, int& ti, int& bh) {
+  const int per_group = group * tiles;
+  const int g0 = (t / per_group) * group;  // first head of t's group
+  const int gh = BH - g0 < group ? BH - g0 : group;  // heads in that group
+  const int r = t - g0 * tiles;
+  ti = r / gh;
+  bh = g0 + r % gh;
 }
 
 // One piece of a CTA's range: key tile kt of head bh, query tiles [q_first, q_end).

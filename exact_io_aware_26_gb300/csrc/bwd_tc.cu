@@ -27,6 +27,7 @@
 // 4 NG + 1 owns TMEM and issues the MMAs.  More compute warps per SM
 // sub-partition hide more of the TMEM, shared-memory and barrier latencies of
 // the elementwise steps, which (with one CTA per SM) bound the loop.
+#include "bwd_sched.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -134,8 +135,11 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
   const int n_tiles = (a.N + kTile - 1) / kTile;
   // QS (a query-split launch, qsplit = 2): CTAs 2u and 2u + 1 share key tile u
   const int unit = QS ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int kt = unit / BH;  // causal: low key tiles see the most queries
-  const int bh = unit % BH;
+  // causal: low key tiles see the most queries, so they go first, within groups
+  // of head_group heads (a query-split launch keeps the unit numbering of its
+  // workspace slots: one group)
+  int kt, bh;
+  group_order(unit, n_tiles, BH, QS ? BH : a.head_group, kt, bh);
   const int b = bh / a.H, h = bh % a.H;
   // this CTA's query tiles: [qt_begin, q_end) (all of them without QS)
   const int q_half = (n_tiles + 1) / 2;
@@ -157,6 +161,10 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     if (threadIdx.x == 0) raise_error(w, FA_ERR_CUDA);
     return;
   }
+  // debug build: the CTA's key tile, head and query range lie inside the problem
+  if (!dbg_check(w, kt >= 0 && kt < n_tiles && bh >= 0 && bh < BH && qt_begin >= 0 &&
+                        q_end <= n_tiles && (int)blockIdx.x < a.direct))
+    return;
   // The producer lane sets up the barriers and, before the block-wide setup
   // barrier, already issues the copies that need no wait (K_j, V_j and the
   // first NS query tiles' Q, dO), so that their latency overlaps the TMEM
@@ -192,6 +200,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     }
     for (int qt = next_q(a.m, b, h, qt_begin, kt, q_end); qt < q_end && pre < NS;
          qt = next_q(a.m, b, h, qt + 1, kt, q_end), ++pre) {
+      if (!dbg_check(w, qt * kTile < a.N)) break;
       const uint32_t dst = sb + L::QS + (uint32_t)pre * 2u * L::TILE;
       mbar_arrive_expect_tx(bar_qf(pre), 2 * L::TILE);
       for (int c = 0; c < D / 64; ++c) {
@@ -220,6 +229,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
          qt = next_q(a.m, b, h, qt + 1, kt, q_end)) {
       const int s = it % NS;
       if (it >= NS && !warp_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
+      if (!__all_sync(0xffffffffu, dbg_check(w, qt >= 0 && qt * kTile < a.N))) break;
       if (lane == 0 && it >= pre) {
         const uint32_t dst = sb + L::QS + (uint32_t)s * 2u * L::TILE;
         mbar_arrive_expect_tx(bar_qf(s), 2 * L::TILE);
@@ -546,7 +556,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && dbg_check(w, g * L::DQG + c0 + L::DQC <= D && qt * kTile < a.N)) {
           tma_reduce_add_3d(&tmdQ, stg, g * L::DQG + c0, qt * kTile + (warp & 3) * 32, bh);
           bulk_commit_group();
         }
@@ -591,7 +601,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         }
       }
     } else if (ok) {
-      const bool store = key < a.N;
+      const bool store = key < a.N && dbg_check(w, (size_t)bh * a.N + key < (size_t)BH * a.N);
       constexpr int EC = L::DQG < 32 ? L::DQG : 32;  // columns per TMEM load
       uint16_t* dVrow = reinterpret_cast<uint16_t*>(a.dV) + ((size_t)bh * a.N + key) * D + g * L::DQG;
       uint16_t* dKrow = reinterpret_cast<uint16_t*>(a.dK) + ((size_t)bh * a.N + key) * D + g * L::DQG;

@@ -37,6 +37,7 @@
 // NS stages with separate K and V barriers); warp 5 TMEM owner and MMA
 // issuer.  Tiles hidden by the causal rule or the block mask are never
 // loaded ("Le masquage causal ...": "jamais chargée et jamais calculée").
+#include "bwd_sched.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -100,8 +101,11 @@ __global__ void __launch_bounds__(192, 2)
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const int split = (int)(blockIdx.x % a.n_splits);
   const int tile = (int)(blockIdx.x / a.n_splits);
-  const int qt = n_tiles - 1 - tile / BH;  // heaviest (causal) tiles first
-  const int bh = tile % BH;
+  // heads in groups of head_group; within a group the heaviest (causal) query
+  // tiles of all its heads first
+  int qt, bh;
+  group_order(tile, n_tiles, BH, a.head_group, qt, bh);
+  qt = n_tiles - 1 - qt;
   const int b = bh / a.H, h = bh % a.H;
   // this CTA's key tiles: [kt_begin, kt_end)
   const int kt_begin = split * a.split_tiles;
@@ -121,6 +125,10 @@ __global__ void __launch_bounds__(192, 2)
     if (threadIdx.x == 0) raise_error(w, FA_ERR_CUDA);
     return;
   }
+  // debug build: the CTA's tile, head and key range lie inside the problem
+  if (!dbg_check(w, qt >= 0 && qt < n_tiles && bh >= 0 && bh < BH && kt_begin >= 0 &&
+                        kt_end <= n_tiles && split < a.n_splits))
+    return;
   // The producer lane sets up the barriers and, before the block-wide setup
   // barrier, already issues the copies that need no wait (Q and the first NS
   // K, V tiles), so that their latency overlaps the TMEM allocation.
@@ -150,6 +158,7 @@ __global__ void __launch_bounds__(192, 2)
       tma_load_3d(sb + L::Q + c * (kTile * 128), &tmQ, bar_q, c * 64, qt * kTile, bh);
     kt_next = next_kept(a.m, b, h, qt, kt_begin, kt_end);
     for (; kt_next < kt_end && nk < NS; kt_next = next_kept(a.m, b, h, qt, kt_next + 1, kt_end)) {
+      if (!dbg_check(w, kt_next >= 0 && kt_next * kTile < a.N)) break;
       const int s = nk;
       mbar_arrive_expect_tx(bar_kf(s), L::TILE);
       for (int c = 0; c < D / 64; ++c)
@@ -177,6 +186,7 @@ __global__ void __launch_bounds__(192, 2)
     if (lane == 0) {
       // the rest of the K, V tiles, each into a stage once it is released
       for (int kt = kt_next; kt < kt_end; kt = next_kept(a.m, b, h, qt, kt + 1, kt_end)) {
+        if (!dbg_check(w, kt >= 0 && kt * kTile < a.N)) break;
         const int s = nk % NS;
         const uint32_t ph = ((nk / NS) - 1) & 1;
         if (nk >= NS && !mbar_wait(w, bar_ke(s), ph)) break;
@@ -333,37 +343,43 @@ __global__ void __launch_bounds__(192, 2)
       const float mneg = (m_use == -INFINITY) ? 0.f : -m_use;
       const uint64_t c2p = f2pack(c2, c2), mp = f2pack(mneg, mneg);
       uint64_t acc[4] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-      uint32_t plo[32], phi[32];  // P~ as 16-bit pairs: keys [0, 64) and [64, 128)
+      // The tile's exponentials in four chunks of 32 keys; each chunk's 16-bit P~
+      // goes to TMEM as soon as it is formed (16 columns), so the stores overlap
+      // the next chunk's arithmetic instead of waiting at the end.
 #pragma unroll
-      for (int c = 0; c < kTile; c += 2) {
-        float x0, x1;
-        f2unpack(ffma2(f2pack(s[c], s[c + 1]), c2p, mp), x0, x1);
-        float p0 = ex2(x0), p1 = ex2(x1);
-        acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], f2pack(p0, p1));  // four independent sums
-        if constexpr (DROP) {  // l sums the undropped weights; P~ V takes the dropped ones
-          p0 = ((kb[c >> 5] >> (c & 31)) & 1u) ? p0 * a.drop.z : 0.f;
-          p1 = ((kb[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? p1 * a.drop.z : 0.f;
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int pr = 0; pr < 16; ++pr) {
+          const int c = 32 * ch + 2 * pr;
+          float x0, x1, p0, p1;
+          f2unpack(ffma2(f2pack(s[c], s[c + 1]), c2p, mp), x0, x1);
+          p0 = ex2(x0);
+          p1 = ex2(x1);
+          acc[pr & 3] = fadd2(acc[pr & 3], f2pack(p0, p1));  // four independent sums
+          if constexpr (DROP) {  // l sums the undropped weights; P~ V takes the dropped ones
+            p0 = ((kb[c >> 5] >> (c & 31)) & 1u) ? p0 * a.drop.z : 0.f;
+            p1 = ((kb[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? p1 * a.drop.z : 0.f;
+          }
+          pk[pr] = pack2<F16>(p0, p1);
         }
-        if (c < 64)
-          plo[c / 2] = pack2<F16>(p0, p1);
-        else
-          phi[(c - 64) / 2] = pack2<F16>(p0, p1);
+        if (ch == 0 && L::PSEP && it > 0) {
+          // P~ V_{j-1} must be done: it reads the P~ columns and writes O (at
+          // d = 128, S_j complete implies it: MMAs complete in issue order)
+          if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
+          tc_fence_after();
+        }
+        // P~ (16-bit pairs); at d = 128 over the first 64 columns of S, all of
+        // which is already in registers
+        tmem_st16(tmem + L::T_P + lane_off + 16 * ch, pk);
       }
+      if (!ok) break;
       float sum0, sum1, sum2, sum3, sum4, sum5, sum6, sum7;
       f2unpack(acc[0], sum0, sum1);
       f2unpack(acc[1], sum2, sum3);
       f2unpack(acc[2], sum4, sum5);
       f2unpack(acc[3], sum6, sum7);
       l = l * alpha + (((sum0 + sum1) + (sum2 + sum3)) + ((sum4 + sum5) + (sum6 + sum7)));
-      if (L::PSEP && it > 0) {
-        // P~ V_{j-1} must be done: it reads the P~ columns and writes O
-        if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
-        tc_fence_after();
-      }
-      // P~ (16-bit pairs); at d = 128 over the first 64 columns of S, all of
-      // which is already in registers
-      tmem_st32(tmem + L::T_P + lane_off, plo);
-      tmem_st32(tmem + L::T_P + lane_off + 32, phi);
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const uint64_t ap = f2pack(alpha, alpha);
 #pragma unroll
@@ -397,6 +413,9 @@ __global__ void __launch_bounds__(192, 2)
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     const float lse = (l > 0.f) ? (m_use + __log2f(l)) * 0.693147180559945309f : -INFINITY;
+    // debug build: the row's outputs lie inside O and LSE (or the split partials)
+    if (row < a.N && ok)
+      ok = dbg_check(w, (size_t)(split + 1) * BH * a.N > (size_t)split * BH * a.N + (size_t)bh * a.N + row);
     if (a.n_splits == 1) {
       if (row < a.N && ok) a.LSE[(size_t)bh * a.N + row] = lse;
       uint16_t* Orow = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D;

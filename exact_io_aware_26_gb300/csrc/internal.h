@@ -18,6 +18,21 @@ struct DevStatus {
   unsigned int abort_epoch;
 };
 
+// Index checks of the debug build (FA_DEBUG): `ok` false records FA_ERR_BOUNDS
+// in the status word (the first error wins) and the caller skips the access;
+// nothing traps, so the context stays usable.  In the release build the checks
+// are constant true and compile away.
+#ifdef __CUDACC__
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool fa_bounds(DevStatus* st, bool ok) {
+  if (!ok) atomicCAS(&st->code, 0, (int)FA_ERR_BOUNDS);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool fa_bounds(DevStatus*, bool) { return true; }
+#endif
+#endif
+
 // Where a launch reports to and how long its waits may last.
 struct Report {
   DevStatus* st;
@@ -65,6 +80,11 @@ struct FwdArgs {
   // persistent forward: CTAs (the slots are 2 per CTA, each fp32 O [128][d]
   // then LSE [128])
   int G_fwd;
+  // grid order: the heads are taken in groups of head_group (the last group may
+  // be smaller); within a group the CTAs run query-tile-major, the heaviest
+  // causal tiles of the group's heads first.  head_group = B*H is one group; a
+  // smaller group keeps the K, V that the running CTAs stream within L2
+  int head_group;
   DropArgs drop;
   Report rep;
 };
@@ -95,6 +115,12 @@ struct BwdArgs {
   // writing fp32 [dV | dK] partial sums (dK unscaled) to slot 2u + s; the
   // finalize kernel adds them up.  1: one CTA per key tile.
   int qsplit;
+  // grid order of a launch whose every unit is its own CTA (qsplit = 1, G = 0):
+  // the heads in groups of head_group, key-tile-major within a group (the
+  // heaviest causal key tiles of the group's heads first); B*H is one group.  A
+  // smaller group keeps the Q, dO and dQ accumulator the running CTAs stream
+  // within L2.  Other launches use the key-tile-major unit numbering.
+  int head_group;
   DropArgs drop;
   Report rep;
 };

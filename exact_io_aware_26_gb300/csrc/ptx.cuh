@@ -69,6 +69,21 @@ __device__ __forceinline__ void raise_error(const WaitCtx& w, int code) {
   atomicMax(&w.st->abort_epoch, w.epoch);
 }
 
+// Index check of the debug build (FA_DEBUG): a failed check aborts the launch
+// the way a timed-out wait does, with FA_ERR_BOUNDS in the status word (the first
+// error wins), and the caller skips the access; nothing traps.  The release build
+// compiles it to `true`.
+__device__ __forceinline__ bool dbg_check(const WaitCtx& w, bool ok) {
+#ifdef FA_DEBUG
+  if (!ok) raise_error(w, FA_ERR_BOUNDS);
+  return ok;
+#else
+  (void)w;
+  (void)ok;
+  return true;
+#endif
+}
+
 // Wait until the phase with the given parity has completed.  Gives up (returns
 // false) when the time limit passes -- recording FA_ERR_TIMEOUT -- or when
 // another thread of this CTA or another CTA of this launch has given up.

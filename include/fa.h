@@ -26,6 +26,11 @@
  *     waiting on an on-chip barrier records FA_ERR_TIMEOUT in the status word,
  *     which fa_get_status() returns.
  *   - Only the current CUDA device is used; it must be compute capability 10.3.
+ *   - A debug build of the library (compiled with FA_DEBUG defined: libfa_debug.so)
+ *     checks, in the kernels, every global-memory index it stores to and every
+ *     tile coordinate it copies from against the tensor's bounds; a failed check
+ *     skips the access and records FA_ERR_BOUNDS in the status word (no trap, so
+ *     the context stays usable).  The release build compiles the checks away.
  */
 #ifndef FA_H
 #define FA_H
@@ -44,7 +49,8 @@ typedef enum {
   FA_ERR_CUDA = -3,        /* a CUDA runtime or driver call failed */
   FA_ERR_TIMEOUT = -4,     /* a kernel gave up waiting on a barrier (via fa_get_status) */
   FA_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required */
-  FA_ERR_DEVICE = -6       /* the current device is not compute capability 10.3 */
+  FA_ERR_DEVICE = -6,      /* the current device is not compute capability 10.3 */
+  FA_ERR_BOUNDS = -7       /* debug build only: a kernel's index check failed (via fa_get_status) */
 } fa_status;
 
 typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;

@@ -1,6 +1,7 @@
 """Host-only check of how the backward main kernel splits its iterations over
-persistent CTAs (csrc/bwd_sched.cuh), by brute force over many shapes: built
-from the same header with the host compiler and run on the CPU."""
+persistent CTAs (csrc/bwd_sched.cuh), and of the head-group grid order of the
+one-CTA-per-tile launches, by brute force over many shapes: built from the same
+header with the host compiler and run on the CPU."""
 import os
 import subprocess
 
@@ -34,5 +35,19 @@ CASES = [
 @pytest.mark.parametrize("n,BH,causal,G,u0", CASES)
 def test_schedule_covers_every_iteration_once(checker, n, BH, causal, G, u0):
     r = subprocess.run([checker, str(n), str(BH), str(causal), str(G), str(u0)], capture_output=True,
+                       text=True)
+    assert r.returncode == 0, r.stderr + r.stdout
+
+
+GROUP_CASES = [
+    # tiles, BH, group
+    (183, 12, 12), (183, 12, 7), (183, 12, 1), (128, 32, 11), (128, 32, 5), (16, 48, 48),
+    (1, 1, 1), (3, 5, 2), (7, 9, 4), (2, 3, 3), (5, 7, 6), (4, 4, 1),
+]
+
+
+@pytest.mark.parametrize("tiles,BH,group", GROUP_CASES)
+def test_group_order_visits_every_tile_once_group_by_group(checker, tiles, BH, group):
+    r = subprocess.run([checker, "group", str(tiles), str(BH), str(group)], capture_output=True,
                        text=True)
     assert r.returncode == 0, r.stderr + r.stdout
