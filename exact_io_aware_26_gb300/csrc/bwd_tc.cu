@@ -19,12 +19,13 @@
 // The score scale is applied once at the end: dK = scale * sum dS^T Q here,
 // dQ = scale * accumulator in the finalize kernel.
 //
-// Warp roles (32 (4 NG + 2) threads): warps 0 .. 4 NG - 1 form NG compute
+// Warp roles (32 (4 NG + 2 + NQW) threads): warps 0 .. 4 NG - 1 form NG compute
 // warpgroups that split the 128 query columns of every tile into NG groups of
 // 128 / NG (TMEM lane = key row; warp w reads the lanes of quadrant w mod 4);
 // warp 4 NG is the producer (TMA copies of K_j, V_j once and of Q_i, dO_i
 // through a ring, plus each query tile's LSE and D staged by its lanes); warp
-// 4 NG + 1 owns TMEM and issues the MMAs.  More compute warps per SM
+// 4 NG + 1 owns TMEM and issues the MMAs; at d = 64, warps 4 NG + 2 .. 4 NG + 5
+// read dQ_i out of TMEM and reduce it into the fp32 accumulator.  More compute warps per SM
 // sub-partition hide more of the TMEM, shared-memory and barrier latencies of
 // the elementwise steps, which (with one CTA per SM) bound the loop.
 #include "bwd_sched.cuh"
@@ -42,13 +43,21 @@ struct BwdLayout {
   static constexpr int CW = kTile / NG;   // query columns per compute warpgroup
   static constexpr int KPG = CW / 16;     // MMA K steps (16 queries) per warpgroup
   static constexpr int NCW = 4 * NG;      // compute warps
-  static constexpr int NT = 32 * (NCW + 2);
-  // dQ read-out: each compute warp stages boxes of 32 query rows x DQC fp32
-  // columns (128-byte rows with the 128-byte swizzle when DQC = 32, 64-byte
-  // rows with the 64-byte swizzle when DQC = 16) for the TMA reduce-add
+  // d = 64: four dQ warps of their own (one per TMEM quadrant) read dQ_i out of
+  // TMEM, stage it and issue its reduce-add, off the compute warps' critical
+  // path; at d = 128 the compute warps do it (the staging shares dS^T there)
+  static constexpr bool QW = (D == 64);
+  static constexpr int NQW = QW ? 4 : 0;
+  static constexpr int NT = 32 * (NCW + 2 + NQW);
+  // dQ read-out: boxes of 32 query rows x DQC fp32 columns (128-byte rows with
+  // the 128-byte swizzle when DQC = 32, 64-byte rows with the 64-byte swizzle
+  // when DQC = 16) for the TMA reduce-add; with dQ warps each stages all D
+  // columns of its 32 rows (D / DQC boxes), else each compute warp its group's
+  // DQG columns
   static constexpr int DQG = D / NG;      // dQ columns per warpgroup
-  static constexpr int DQC = (NG == 2) ? 32 : 16;
+  static constexpr int DQC = (QW || NG == 2) ? 32 : 16;
   static constexpr uint32_t BOXB = 32u * DQC * 4u;
+  static constexpr int DQ_READERS = QW ? NQW : NCW;  // arrivals on dq_free
   static constexpr uint32_t TILE = kTile * D * 2;
   static constexpr int NS = (D == 64) ? 3 : 2;         // Q/dO ring depth
   static constexpr uint32_t K = 0;
@@ -62,7 +71,7 @@ struct BwdLayout {
   // staging
   static constexpr bool STG_SEP = (D == 64);
   static constexpr uint32_t STG = STG_SEP ? STAT + NS * 256 * 4 : DST;
-  static_assert(NCW * BOXB == 2 * kTile * 128, "staging size");
+  static_assert((QW ? NQW * (D / DQC) : NCW) * BOXB == 2 * kTile * 128, "staging size");
   static constexpr uint32_t BAR = STAT + NS * 256 * 4 + (STG_SEP ? 2 * kTile * 128 : 0);
   // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
   //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS],
@@ -180,7 +189,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     mbar_init(bar_ds_full, L::NCW);
     mbar_init(bar_ds_free, 1);
     mbar_init(bar_dq_full, 1);
-    mbar_init(bar_dq_free, L::NCW);
+    mbar_init(bar_dq_free, L::DQ_READERS);
     mbar_init(bar_done, 1);
     mbar_init(bar_pt_free, 1);
     for (int s = 0; s < NS; ++s) {
@@ -386,11 +395,64 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       if (lane == 0) mbar_drain(w, bar_done, 0);
       __syncwarp();
     }
+  } else if (warp > kMma) {
+    if constexpr (L::QW) {
+      // ------------------------------------------------------------ dQ warps
+      // Warp of TMEM quadrant qd: query rows 32 qd .. 32 qd + 31 of each tile's
+      // dQ_i = dS K_j (TMEM lane = query row), all D columns, read out as soon as
+      // the MMA completes, staged in its own 128-byte-swizzled boxes of 32 rows x
+      // 32 fp32 columns and added into the fp32 accumulator by TMA reduce-adds (L2
+      // performs the adds).  A box is rewritten only after the previous tile's
+      // reduces have finished reading it.
+      const int qd = warp & 3;
+      const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+      const uint32_t stg = sb + L::STG + (uint32_t)qd * (D / L::DQC) * L::BOXB;
+      bool pend = false;
+      bool ok = true;
+      int it = 0;
+      for (int qt = next_q(a.m, b, h, qt_begin, kt, q_end); qt < q_end;
+           qt = next_q(a.m, b, h, qt + 1, kt, q_end), ++it) {
+        if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
+        tc_fence_after();
+        if (pend) {
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+        }
+        // one box (DQC columns) at a time: out of TMEM, then into shared memory
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += L::DQC) {
+          uint32_t dq[L::DQC];
+          tmem_ld_n<L::DQC>(tmem + L::T_DQ + lane_off + (uint32_t)c0, dq);
+          if (c0 + L::DQC == D) {  // all of dQ_i is in registers: the next dQ may be computed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_dq_free);
+          }
+          // row `lane` of the box: 16-byte chunk x at x ^ (row mod 8) (the map's
+          // 128-byte swizzle)
+          const uint32_t box = stg + (uint32_t)(c0 / L::DQC) * L::BOXB;
+#pragma unroll
+          for (int x = 0; x < L::DQC / 4; ++x)
+            st_shared_v4(box + (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16), dq[4 * x],
+                         dq[4 * x + 1], dq[4 * x + 2], dq[4 * x + 3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && dbg_check(w, qt * kTile < a.N)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += L::DQC)
+            tma_reduce_add_3d(&tmdQ, stg + (uint32_t)(c0 / L::DQC) * L::BOXB, c0, qt * kTile + qd * 32, bh);
+          bulk_commit_group();
+        }
+        pend = true;
+      }
+      if (lane == 0) bulk_wait_group0();  // this warp's dQ reductions fully done
+    }
   } else {
     // ------------------------------------------------------------ compute warpgroups
-    // Software-pipelined per query tile i:  dS_i | P_{i+1} | dQ_i, so that the
-    // exponentials of the next tile run while the tensor core computes dK_i,
-    // dQ_i and dP^T_{i+1}.
+    // Software-pipelined per query tile i:  dS_i | P_{i+1} | dQ_i (dQ_i only
+    // without dQ warps), so that the exponentials of the next tile run while the
+    // tensor core computes dK_i, dQ_i and dP^T_{i+1}.
     constexpr int CW = L::CW;
     const int g = warp >> 2;                 // query columns [CW g, CW g + CW)
     const int r = (warp & 3) * 32 + lane;    // key row in the tile = TMEM lane
@@ -493,30 +555,37 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
       tc_fence_after();
       uint32_t pk[CW / 2];
-      {
-        uint32_t u[CW];
-        tmem_ld_n<CW>(tmem + L::T_DP + lane_off + CW * g, u);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_dp_free);
+      // in two halves of CW / 2 columns, so that only half of dP^T is held in
+      // registers at a time; the MMA may overwrite dP^T once both are loaded
+      const float4* nd4 = reinterpret_cast<const float4*>(stat(it) + 128 + CW * g);  // -D
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        constexpr int HW = CW / 2;
+        uint32_t u[HW];
+        tmem_ld_n<HW>(tmem + L::T_DP + lane_off + CW * g + HW * hf, u);
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dp_free);
+        }
         if constexpr (DROP) {
 #pragma unroll
-          for (int c = 0; c < CW; ++c)
-            u[c] = __float_as_uint(keep(c) ? __uint_as_float(u[c]) * a.drop.z : 0.f);
+          for (int c = 0; c < HW; ++c)
+            u[c] = __float_as_uint(keep(HW * hf + c) ? __uint_as_float(u[c]) * a.drop.z : 0.f);
         }
-        const float4* nd4 = reinterpret_cast<const float4*>(stat(it) + 128 + CW * g);  // -D
 #pragma unroll
-        for (int c = 0; c < CW; c += 4) {
-          const float4 nd = nd4[c / 4];
+        for (int c = 0; c < HW; c += 4) {
+          const int cc = HW * hf + c;  // column within the warp's CW
+          const float4 nd = nd4[cc / 4];
           float y0, y1, y2, y3;
-          f2unpack(fmul2(f2pack(p[c], p[c + 1]),
+          f2unpack(fmul2(f2pack(p[cc], p[cc + 1]),
                          fadd2(f2pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), f2pack(nd.x, nd.y))),
                    y0, y1);
-          f2unpack(fmul2(f2pack(p[c + 2], p[c + 3]),
+          f2unpack(fmul2(f2pack(p[cc + 2], p[cc + 3]),
                          fadd2(f2pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), f2pack(nd.z, nd.w))),
                    y2, y3);
-          pk[c / 2] = pack2<F16>(y0, y1);
-          pk[c / 2 + 1] = pack2<F16>(y2, y3);
+          pk[cc / 2] = pack2<F16>(y0, y1);
+          pk[cc / 2 + 1] = pack2<F16>(y2, y3);
         }
       }
       if (it > 0 && !(ok = warp_wait(w, bar_ds_free, (it - 1) & 1))) break;
@@ -535,6 +604,11 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       if (qn < q_end && !(ok = p_phase(it + 1, qn))) break;
 
       // ---- dQ_i (TMEM lane = query row) -> fp32 accumulator by TMA reduce-add
+      // (the dQ warps' job when there are dQ warps)
+      if constexpr (L::QW) {
+        qt = qn;
+        continue;
+      }
       if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
       tc_fence_after();
       uint32_t dq[L::DQG];
