@@ -88,9 +88,6 @@ def load() -> ctypes.CDLL:
         "fa_fwd_split": (I, [PP, P, P, P, P, P, I, P, S, P]),
         "fa_fwd_split_workspace_size": (S, [PP, I]),
         "fa_fwd_num_splits": (I, [PP, I]),
-        "fa_fwd_balanced": (I, [PP, P, P, P, P, P, P, S, P]),
-        "fa_fwd_balanced_workspace_size": (S, [PP]),
-        "fa_set_fwd_ctas": (I, [I]),
         "fa_bwd_workspace_size": (S, [PP]),
         "fa_bwd": (I, [PP, P, P, P, P, P, P, P, P, P, P, S, P]),
         "fa_bwd_preprocess": (I, [PP, P, P, P, S, P]),
@@ -309,41 +306,6 @@ def attention_fwd_split(q, k, v, scale=None, causal=False, block_mask=None, mask
                             0 if workspace is None else workspace.numel(), _stream(stream)),
            "fa_fwd_split")
     return out, lse
-
-
-def balanced_workspace_bytes(p: FaParams) -> int:
-    return int(load().fa_fwd_balanced_workspace_size(ctypes.byref(p)))
-
-
-def set_fwd_ctas(n: int) -> int:
-    """fa_set_fwd_ctas: cap on the balanced forward's CTAs (0 = two per SM)."""
-    return int(load().fa_set_fwd_ctas(int(n)))
-
-
-def attention_fwd_balanced(q, k, v, scale=None, causal=False, block_mask=None, mask_block=128,
-                           out=None, lse=None, workspace=None, stream=None, dropout_p=0.0,
-                           seed=0, offset=0):
-    """O, LSE = fa_fwd_balanced(Q, K, V): persistent CTAs with equal shares."""
-    import torch
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _check_tensor(t, n, q)
-    p, keep = make_params(q, scale, causal, block_mask, mask_block, dropout_p, seed, offset)
-    lib = load()
-    nbytes = int(lib.fa_fwd_balanced_workspace_size(ctypes.byref(p)))
-    if workspace is None and nbytes > 0:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    fwd_balanced_raw(p, q, k, v, out, lse, workspace, stream)
-    return out, lse
-
-
-def fwd_balanced_raw(p: FaParams, q, k, v, o, lse, workspace, stream=None):
-    _check(load().fa_fwd_balanced(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                  _ptr(workspace), 0 if workspace is None else workspace.numel(),
-                                  _stream(stream)), "fa_fwd_balanced")
 
 
 def fwd_split_raw(p: FaParams, q, k, v, o, lse, splits, workspace, stream=None):

@@ -56,8 +56,6 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 std::atomic<uint32_t> g_epoch{0};
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 std::atomic<int> g_bwd_ctas{0};  // cap on persistent backward CTAs; 0 = one per SM
-std::atomic<int> g_fwd_ctas{0};  // cap on persistent forward CTAs; 0 = two per SM
-constexpr int kFwdMaxCtas = 320;
 
 constexpr int kMaxDev = 64;
 struct DevState {
@@ -721,77 +719,6 @@ fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const v
   if (e != cudaSuccess) return cuda_fail(e, "split forward launch");
   e = launch_fwd_merge(a, p->d, p->dtype == FA_F16, s);
   if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
-  return FA_OK;
-}
-
-namespace {
-// persistent forward: iterations and CTAs
-long long fwd_iterations(const fa_params* p) {
-  return make_sched((p->N + 127) / 128, p->B * p->H, p->causal ? 1 : 0, 1).T;
-}
-bool fwd_balanced_applies(const fa_params* p) {
-  return p->dtype != FA_F32 && !p->block_mask && p->dropout_p == 0.f;
-}
-}  // namespace
-
-size_t fa_fwd_balanced_workspace_size(const fa_params* p) {
-  if (fa_check(p, 0) != FA_OK || !fwd_balanced_applies(p)) return 0;
-  const long long T = fwd_iterations(p);
-  const long long G = T < kFwdMaxCtas ? T : kFwdMaxCtas;
-  // two slots per CTA, each fp32 O [128][d] then LSE [128]
-  return align256((size_t)G * 2 * (128 * (size_t)p->d + 128) * 4);
-}
-
-int fa_set_fwd_ctas(int n) { return g_fwd_ctas.exchange(n < 0 ? 0 : n); }
-
-fa_status fa_fwd_balanced(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
-                          float* LSE, void* workspace, size_t workspace_bytes, void* stream) {
-  NvtxRange nvtx_range("fa_fwd_balanced");
-  FA_TRY(fa_check(p, 0));
-  if (!fwd_balanced_applies(p)) return fa_fwd(p, Q, K, V, O, LSE, stream);
-  FA_TRY(need16(Q, "Q"));
-  FA_TRY(need16(K, "K"));
-  FA_TRY(need16(V, "V"));
-  FA_TRY(need16(O, "O"));
-  if (!LSE || !aligned(LSE, 4)) {
-    set_err("LSE is NULL or misaligned");
-    return FA_ERR_INVALID;
-  }
-  const size_t need = fa_fwd_balanced_workspace_size(p);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) {
-    set_err("balanced forward workspace is NULL, not 256-byte aligned or too small");
-    return FA_ERR_WORKSPACE;
-  }
-  DevStatus* st = nullptr;
-  FA_TRY(device_ready(&st));
-  long long G = 2LL * device_sms();
-  if (G > kFwdMaxCtas) G = kFwdMaxCtas;
-  const int cap = g_fwd_ctas.load();
-  if (cap > 0 && cap < G) G = cap;
-  const long long T = fwd_iterations(p);
-  if (G > T) G = T;
-  FwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.B = p->B;
-  a.H = p->H;
-  a.N = p->N;
-  a.scale = p->scale;
-  a.scale_log2 = p->scale * 1.4426950408889634f;
-  a.m = mask_args(p);
-  a.drop = drop_args(p);
-  a.O = O;
-  a.LSE = LSE;
-  a.n_splits = 1;
-  a.split_tiles = (p->N + 127) / 128;
-  a.Opart = static_cast<float*>(workspace);
-  a.G_fwd = (int)G;
-  a.rep = make_report(st);
-  CUtensorMap tm[3];
-  FA_TRY(encode_bhnd(&tm[0], Q, p));
-  FA_TRY(encode_bhnd(&tm[1], K, p));
-  FA_TRY(encode_bhnd(&tm[2], V, p));
-  cudaError_t e = launch_fwd_persist(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "balanced forward launch");
   return FA_OK;
 }
 

@@ -75,11 +75,8 @@ struct FwdArgs {
   // partial O and its LSE to Opart / LSEpart [s] instead of O / LSE
   int n_splits;
   int split_tiles;
-  float* Opart;    // [n_splits][B*H*N][d]; persistent forward: the slots
+  float* Opart;    // [n_splits][B*H*N][d]
   float* LSEpart;  // [n_splits][B*H*N]
-  // persistent forward: CTAs (the slots are 2 per CTA, each fp32 O [128][d]
-  // then LSE [128])
-  int G_fwd;
   // grid order: the heads are taken in groups of head_group (the last group may
   // be smaller); within a group the CTAs run query-tile-major, the heaviest
   // causal tiles of the group's heads first.  head_group = B*H is one group; a
@@ -131,8 +128,6 @@ cudaError_t launch_fwd_f32(const FwdArgs& a, int d, const float* Q, const float*
 cudaError_t launch_fwd_tc(const FwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);
 cudaError_t launch_fwd_merge(const FwdArgs& a, int d, bool f16, cudaStream_t s);
-cudaError_t launch_fwd_persist(const FwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
-                               cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);

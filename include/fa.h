@@ -124,34 +124,6 @@ fa_status fa_check(const fa_params* p, int for_backward);
 fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
                  float* LSE, void* stream);
 
-/*
- * Balanced forward: the same O and LSE as fa_fwd, computed by persistent CTAs
- * (two per SM) that take equal shares of all (query tile, key tile) iterations,
- * numbered query tile by query tile (heaviest causal tiles first), so that no
- * wave runs part-empty.  A CTA's share may begin or end inside a query tile;
- * it then writes that piece's normalised fp32 O and LSE to a workspace slot,
- * and a second kernel merges the pieces of each shared query tile with the
- * statistics merge of "Rastreamento Incremental do Softmax" (the reading guide
- * to the FlashAttention paper): LSE = log sum_s exp(LSE_s),
- * O = sum_s exp(LSE_s - LSE) O_s.  `workspace`: device memory owned by the
- * caller, 256-byte aligned, at least fa_fwd_balanced_workspace_size(p) bytes
- * (else FA_ERR_WORKSPACE); its contents on entry do not matter.  With a block
- * mask, fp32 inputs or dropout this is fa_fwd (the workspace is not used).
- */
-fa_status fa_fwd_balanced(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
-                          float* LSE, void* workspace, size_t workspace_bytes, void* stream);
-
-/* Bytes of workspace fa_fwd_balanced needs: two fp32 slots of 128 x d + 128
- * values per CTA, for min(320, iterations) CTAs, where iterations =
- * B*H*T^2 or B*H*T(T+1)/2 causal, T = ceil(N / 128); 0 when the call would
- * be fa_fwd (block mask, fp32, dropout) or p is invalid. */
-size_t fa_fwd_balanced_workspace_size(const fa_params* p);
-
-/* Upper bound on the CTAs of fa_fwd_balanced (0, the default: two per SM, at
- * most 320).  Returns the previous value; the tests use it to make query tiles
- * shared between CTAs on small problems. */
-int fa_set_fwd_ctas(int n);
-
 /* Largest split count fa_fwd_split accepts. */
 #define FA_MAX_SPLITS 64
 

@@ -169,41 +169,6 @@ def test_split_invalid_calls_return_before_any_launch(lib):
                             ok_ptr, need, None) == fa.FA_ERR_INVALID
 
 
-def test_balanced_forward_workspace_and_fallbacks(lib):
-    up = lambda x: (x + 255) // 256 * 256
-    p = _p(B=4, H=12, N=2048, d=64)
-    assert fa.balanced_workspace_bytes(p) == up(320 * 2 * (128 * 64 + 128) * 4)
-    p = _p(N=300, d=128, causal=1)  # 6 causal iterations: 6 CTAs at most
-    assert fa.balanced_workspace_bytes(p) == up(6 * 2 * (128 * 128 + 128) * 4)
-    assert fa.balanced_workspace_bytes(_p(dtype=fa.FA_F32)) == 0       # fa_fwd
-    assert fa.balanced_workspace_bytes(_p(block_mask=4096)) == 0        # fa_fwd
-    assert fa.balanced_workspace_bytes(_p(d=32)) == 0
-    ok_ptr = 1 << 20
-    p = _p(N=1024)
-    need = fa.balanced_workspace_bytes(p)
-    call = lambda ws, n: lib.fa_fwd_balanced(ctypes.byref(p), ok_ptr, ok_ptr, ok_ptr, ok_ptr, ok_ptr,
-                                             ws, n, None)
-    assert call(ok_ptr, need - 1) == fa.FA_ERR_WORKSPACE
-    assert call(None, need) == fa.FA_ERR_WORKSPACE
-    assert call(ok_ptr + 16, need) == fa.FA_ERR_WORKSPACE
-    old = fa.set_fwd_ctas(9)
-    assert fa.set_fwd_ctas(old) == 9
-
-
-def test_params_mirror_the_header_layout(lib):
-    """The dropout fields sit after the mask strides (float, 8-byte seed, 4-byte offset)."""
-    import ctypes
-    assert fa.FaParams.dropout_p.offset == fa.FaParams.mask_stride_h.offset + 8
-    assert fa.FaParams.dropout_seed.offset == fa.FaParams.dropout_p.offset + 8
-    assert fa.FaParams.dropout_offset.offset == fa.FaParams.dropout_seed.offset + 8
-    assert ctypes.sizeof(fa.FaParams) == fa.FaParams.dropout_offset.offset + 8
-
-
-def test_balanced_forward_with_dropout_is_the_plain_forward(lib):
-    assert fa.balanced_workspace_bytes(_p(N=1024, dropout_p=0.1)) == 0
-    assert fa.balanced_workspace_bytes(_p(N=1024)) > 0
-
-
 def test_fp8_calls_validate_before_any_launch(lib):
     """The FP8 calls reject unsupported settings and bad pointers on the host."""
     ok = 1 << 20  # never dereferenced
