@@ -37,11 +37,11 @@
 // TMEM and issues the MMAs.
 #include "bwd_sched.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kTile = 128;
 
 template <int D>
 struct BwdLayout {
@@ -108,32 +108,8 @@ struct TileInfo {
 };
 constexpr int kFirst = 1, kLast = 2, kMore = 4;
 
-__device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
-  if (m.causal && kt > qt) return false;
-  if (m.mask) {
-    const long long at = (long long)b * m.mask_sb + (long long)h * m.mask_sh +
-                         (long long)((qt * kTile) / m.mask_block) * m.mask_cols +
-                         (kt * kTile) / m.mask_block;
-    return m.mask[at] != 0;
-  }
-  return true;
-}
 
-// First query tile at or after qt, before q_end, that sees key tile kt; else q_end.
-__device__ __forceinline__ int next_q(const MaskArgs& m, int b, int h, int qt, int kt, int q_end) {
-  while (qt < q_end && !tile_kept(m, b, h, qt, kt)) ++qt;
-  return qt;
-}
 
-// Row statistics of query q as the compute warps use them: LSE * log2(e), with
-// +inf hiding the row (past the end, or a row that saw no key), and D.
-__device__ __forceinline__ float lse2_of(const BwdArgs& a, int bh, int q) {
-  const float lse = q < a.N ? a.LSE[(size_t)bh * a.N + q] : -INFINITY;
-  return (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
-}
-__device__ __forceinline__ float d_of(const BwdArgs& a, int bh, int q) {
-  return q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
-}
 
 // Out of line: called once per piece, and inlined into the producer it would
 // cost registers in its loop.

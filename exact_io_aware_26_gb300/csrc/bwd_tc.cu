@@ -30,11 +30,11 @@
 // the elementwise steps, which (with one CTA per SM) bound the loop.
 #include "bwd_sched.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kTile = 128;
 
 template <int D, int NG>
 struct BwdLayout {
@@ -79,7 +79,9 @@ struct BwdLayout {
   static constexpr uint32_t NBAR = 11 + 2 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
-  static constexpr uint32_t BYTES = ABORT + 4;
+  static constexpr uint32_t QBITS = ABORT + 4;  // the query tiles that see this key tile (block mask)
+  static constexpr uint32_t BYTES = QBITS + kMaskBitBytes;
+  static_assert(BYTES <= 232448, "shared memory per CTA");
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns.  S^T [0,128) (warpgroup g reads [CW g, CW g + CW)), dP^T
   // [128,256), dV and dK d columns each.  At d = 64, dQ [384,448) and the 16-bit
@@ -101,34 +103,10 @@ struct BwdLayout {
   }
 };
 
-__device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
-  if (m.causal && kt > qt) return false;
-  if (m.mask) {
-    const long long at = (long long)b * m.mask_sb + (long long)h * m.mask_sh +
-                         (long long)((qt * kTile) / m.mask_block) * m.mask_cols +
-                         (kt * kTile) / m.mask_block;
-    return m.mask[at] != 0;
-  }
-  return true;
-}
 
-// First query tile at or after qt that sees key tile kt, or n_tiles.
-__device__ __forceinline__ int next_q(const MaskArgs& m, int b, int h, int qt, int kt, int n_tiles) {
-  while (qt < n_tiles && !tile_kept(m, b, h, qt, kt)) ++qt;
-  return qt;
-}
 
-// Row statistics of query q as the compute warps use them: LSE * log2(e), with
-// +inf hiding the row (past the end, or a row that saw no key), and D.
-__device__ __forceinline__ float lse2_of(const BwdArgs& a, int bh, int q) {
-  const float lse = q < a.N ? a.LSE[(size_t)bh * a.N + q] : -INFINITY;
-  return (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
-}
-__device__ __forceinline__ float d_of(const BwdArgs& a, int bh, int q) {
-  return q < a.N ? a.Dsum[(size_t)bh * a.N + q] : 0.f;
-}
 
-template <int D, bool F16, int NG, bool DROP, bool QS>
+template <int D, bool F16, int NG, bool DROP, bool QS, bool MASKED>
 __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -218,12 +196,23 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       }
     }
   }
+  // block mask (its own instantiation, MASKED, so that launches without one run
+  // unchanged code): the column of query tiles that see this key tile, as bits in
+  // shared memory
+  uint32_t* qbits = reinterpret_cast<uint32_t*>(smem + L::QBITS);
+  const bool use_bits = MASKED && n_tiles <= kMaskBits;
+  if (use_bits)
+    build_tile_bits(qbits, n_tiles, warp, L::NT / 32, lane, [&](int t) { return tile_kept(a.m, b, h, t, kt); });
   if (warp == kMma) {
     tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
+  // the next query tile at or after qt that sees this key tile (after the setup barrier)
+  auto next_qt = [&](int qt) {
+    return use_bits ? next_bit(qbits, qt, q_end) : next_q(a.m, b, h, qt, kt, q_end);
+  };
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
 
@@ -234,8 +223,8 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     // barrier covers Q, dO and the statistics together.
     pre = __shfl_sync(0xffffffffu, pre, 0);
     int it = 0;
-    for (int qt = next_q(a.m, b, h, qt_begin, kt, q_end); qt < q_end;
-         qt = next_q(a.m, b, h, qt + 1, kt, q_end)) {
+    for (int qt = next_qt(qt_begin); qt < q_end;
+         qt = next_qt(qt + 1)) {
       const int s = it % NS;
       if (it >= NS && !warp_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
       if (!__all_sync(0xffffffffu, dbg_check(w, qt >= 0 && qt * kTile < a.N))) break;
@@ -316,7 +305,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         tc_mma_ss_elect(tDQ, dS_mn + mnmajor_step(kk), dK_mn + mnmajor_step(kk), idQ, kk > 0 ? 1u : 0u);
       };
       bool ok = warp_wait(w, bar_kv, 0);
-      int qt = next_q(a.m, b, h, qt_begin, kt, q_end);
+      int qt = next_qt(qt_begin);
       if (ok && qt < q_end && (ok = warp_wait(w, bar_qf(0), 0))) {
         tc_fence_after();
 #pragma unroll
@@ -328,7 +317,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         tc_commit_elect(bar_dp_full);
       }
       for (int it = 0; ok && qt < q_end; ++it) {
-        const int qn = next_q(a.m, b, h, qt + 1, kt, q_end);
+        const int qn = next_qt(qt + 1);
         const bool next = qn < q_end;
         // Within each group the MMA the compute warps wait for next goes first
         // (MMAs execute in issue order).
@@ -410,8 +399,8 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       bool pend = false;
       bool ok = true;
       int it = 0;
-      for (int qt = next_q(a.m, b, h, qt_begin, kt, q_end); qt < q_end;
-           qt = next_q(a.m, b, h, qt + 1, kt, q_end), ++it) {
+      for (int qt = next_qt(qt_begin); qt < q_end;
+           qt = next_qt(qt + 1), ++it) {
         if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
         tc_fence_after();
         if (pend) {
@@ -547,10 +536,10 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     };
     bool ok = true;
     int it = 0;
-    int qt = next_q(a.m, b, h, qt_begin, kt, q_end);
+    int qt = next_qt(qt_begin);
     if (qt < q_end) ok = p_phase(0, qt);
     for (; ok && qt < q_end; ++it) {
-      const int qn = next_q(a.m, b, h, qt + 1, kt, q_end);
+      const int qn = next_qt(qt + 1);
       // ---- dS_i = P_i * (dP_i - D), with dropout P_i * (z_i dP_i - D)
       if (!(ok = warp_wait(w, bar_dp_full, it & 1))) break;
       tc_fence_after();
@@ -727,8 +716,13 @@ cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
     if (a.qsplit > 1) return cudaErrorInvalidValue;
   }
   constexpr bool kQs = (D == 64);
-  auto kern = a.qsplit > 1 ? (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, kQs> : bwd_tc_kernel<D, F16, NG, false, kQs>)
-                           : (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, false> : bwd_tc_kernel<D, F16, NG, false, false>);
+  // query-split launches have no block mask
+  auto kern = a.qsplit > 1 ? (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, kQs, false>
+                                        : bwd_tc_kernel<D, F16, NG, false, kQs, false>)
+              : a.m.mask ? (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, false, true>
+                                      : bwd_tc_kernel<D, F16, NG, false, false, true>)
+                         : (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, false, false>
+                                      : bwd_tc_kernel<D, F16, NG, false, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   // the first a.direct key tiles, one CTA each (the rest, if any, go to the

@@ -31,6 +31,7 @@
 // S and the schedule is serial, as in the 16-bit kernel.
 #include "fp8.h"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace fa {
 namespace {
@@ -107,20 +108,7 @@ __device__ __forceinline__ float pow2_scale(float amax, float& inv) {
   return __uint_as_float((uint32_t)(127 + k) << 23);
 }
 
-__device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
-  if (m.causal && kt > qt) return false;
-  if (m.mask) {
-    const long long at = (long long)b * m.mask_sb + (long long)h * m.mask_sh +
-                         (long long)((qt * kT) / m.mask_block) * m.mask_cols + (kt * kT) / m.mask_block;
-    return m.mask[at] != 0;
-  }
-  return true;
-}
 
-__device__ __forceinline__ int next_kept(const MaskArgs& m, int b, int h, int qt, int kt, int kt_end) {
-  while (kt < kt_end && !tile_kept(m, b, h, qt, kt)) ++kt;
-  return kt;
-}
 
 // ---------------------------------------------------------------- quantise
 

@@ -39,11 +39,11 @@
 // loaded ("Le masquage causal ...": "jamais chargée et jamais calculée").
 #include "bwd_sched.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kTile = 128;        // query rows per CTA = keys per K/V tile
 constexpr float kRescaleThr = 8.f;  // move the running max only past 2^8
 
 template <int D>
@@ -59,7 +59,8 @@ struct FwdLayout {
   static constexpr uint32_t NBAR = 6 + 4 * NS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
-  static constexpr uint32_t BYTES = ABORT + 4;
+  static constexpr uint32_t KBITS = ABORT + 4;  // the key tiles this query tile sees (block mask)
+  static constexpr uint32_t BYTES = KBITS + kMaskBitBytes;
   // TMEM (256 columns): S at [0, 128), O at [128, 128 + D).  At d = 64 the 16-bit
   // P~ has columns of its own, [192, 256), so S_{j+1} can be computed while the
   // softmax of tile j runs; at d = 128 P~ is written over the first 64 columns of S
@@ -69,25 +70,9 @@ struct FwdLayout {
   static constexpr uint32_t T_S = 0, T_O = 128, T_P = PSEP ? 192 : 0;
 };
 
-__device__ __forceinline__ bool tile_kept(const MaskArgs& m, int b, int h, int qt, int kt) {
-  if (m.causal && kt > qt) return false;
-  if (m.mask) {
-    const long long at = (long long)b * m.mask_sb + (long long)h * m.mask_sh +
-                         (long long)((qt * kTile) / m.mask_block) * m.mask_cols +
-                         (kt * kTile) / m.mask_block;
-    return m.mask[at] != 0;
-  }
-  return true;
-}
 
-// First kept key tile at or after kt, or kt_end when there is none.
-__device__ __forceinline__ int next_kept(const MaskArgs& m, int b, int h, int qt, int kt,
-                                         int kt_end) {
-  while (kt < kt_end && !tile_kept(m, b, h, qt, kt)) ++kt;
-  return kt;
-}
 
-template <int D, bool F16, bool DROP>
+template <int D, bool F16, bool DROP, bool MASKED>
 __global__ void __launch_bounds__(192, 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -172,12 +157,22 @@ __global__ void __launch_bounds__(192, 2)
       ++nv;
     }
   }
+  // block mask (its own instantiation, MASKED, so that launches without one run
+  // unchanged code): this query tile's row of kept key tiles as bits in shared memory
+  uint32_t* kbits = reinterpret_cast<uint32_t*>(smem + L::KBITS);
+  const bool use_bits = MASKED && n_tiles <= kMaskBits;
+  if (use_bits)
+    build_tile_bits(kbits, n_tiles, warp, 6, lane, [&](int t) { return tile_kept(a.m, b, h, qt, t); });
   if (warp == 5) {
     tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
+  // the next kept key tile at or after kt (after the setup barrier)
+  auto next_k = [&](int kt) {
+    return use_bits ? next_bit(kbits, kt, kt_end) : next_kept(a.m, b, h, qt, kt, kt_end);
+  };
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
 
@@ -185,7 +180,7 @@ __global__ void __launch_bounds__(192, 2)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       // the rest of the K, V tiles, each into a stage once it is released
-      for (int kt = kt_next; kt < kt_end; kt = next_kept(a.m, b, h, qt, kt + 1, kt_end)) {
+      for (int kt = kt_next; kt < kt_end; kt = next_k(kt + 1)) {
         if (!dbg_check(w, kt >= 0 && kt * kTile < a.N)) break;
         const int s = nk % NS;
         const uint32_t ph = ((nk / NS) - 1) & 1;
@@ -235,11 +230,11 @@ __global__ void __launch_bounds__(192, 2)
         return true;
       };
       bool ok = warp_wait(w, bar_q, 0);
-      int kt = next_kept(a.m, b, h, qt, kt_begin, kt_end);
+      int kt = next_k(kt_begin);
       if (ok && kt < kt_end) ok = issue_s(0);
       for (int it = 0; ok && kt < kt_end; ++it) {
         const int s = it % NS;
-        const int kn = next_kept(a.m, b, h, qt, kt + 1, kt_end);
+        const int kn = next_k(kt + 1);
         // d = 64: S_{j+1} as soon as the softmax has copied S_j out of TMEM
         if (L::PSEP && kn < kt_end) {
           if (!(ok = warp_wait(w, bar_sfree, it & 1))) break;
@@ -277,8 +272,7 @@ __global__ void __launch_bounds__(192, 2)
     float l = 0.f;            // running sum of P~ (fp32)
     bool ok = true;
     int it = 0;
-    for (int kt = next_kept(a.m, b, h, qt, kt_begin, kt_end); kt < kt_end;
-         kt = next_kept(a.m, b, h, qt, kt + 1, kt_end), ++it) {
+    for (int kt = next_k(kt_begin); kt < kt_end; kt = next_k(kt + 1), ++it) {
       // d = 128: S_j is complete, and so is every earlier MMA (P~ V_{j-1}
       // included), so O is stable and P~_{j-1} has been consumed.  d = 64 waits
       // for P~ V_{j-1} separately below.
@@ -346,16 +340,16 @@ __global__ void __launch_bounds__(192, 2)
       // The tile's exponentials in four chunks of 32 keys; each chunk's 16-bit P~
       // goes to TMEM as soon as it is formed (16 columns), so the stores overlap
       // the next chunk's arithmetic instead of waiting at the end.
+      bool o_ready = !(L::PSEP && it > 0);  // P~ V_{j-1} done (d = 128: implied by S_j)
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int pr = 0; pr < 16; ++pr) {
           const int c = 32 * ch + 2 * pr;
-          float x0, x1, p0, p1;
+          float x0, x1;
           f2unpack(ffma2(f2pack(s[c], s[c + 1]), c2p, mp), x0, x1);
-          p0 = ex2(x0);
-          p1 = ex2(x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
           acc[pr & 3] = fadd2(acc[pr & 3], f2pack(p0, p1));  // four independent sums
           if constexpr (DROP) {  // l sums the undropped weights; P~ V takes the dropped ones
             p0 = ((kb[c >> 5] >> (c & 31)) & 1u) ? p0 * a.drop.z : 0.f;
@@ -363,11 +357,11 @@ __global__ void __launch_bounds__(192, 2)
           }
           pk[pr] = pack2<F16>(p0, p1);
         }
-        if (ch == 0 && L::PSEP && it > 0) {
-          // P~ V_{j-1} must be done: it reads the P~ columns and writes O (at
-          // d = 128, S_j complete implies it: MMAs complete in issue order)
+        if (!o_ready) {
+          // P~ V_{j-1} must be done: it reads the P~ columns and writes O
           if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
           tc_fence_after();
+          o_ready = true;
         }
         // P~ (16-bit pairs); at d = 128 over the first 64 columns of S, all of
         // which is already in registers
@@ -477,7 +471,8 @@ __global__ void __launch_bounds__(192, 2)
 template <int D, bool F16>
 cudaError_t launch_t(const FwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   using L = FwdLayout<D>;
-  auto kern = a.drop.on ? fwd_tc_kernel<D, F16, true> : fwd_tc_kernel<D, F16, false>;
+  auto kern = a.m.mask ? (a.drop.on ? fwd_tc_kernel<D, F16, true, true> : fwd_tc_kernel<D, F16, false, true>)
+                       : (a.drop.on ? fwd_tc_kernel<D, F16, true, false> : fwd_tc_kernel<D, F16, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
