@@ -282,9 +282,9 @@ def run_reference(args, w, rank):
                 "d2h_bytes_per_step": 0}}), flush=True)
 
 
-KERNEL_SOURCES = {"bwd_main": ("bwd_tc.cu", "ptx.cuh", "internal.h", "bwd_sched.cuh"),
-                  "fwd": ("fwd_tc.cu", "ptx.cuh", "internal.h", "bwd_sched.cuh"),
-                  "fwd_fp8": ("fwd_fp8.cu", "fp8.h", "ptx.cuh", "internal.h")}
+KERNEL_SOURCES = {"bwd_main": ("bwd_tc.cu", "ptx.cuh", "internal.h", "bwd_sched.cuh", "tiles.cuh"),
+                  "fwd": ("fwd_tc.cu", "ptx.cuh", "internal.h", "bwd_sched.cuh", "tiles.cuh"),
+                  "fwd_fp8": ("fwd_fp8.cu", "fp8.h", "ptx.cuh", "internal.h", "tiles.cuh")}
 TRAFFIC_KEY = {"main": "bwd_main", "fwd": "fwd", "fwd_fp8": "fwd_fp8", "bwd_main": "bwd_main"}
 
 
