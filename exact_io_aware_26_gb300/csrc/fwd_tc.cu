@@ -293,14 +293,23 @@ __global__ void __launch_bounds__(192, 2)
       if (!(ok = warp_wait(w, bar_s, it & 1))) break;
       tc_fence_after();
       float s[kTile];
+      float m8[8];
       {
-        uint32_t u[64];
+        uint32_t u[64], v[64];
         tmem_ld64(tS, u);
+        tmem_ld64_nowait(tS + 64, v);
 #pragma unroll
         for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
-        tmem_ld64(tS + 64, u);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(u[c]);
+        for (int j = 0; j < 4; ++j) {  // maxima of the first half while the second half arrives
+          float mj = fmax3(s[16 * j], s[16 * j + 1], s[16 * j + 2]);
+#pragma unroll
+          for (int c = 3; c + 1 < 16; c += 2) mj = fmax3(mj, s[16 * j + c], s[16 * j + c + 1]);
+          m8[j] = fmaxf(mj, s[16 * j + 15]);
+        }
+        tmem_wait_ld64(v);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(v[c]);
       }
       if (L::PSEP) {  // S_j is in registers: the MMA warp may compute S_{j+1}
         tc_fence_before();
@@ -317,17 +326,28 @@ __global__ void __launch_bounds__(192, 2)
         for (int c = 0; c < kTile; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      // row max as four independent chains (a single chain of dependent maxes
-      // would expose its latency: only two softmax warps share a sub-partition)
-      float m4[4];
+      // the rest of the row max as four more independent chains of sixteen (eight
+      // chains keep the dependent-max latency short: only two softmax warps share
+      // an SM sub-partition); on a tile that masks keys the first four are redone
+      // on the masked values
+      const bool masked_tile = kt * kTile + kTile > a.N || (a.m.causal && kt == qt);
+      if (masked_tile) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float mj = fmax3(s[32 * j], s[32 * j + 1], s[32 * j + 2]);
+        for (int j = 0; j < 4; ++j) {
+          float mj = fmax3(s[16 * j], s[16 * j + 1], s[16 * j + 2]);
 #pragma unroll
-        for (int c = 3; c + 1 < 32; c += 2) mj = fmax3(mj, s[32 * j + c], s[32 * j + c + 1]);
-        m4[j] = fmaxf(mj, s[32 * j + 31]);
+          for (int c = 3; c + 1 < 16; c += 2) mj = fmax3(mj, s[16 * j + c], s[16 * j + c + 1]);
+          m8[j] = fmaxf(mj, s[16 * j + 15]);
+        }
       }
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+#pragma unroll
+      for (int j = 4; j < 8; ++j) {
+        float mj = fmax3(s[16 * j], s[16 * j + 1], s[16 * j + 2]);
+#pragma unroll
+        for (int c = 3; c + 1 < 16; c += 2) mj = fmax3(mj, s[16 * j + c], s[16 * j + c + 1]);
+        m8[j] = fmaxf(mj, s[16 * j + 15]);
+      }
+      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float m_tile = mx * c2;
       float alpha = 1.f;
       if (m_tile > m_use + kRescaleThr) {
