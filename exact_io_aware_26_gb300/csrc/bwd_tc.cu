@@ -51,9 +51,9 @@ struct BwdLayout {
   static constexpr int NT = 32 * (NCW + 2 + NQW);
   // dQ read-out: boxes of 32 query rows x DQC fp32 columns (128-byte rows with
   // the 128-byte swizzle when DQC = 32, 64-byte rows with the 64-byte swizzle
-  // when DQC = 16) for the TMA reduce-add; with dQ warps each stages all D
-  // columns of its 32 rows (D / DQC boxes), else each compute warp its group's
-  // DQG columns
+  // when DQC = 16) for the TMA reduce-add; a dQ warp stages the D columns of
+  // its 32 rows through one box, D / DQC rounds, else each compute warp its
+  // group's DQG columns
   static constexpr int DQG = D / NG;      // dQ columns per warpgroup
   static constexpr int DQC = (QW || NG == 2) ? 32 : 16;
   static constexpr uint32_t BOXB = 32u * DQC * 4u;
@@ -63,20 +63,27 @@ struct BwdLayout {
   static constexpr uint32_t K = 0;
   static constexpr uint32_t V = TILE;
   static constexpr uint32_t QS = 2 * TILE;             // stage s: Q at QS + 2s TILE, dO after it
-  static constexpr uint32_t DST = QS + NS * 2 * TILE;  // dS^T, 128 x 128 16-bit
+  // dS^T, 128 x 128 16-bit: at d = 64 two buffers, so that the compute warps
+  // write dS_{i+1} while the dK_i and dQ_i MMAs still read dS_i; at d = 128 one
+  static constexpr int NDS = (D == 64) ? 2 : 1;
+  static constexpr uint32_t DSB = kTile * kTile * 2;    // bytes of one dS^T buffer
+  static constexpr uint32_t DST = QS + NS * 2 * TILE;  // dS^T buffer b at DST + b DSB
   // per ring stage, the query tile's row statistics: [128] LSE*log2e then [128] D
-  static constexpr uint32_t STAT = DST + kTile * kTile * 2;
-  // dQ staging (one box per compute warp, 32 KiB in all): a buffer of its own
-  // at d = 64; at d = 128 shared memory is full and the dS^T buffer doubles as
-  // staging
+  static constexpr uint32_t STAT = DST + NDS * DSB;
+  // dQ staging: at d = 64 a buffer of its own, one 32 x 32 fp32 box per dQ warp
+  // (16 KiB; each warp stages its 64 columns in two rounds); at d = 128 shared
+  // memory is full and the dS^T buffer doubles as staging, one box per compute
+  // warp
   static constexpr bool STG_SEP = (D == 64);
+  static constexpr uint32_t STG_BYTES = QW ? NQW * BOXB : NCW * BOXB;
   static constexpr uint32_t STG = STG_SEP ? STAT + NS * 256 * 4 : DST;
-  static_assert((QW ? NQW * (D / DQC) : NCW) * BOXB == 2 * kTile * 128, "staging size");
-  static constexpr uint32_t BAR = STAT + NS * 256 * 4 + (STG_SEP ? 2 * kTile * 128 : 0);
-  // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full, 6 ds_free,
-  //           7 dq_full, 8 dq_free, 9 done, 10.. q_full[NS], 10+NS.. q_empty[NS],
-  //           10+2NS pt_free (d = 64: dV_i has finished reading P^T_i)
-  static constexpr uint32_t NBAR = 11 + 2 * NS;
+  static_assert(STG_SEP || STG_BYTES == DSB, "staging size");
+  static constexpr uint32_t BAR = STAT + NS * 256 * 4 + (STG_SEP ? STG_BYTES : 0);
+  // barriers: 0 kv_full, 1 s_full, 2 dp_full, 3 dp_free, 4 p_full, 5 ds_full,
+  //           6 dq_full, 7 dq_free, 8 done, 9 pt_free (d = 64: dV_i has finished
+  //           reading P^T_i), 10.. q_full[NS], 10+NS.. q_empty[NS],
+  //           10+2NS.. ds_free[NDS]
+  static constexpr uint32_t NBAR = 10 + 2 * NS + NDS;
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t QBITS = ABORT + 4;  // the query tiles that see this key tile (block mask)
@@ -135,11 +142,11 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
   const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_dp_full = bar(2), bar_dp_free = bar(3),
-                 bar_p_full = bar(4), bar_ds_full = bar(5), bar_ds_free = bar(6),
-                 bar_dq_full = bar(7), bar_dq_free = bar(8), bar_done = bar(9);
+                 bar_p_full = bar(4), bar_ds_full = bar(5), bar_dq_full = bar(6), bar_dq_free = bar(7),
+                 bar_done = bar(8), bar_pt_free = bar(9);
   auto bar_qf = [&](int s) { return bar(10 + s); };
   auto bar_qe = [&](int s) { return bar(10 + NS + s); };
-  const uint32_t bar_pt_free = bar(10 + 2 * NS);
+  auto bar_ds_free = [&](int b) { return bar(10 + 2 * NS + b); };
 
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     mbar_init(bar_dp_free, L::NCW);
     mbar_init(bar_p_full, L::NCW);
     mbar_init(bar_ds_full, L::NCW);
-    mbar_init(bar_ds_free, 1);
+    for (int b2 = 0; b2 < L::NDS; ++b2) mbar_init(bar_ds_free(b2), 1);
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, L::DQ_READERS);
     mbar_init(bar_done, 1);
@@ -226,6 +233,18 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     for (int qt = next_qt(qt_begin); qt < q_end;
          qt = next_qt(qt + 1)) {
       const int s = it % NS;
+      // the tile's statistics, negated as the compute warps use them (-LSE*log2(e)
+      // and -D), loaded before waiting for the stage to be free, so that their
+      // global-memory latency overlaps that wait
+      float4 l4, d4;
+      l4.x = -lse2_of(a, bh, qt * kTile + lane * 4 + 0);
+      l4.y = -lse2_of(a, bh, qt * kTile + lane * 4 + 1);
+      l4.z = -lse2_of(a, bh, qt * kTile + lane * 4 + 2);
+      l4.w = -lse2_of(a, bh, qt * kTile + lane * 4 + 3);
+      d4.x = -d_of(a, bh, qt * kTile + lane * 4 + 0);
+      d4.y = -d_of(a, bh, qt * kTile + lane * 4 + 1);
+      d4.z = -d_of(a, bh, qt * kTile + lane * 4 + 2);
+      d4.w = -d_of(a, bh, qt * kTile + lane * 4 + 3);
       if (it >= NS && !warp_wait(w, bar_qe(s), ((it / NS) - 1) & 1)) break;
       if (!__all_sync(0xffffffffu, dbg_check(w, qt >= 0 && qt * kTile < a.N))) break;
       if (lane == 0 && it >= pre) {
@@ -236,17 +255,7 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
           tma_load_3d(dst + L::TILE + c * (kTile * 128), &tmdO, bar_qf(s), c * 64, qt * kTile, bh);
         }
       }
-      // negated, as the compute warps use them: -LSE*log2(e) and -D
       float* st = reinterpret_cast<float*>(smem + L::STAT) + s * 256;
-      float4 l4, d4;
-      l4.x = -lse2_of(a, bh, qt * kTile + lane * 4 + 0);
-      l4.y = -lse2_of(a, bh, qt * kTile + lane * 4 + 1);
-      l4.z = -lse2_of(a, bh, qt * kTile + lane * 4 + 2);
-      l4.w = -lse2_of(a, bh, qt * kTile + lane * 4 + 3);
-      d4.x = -d_of(a, bh, qt * kTile + lane * 4 + 0);
-      d4.y = -d_of(a, bh, qt * kTile + lane * 4 + 1);
-      d4.z = -d_of(a, bh, qt * kTile + lane * 4 + 2);
-      d4.w = -d_of(a, bh, qt * kTile + lane * 4 + 3);
       reinterpret_cast<float4*>(st)[lane] = l4;
       reinterpret_cast<float4*>(st + 128)[lane] = d4;
       mbar_arrive(bar_qf(s));
@@ -279,8 +288,10 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       // base descriptors; per-step descriptors are one add away
       const uint64_t dK_k = desc_kmajor_base(sb + L::K), dV_k = desc_kmajor_base(sb + L::V);
       const uint64_t dK_mn = desc_mnmajor_base(sb + L::K, kTile);
+      // dS^T buffer of query tile i: it mod NDS
       const uint64_t dS_k = desc_kmajor_base(sb + L::DST);
       const uint64_t dS_mn = desc_mnmajor_base(sb + L::DST, kTile);
+      auto ds_off = [&](int it) { return (uint32_t)(it % L::NDS) * L::DSB; };
       const uint64_t dQ_k0 = desc_kmajor_base(sb + L::QS), dQ_mn0 = desc_mnmajor_base(sb + L::QS, kTile);
       auto stage_off = [&](int it) { return (uint32_t)(it % NS) * 2u * L::TILE; };
       auto mma_s = [&](int it, int kk) {
@@ -298,11 +309,12 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
                         (it > 0 || kk > 0) ? 1u : 0u);
       };
       auto mma_dk = [&](int it, int kk) {
-        tc_mma_ss_elect(tDK, dS_k + kmajor_step(kk, kTile), desc_add(dQ_mn0, stage_off(it)) + mnmajor_step(kk),
-                        idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_mma_ss_elect(tDK, desc_add(dS_k, ds_off(it)) + kmajor_step(kk, kTile),
+                        desc_add(dQ_mn0, stage_off(it)) + mnmajor_step(kk), idKV, (it > 0 || kk > 0) ? 1u : 0u);
       };
-      auto mma_dq = [&](int kk) {
-        tc_mma_ss_elect(tDQ, dS_mn + mnmajor_step(kk), dK_mn + mnmajor_step(kk), idQ, kk > 0 ? 1u : 0u);
+      auto mma_dq = [&](int it, int kk) {
+        tc_mma_ss_elect(tDQ, desc_add(dS_mn, ds_off(it)) + mnmajor_step(kk), dK_mn + mnmajor_step(kk), idQ,
+                        kk > 0 ? 1u : 0u);
       };
       bool ok = warp_wait(w, bar_kv, 0);
       int qt = next_qt(qt_begin);
@@ -360,14 +372,14 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
         if (!L::ALIAS && it > 0 && !(ok = warp_wait(w, bar_dq_free, (it - 1) & 1))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) mma_dq(kk);
+        for (int kk = 0; kk < kTile / 16; ++kk) mma_dq(it, kk);
         // at d = 64 dQ_i may be read out while dK_i runs; at d = 128 the dQ staging
         // reuses the dS^T buffer that dK_i reads, so dq_full waits for dK_i too
         if (L::STG_SEP) tc_commit_elect(bar_dq_full);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) mma_dk(it, kk);
         if (!L::STG_SEP) tc_commit_elect(bar_dq_full);
-        tc_commit_elect(bar_ds_free);
+        tc_commit_elect(bar_ds_free(it % L::NDS));
         tc_commit_elect(bar_qe(it % NS));
         if (L::ALIAS && next) {
           // dP^T_{i+1} goes over dQ_i: wait until it has been read out
@@ -395,19 +407,17 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
       // reduces have finished reading it.
       const int qd = warp & 3;
       const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-      const uint32_t stg = sb + L::STG + (uint32_t)qd * (D / L::DQC) * L::BOXB;
-      bool pend = false;
+      const uint32_t stg = sb + L::STG + (uint32_t)qd * L::BOXB;  // this warp's box
+      bool pend = false;  // a reduce may still be reading the box
       bool ok = true;
       int it = 0;
       for (int qt = next_qt(qt_begin); qt < q_end;
            qt = next_qt(qt + 1), ++it) {
         if (!(ok = warp_wait(w, bar_dq_full, it & 1))) break;
         tc_fence_after();
-        if (pend) {
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-        }
-        // one box (DQC columns) at a time: out of TMEM, then into shared memory
+        // one box (DQC columns) at a time: out of TMEM, into the box once the
+        // previous reduce has finished reading it, then reduced into the
+        // accumulator
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += L::DQC) {
           uint32_t dq[L::DQC];
@@ -417,23 +427,24 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_dq_free);
           }
+          if (pend) {
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
           // row `lane` of the box: 16-byte chunk x at x ^ (row mod 8) (the map's
           // 128-byte swizzle)
-          const uint32_t box = stg + (uint32_t)(c0 / L::DQC) * L::BOXB;
 #pragma unroll
           for (int x = 0; x < L::DQC / 4; ++x)
-            st_shared_v4(box + (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16), dq[4 * x],
+            st_shared_v4(stg + (uint32_t)lane * 128u + (uint32_t)((x ^ (lane & 7)) * 16), dq[4 * x],
                          dq[4 * x + 1], dq[4 * x + 2], dq[4 * x + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0 && dbg_check(w, qt * kTile < a.N)) {
+            tma_reduce_add_3d(&tmdQ, stg, c0, qt * kTile + qd * 32, bh);
+            bulk_commit_group();
+          }
+          pend = true;
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0 && dbg_check(w, qt * kTile < a.N)) {
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += L::DQC)
-            tma_reduce_add_3d(&tmdQ, stg + (uint32_t)(c0 / L::DQC) * L::BOXB, c0, qt * kTile + qd * 32, bh);
-          bulk_commit_group();
-        }
-        pend = true;
       }
       if (lane == 0) bulk_wait_group0();  // this warp's dQ reductions fully done
     }
@@ -577,12 +588,15 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
           pk[cc / 2 + 1] = pack2<F16>(y2, y3);
         }
       }
-      if (it > 0 && !(ok = warp_wait(w, bar_ds_free, (it - 1) & 1))) break;
+      // the dS^T buffer of this tile (it mod NDS) must have been read by the dK and
+      // dQ MMAs of its previous use, tile it - NDS
+      if (it >= L::NDS && !(ok = warp_wait(w, bar_ds_free(it % L::NDS), ((it / L::NDS) - 1) & 1))) break;
       // at d = 128 the last dQ reduction must have finished reading this region
       if (!L::STG_SEP) stg_acquire();
 #pragma unroll
       for (int ch = 0; ch < CW / 8; ++ch)
-        st_shared_v4(sb + L::DST + sw128_chunk_offset(r, (CW / 8) * g + ch, kTile), pk[ch * 4 + 0],
+        st_shared_v4(sb + L::DST + (uint32_t)(it % L::NDS) * L::DSB + sw128_chunk_offset(r, (CW / 8) * g + ch, kTile),
+                     pk[ch * 4 + 0],
                      pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
       fence_async_smem();
       tc_fence_before();
