@@ -153,7 +153,7 @@ __device__ void qsplit_key_tile(const BwdArgs& a, int unit, int part) {
   const int kt = unit / BH, bh = unit % BH;
   constexpr int PER = 2 * 128 * D / 4;  // float4 per slot ([dV | dK])
   constexpr int SLICE = PER / kFixupParts;
-  const float4* base = reinterpret_cast<const float4*>(a.slots) + (size_t)unit * a.qsplit * PER;
+  const float4* base = reinterpret_cast<const float4*>(a.slots) + (size_t)(unit - a.qs_from) * a.qsplit * PER;
   for (int e = part * SLICE + (int)threadIdx.x; e < (part + 1) * SLICE; e += blockDim.x) {
     float4 acc = base[e];
     for (int sp = 1; sp < a.qsplit; ++sp) {
@@ -179,12 +179,13 @@ __device__ void qsplit_key_tile(const BwdArgs& a, int unit, int part) {
 }
 
 // Blocks [0, dq_blocks) convert the dQ accumulator; blocks after them,
-// kFixupParts per key tile, add up a query-split backward's partial dK, dV.
+// kFixupParts per split key tile (units qs_from on), add up a query-split
+// backward's partial dK, dV.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) bwd_finalize_qsplit_kernel(const BwdArgs a, int dq_blocks) {
   if ((int)blockIdx.x >= dq_blocks) {
     const int k = (int)blockIdx.x - dq_blocks;
-    qsplit_key_tile<D, F16>(a, k / kFixupParts, k % kFixupParts);
+    qsplit_key_tile<D, F16>(a, a.qs_from + k / kFixupParts, k % kFixupParts);
     return;
   }
   const long long n8 = (long long)a.B * a.H * a.N * D / 8;
@@ -239,8 +240,9 @@ cudaError_t pre_t(const BwdArgs& a, cudaStream_t s) {
 
 template <int D, bool F16>
 cudaError_t fin_qsplit_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
-  const int units = a.B * a.H * ((a.N + 127) / 128);
-  bwd_finalize_qsplit_kernel<D, F16><<<dq_blocks + units * kFixupParts, 256, 0, s>>>(a, dq_blocks);
+  const int units = a.B * a.H * ((a.N + 127) / 128);  // the split ones: [qs_from, units)
+  bwd_finalize_qsplit_kernel<D, F16><<<dq_blocks + (units - a.qs_from) * kFixupParts, 256, 0, s>>>(
+      a, dq_blocks);
   return cudaGetLastError();
 }
 

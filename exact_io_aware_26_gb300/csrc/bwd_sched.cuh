@@ -92,13 +92,24 @@ __host__ __device__ inline void sched_locate(const Sched& s, long long g, int& b
 // Grid order of a one-CTA-per-tile launch (both passes): CTA t of a grid over
 // `tiles` tiles of each of BH heads, the heads taken in groups of `group` (the
 // last group may be smaller) and the tiles of a group tile-major, so that the
-// CTAs running at any moment share the streamed operands of one group of heads.
-// Returns the tile index ti (0 first: the caller maps it to its heaviest tile)
-// and the head bh.  group = BH is plain tile-major order over all heads.
-__host__ __device__ inline void group_order(int t, int tiles, int BH, int group, int& ti, int& bh) {
+// CTAs running at any moment share the streamed operands of one group of heads;
+// the last `tail` heads (0: none) form one more tile-major group after them, so
+// that on a causal problem their heaviest tiles start early enough not to
+// finish alone after everything else.  Returns the tile index ti (0 first: the
+// caller maps it to its heaviest tile) and the head bh.  group = BH, tail = 0
+// is plain tile-major order over all heads.
+__host__ __device__ inline void group_order(int t, int tiles, int BH, int group, int tail, int& ti,
+                                            int& bh) {
+  const int body = BH - tail;  // heads before the tail group
+  if (t >= body * tiles) {
+    const int r = t - body * tiles;
+    ti = r / tail;
+    bh = body + r % tail;
+    return;
+  }
   const int per_group = group * tiles;
   const int g0 = (t / per_group) * group;  // first head of t's group
-  const int gh = BH - g0 < group ? BH - g0 : group;  // heads in that group
+  const int gh = body - g0 < group ? body - g0 : group;  // heads in that group
   const int r = t - g0 * tiles;
   ti = r / gh;
   bh = g0 + r % gh;

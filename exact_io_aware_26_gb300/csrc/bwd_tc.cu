@@ -127,18 +127,24 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
 
   const int BH = a.B * a.H;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  // QS (a query-split launch, qsplit = 2): CTAs 2u and 2u + 1 share key tile u
-  const int unit = QS ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  // QS (a query-split launch, qsplit > 1): from unit qs_from on, qsplit CTAs
+  // share each key tile, CTA part taking the part-th slice of its query tiles
+  int unit = (int)blockIdx.x, part = -1;
+  if (QS && unit >= a.qs_from) {
+    const int j = unit - a.qs_from;
+    unit = a.qs_from + j / a.qsplit;
+    part = j % a.qsplit;
+  }
   // causal: low key tiles see the most queries, so they go first, within groups
   // of head_group heads (a query-split launch keeps the unit numbering of its
   // workspace slots: one group)
   int kt, bh;
-  group_order(unit, n_tiles, BH, QS ? BH : a.head_group, kt, bh);
+  group_order(unit, n_tiles, BH, QS ? BH : a.head_group, QS ? 0 : a.head_tail, kt, bh);
   const int b = bh / a.H, h = bh % a.H;
-  // this CTA's query tiles: [qt_begin, q_end) (all of them without QS)
-  const int q_half = (n_tiles + 1) / 2;
-  const int qt_begin = QS ? (int)(blockIdx.x & 1) * q_half : (a.m.causal ? kt : 0);
-  const int q_end = QS ? min(n_tiles, qt_begin + q_half) : n_tiles;
+  // this CTA's query tiles: [qt_begin, q_end) (all of them for a whole key tile)
+  const int q_per = QS ? (n_tiles + a.qsplit - 1) / a.qsplit : n_tiles;
+  const int qt_begin = part >= 0 ? part * q_per : (a.m.causal ? kt : 0);
+  const int q_end = part >= 0 ? min(n_tiles, qt_begin + q_per) : n_tiles;
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
   const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_dp_full = bar(2), bar_dp_free = bar(3),
@@ -652,10 +658,10 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     }
     // tcgen05.ld is .sync.aligned: every lane of the warp loads (the condition
     // `ok`/`have` is warp-uniform); only the stores are predicated on the row
-    if constexpr (QS) {
+    if (QS && part >= 0) {
       if (ok) {
-        // half of the key tile's query tiles: fp32 partial sums, dK unscaled
-        float* slot = a.slots + (size_t)blockIdx.x * (2 * kTile * D);
+        // a slice of the key tile's query tiles: fp32 partial sums, dK unscaled
+        float* slot = a.slots + ((size_t)(unit - a.qs_from) * a.qsplit + part) * (2 * kTile * D);
         for (int which = 0; which < 2; ++which) {
           const uint32_t col = (which == 0 ? L::T_DV : L::T_DK) + g * L::DQG;
           float* dst = slot + (size_t)which * (kTile * D) + (size_t)r * D + g * L::DQG;
@@ -725,7 +731,7 @@ cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   // enough); with four they would fall into other warps' boxes
   constexpr int NG = (D == 64) ? 4 : 2;
   using L = BwdLayout<D, NG>;
-  // query-split launches (two CTAs per key tile) exist at d = 64 only
+  // query-split launches (several CTAs per key tile) exist at d = 64 only
   if constexpr (D == 128) {
     if (a.qsplit > 1) return cudaErrorInvalidValue;
   }

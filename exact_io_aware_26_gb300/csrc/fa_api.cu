@@ -133,14 +133,22 @@ long long device_l2_bytes() {
 // V fit in three quarters of L2 (the causal N = 23400, 12-head forward is 12%
 // faster that way than head by head, its heaviest tiles all running first); the
 // backward goes head by head beyond half of L2 (faster there than groups sized
-// to fit L2, and than tile-major order).
-int head_group(const fa_params* p, bool backward) {
+// to fit L2, and than tile-major order).  Head by head, a causal launch would
+// end with the last head's heaviest tiles running alone (they start last), so
+// its last heads -- as many as fit the same budget -- form one tile-major group.
+struct HeadOrder {
+  int group, tail;
+};
+HeadOrder head_order(const fa_params* p, bool backward) {
   const long long e = p->dtype == FA_F32 ? 4 : 2;
   const long long per_head = backward ? (long long)p->N * p->d * (2 * e + 4) : (long long)p->N * p->d * 2 * e;
   const long long bh = (long long)p->B * p->H;
   const long long l2 = device_l2_bytes();
   const long long budget = backward ? l2 / 2 : l2 * 3 / 4;
-  return (l2 <= 0 || bh * per_head <= budget) ? (int)bh : 1;
+  if (l2 <= 0 || bh * per_head <= budget) return {(int)bh, 0};
+  long long tail = p->causal ? budget / per_head : 0;
+  if (tail < 2) tail = 0;
+  return {1, (int)tail};
 }
 
 Report make_report(DevStatus* st) {
@@ -299,6 +307,7 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
   a.G = 0;
   a.u0 = (int)units;
   a.qsplit = 1;
+  a.qs_from = (int)units;
   if (!p->block_mask) {
     // ... unless that leaves SMs idle, with fewer key tiles than CTAs (one per
     // SM, at most kBwdMaxCtas, or the cap set by fa_set_bwd_ctas):
@@ -312,8 +321,26 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
       //   added up by the finalize kernel (cheaper per (key tile, query tile)
       //   pair than the persistent CTAs, which pay for their piece changes);
       a.qsplit = 2;
+      a.qs_from = 0;
       a.direct = (int)(2 * units);
       return a;
+    }
+    const long long r = units % G;
+    if (p->d == 64 && !p->causal && cap == 0 && units > G && r > 0 && n >= 4) {
+      // - d = 64, non-causal, a grid that ends in a partly filled wave of r key
+      //   tiles: those r tiles are split k ways over the SMs the wave leaves
+      //   idle, so the launch ends about (k - 1) / k of a key tile sooner; k
+      //   slices of at least two query tiles each, every slice non-empty, and
+      //   r k partial-sum slots within the workspace's two per persistent CTA
+      const long long slots = 2 * (long long)kBwdMaxCtas;
+      long long k = std::min<long long>(G / r, n / 2);
+      while (k > 1 && (r * k > slots || (k - 1) * ((n + k - 1) / k) >= n)) --k;
+      if (k >= 2) {
+        a.qsplit = (int)k;
+        a.qs_from = (int)(units - r);
+        a.direct = (int)(units - r + r * k);
+        return a;
+      }
     }
     // - otherwise persistent stream-K CTAs take them all.  A cap also hands the
     //   last one to two waves' worth of a non-causal grid that would end in a
@@ -335,7 +362,11 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
   }
   // every key tile its own CTA: in groups of heads whose streamed operands fit
   // in L2 together
-  a.head_group = (a.G == 0 && a.direct == units && a.qsplit == 1) ? head_group(p, true) : p->B * p->H;
+  if (a.G == 0 && a.direct == units && a.qsplit == 1) {
+    const HeadOrder ho = head_order(p, true);
+    a.head_group = ho.group;
+    a.head_tail = ho.tail;
+  }
   return a;
 }
 
@@ -580,7 +611,9 @@ fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V
   a.LSE = LSE;
   a.n_splits = 1;
   a.split_tiles = (p->N + 127) / 128;
-  a.head_group = head_group(p, false);
+  const HeadOrder ho = head_order(p, false);
+  a.head_group = ho.group;
+  a.head_tail = ho.tail;
   a.rep = make_report(st);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -705,7 +738,9 @@ fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const v
   a.LSE = LSE;
   a.n_splits = used;
   a.split_tiles = per;
-  a.head_group = head_group(p, false);
+  const HeadOrder ho = head_order(p, false);
+  a.head_group = ho.group;
+  a.head_tail = ho.tail;
   a.Opart = static_cast<float*>(workspace);
   a.LSEpart = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                        align256((size_t)num_splits * rows * (size_t)p->d * 4));

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(192, 2)
   // heads in groups of head_group; within a group the heaviest (causal) query
   // tiles of all its heads first
   int qt, bh;
-  group_order(tile, n_tiles, BH, a.head_group, qt, bh);
+  group_order(tile, n_tiles, BH, a.head_group, a.head_tail, qt, bh);
   qt = n_tiles - 1 - qt;
   const int b = bh / a.H, h = bh % a.H;
   // this CTA's key tiles: [kt_begin, kt_end)

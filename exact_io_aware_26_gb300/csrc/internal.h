@@ -80,8 +80,10 @@ struct FwdArgs {
   // grid order: the heads are taken in groups of head_group (the last group may
   // be smaller); within a group the CTAs run query-tile-major, the heaviest
   // causal tiles of the group's heads first.  head_group = B*H is one group; a
-  // smaller group keeps the K, V that the running CTAs stream within L2
+  // smaller group keeps the K, V that the running CTAs stream within L2.  The
+  // last head_tail heads (0: none) form one more group after the others
   int head_group;
+  int head_tail;
   DropArgs drop;
   Report rep;
 };
@@ -107,17 +109,22 @@ struct BwdArgs {
   int G;
   int u0;
   float* slots;
-  // qsplit = 2 (d = 64, non-causal, direct CTAs only): the direct grid has two
-  // CTAs per key tile, CTA 2u + s taking the s-th half of the query tiles and
-  // writing fp32 [dV | dK] partial sums (dK unscaled) to slot 2u + s; the
-  // finalize kernel adds them up.  1: one CTA per key tile.
+  // qsplit > 1 (d = 64, non-causal, no block mask, direct CTAs only): key tiles
+  // (units) [0, qs_from) run one CTA each; each unit u >= qs_from runs qsplit
+  // CTAs, CTA qs_from + (u - qs_from) qsplit + s taking the s-th of qsplit equal
+  // slices of the query tiles and writing fp32 [dV | dK] partial sums (dK
+  // unscaled) to slot (u - qs_from) qsplit + s; the finalize kernel adds them
+  // up.  qsplit = 1: one CTA per key tile.
   int qsplit;
+  int qs_from;
   // grid order of a launch whose every unit is its own CTA (qsplit = 1, G = 0):
   // the heads in groups of head_group, key-tile-major within a group (the
   // heaviest causal key tiles of the group's heads first); B*H is one group.  A
   // smaller group keeps the Q, dO and dQ accumulator the running CTAs stream
-  // within L2.  Other launches use the key-tile-major unit numbering.
+  // within L2; the last head_tail heads (0: none) form one more group after the
+  // others.  Other launches use the key-tile-major unit numbering.
   int head_group;
+  int head_tail;
   DropArgs drop;
   Report rep;
 };

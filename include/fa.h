@@ -207,7 +207,9 @@ fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V
  *       and fp32 partial dK, dV in the workspace; otherwise persistent CTAs
  *       (about one per SM) that split the (key tile, query tile) iterations
  *       evenly, a key tile whose iterations several CTAs share getting fp32
- *       partial sums in the workspace.
+ *       partial sums in the workspace.  At d = 64, non-causal, unmasked, with
+ *       more key tiles than SMs and no cap set: the key tiles of a last, partly
+ *       filled wave are split the same way over the SMs it leaves idle.
  * finalize: dQ = scale * accumulator, converted to `dtype`, and dK, dV of the
  *       shared key tiles from their partial sums.  Must follow the main stage
  *       of the same call sequence (same p, workspace and fa_set_bwd_ctas). */

@@ -5,7 +5,7 @@
 // key tiles that sched_shared reports (one boundary each) name exactly the
 // CTAs and slots that hold their partial sums.
 // Usage: sched_check n BH causal G u0   (exit status 0 when every check holds)
-//        sched_check group tiles BH group   (the head-group grid order)
+//        sched_check group tiles BH group tail   (the head-group grid order)
 #include <cstdio>
 #include <cstdlib>
 #include <map>
@@ -27,32 +27,41 @@ using namespace fa;
   } while (0)
 
 // Grid order (group_order): CTAs 0 .. tiles*BH - 1 visit every (tile, head) once;
-// the heads come in groups of `group` (the last smaller), a group's CTAs are
-// contiguous and tile-major (non-decreasing tile index, heads cycling within the
-// group), and group = BH is the plain order ti = t / BH, bh = t % BH.
-static int check_group(int tiles, int BH, int group) {
+// the first BH - tail heads come in groups of `group` (the last smaller) and the
+// last `tail` heads in one group after them; a group's CTAs are contiguous and
+// tile-major (non-decreasing tile index, heads cycling within the group), and
+// group = BH, tail = 0 is the plain order ti = t / BH, bh = t % BH.
+static int check_group(int tiles, int BH, int group, int tail) {
   std::set<std::pair<int, int>> seen;
   int prev_g0 = -1, prev_ti = -1;
+  const int body = BH - tail;
   for (int t = 0; t < tiles * BH; ++t) {
     int ti, bh;
-    group_order(t, tiles, BH, group, ti, bh);
+    group_order(t, tiles, BH, group, tail, ti, bh);
     CHECK(ti >= 0 && ti < tiles && bh >= 0 && bh < BH);
     CHECK(seen.insert({ti, bh}).second);
-    const int g0 = bh / group * group, gh = BH - g0 < group ? BH - g0 : group;
+    int g0, gh;  // the first head of bh's group and the group's size
+    if (bh >= body) {
+      g0 = body;
+      gh = tail;
+    } else {
+      g0 = bh / group * group;
+      gh = body - g0 < group ? body - g0 : group;
+    }
     CHECK(t >= g0 * tiles && t < (g0 + gh) * tiles);  // the group's CTAs are contiguous
     if (g0 == prev_g0) CHECK(ti >= prev_ti);           // tile-major within the group
     CHECK(bh - g0 == (t - g0 * tiles) % gh);
     prev_g0 = g0;
     prev_ti = ti;
-    if (group == BH) CHECK(ti == t / BH && bh == t % BH);
+    if (group == BH && tail == 0) CHECK(ti == t / BH && bh == t % BH);
   }
   CHECK((int)seen.size() == tiles * BH);
   return 0;
 }
 
 int main(int argc, char** argv) {
-  if (argc == 5 && std::string(argv[1]) == "group")
-    return check_group(std::atoi(argv[2]), std::atoi(argv[3]), std::atoi(argv[4]));
+  if (argc == 6 && std::string(argv[1]) == "group")
+    return check_group(std::atoi(argv[2]), std::atoi(argv[3]), std::atoi(argv[4]), std::atoi(argv[5]));
   if (argc != 6) return 2;
   const int n = std::atoi(argv[1]), BH = std::atoi(argv[2]), causal = std::atoi(argv[3]),
             G = std::atoi(argv[4]), u0 = std::atoi(argv[5]);

@@ -40,14 +40,17 @@ def test_schedule_covers_every_iteration_once(checker, n, BH, causal, G, u0):
 
 
 GROUP_CASES = [
-    # tiles, BH, group
-    (183, 12, 12), (183, 12, 7), (183, 12, 1), (128, 32, 11), (128, 32, 5), (16, 48, 48),
-    (1, 1, 1), (3, 5, 2), (7, 9, 4), (2, 3, 3), (5, 7, 6), (4, 4, 1),
+    # tiles, BH, group, tail
+    (183, 12, 12, 0), (183, 12, 7, 0), (183, 12, 1, 0), (128, 32, 11, 0), (128, 32, 5, 0),
+    (16, 48, 48, 0), (1, 1, 1, 0), (3, 5, 2, 0), (7, 9, 4, 0), (2, 3, 3, 0), (5, 7, 6, 0), (4, 4, 1, 0),
+    # the last heads as one more group (causal launches run head by head)
+    (183, 12, 1, 5), (183, 12, 1, 12), (183, 12, 1, 2), (128, 32, 1, 7), (7, 9, 4, 3), (5, 7, 2, 6),
+    (1, 3, 1, 3), (3, 2, 1, 1),
 ]
 
 
-@pytest.mark.parametrize("tiles,BH,group", GROUP_CASES)
-def test_group_order_visits_every_tile_once_group_by_group(checker, tiles, BH, group):
-    r = subprocess.run([checker, "group", str(tiles), str(BH), str(group)], capture_output=True,
-                       text=True)
+@pytest.mark.parametrize("tiles,BH,group,tail", GROUP_CASES)
+def test_group_order_visits_every_tile_once_group_by_group(checker, tiles, BH, group, tail):
+    r = subprocess.run([checker, "group", str(tiles), str(BH), str(group), str(tail)],
+                       capture_output=True, text=True)
     assert r.returncode == 0, r.stderr + r.stdout
