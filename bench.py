@@ -723,7 +723,7 @@ def kernel_pass(fa, t, runs, stream, flush, iters: int):
     return out
 
 
-KERNEL_NAMES = {"fwd": "fwd_tc_kernel", "main": "bwd_tc_kernel / bwd_persist_kernel",
+KERNEL_NAMES = {"fwd": "fwd_tc_kernel", "main": "bwd_tc_kernel",
                 "pre": "bwd_preprocess_kernel", "fin": "bwd_finalize_kernel"}
 
 

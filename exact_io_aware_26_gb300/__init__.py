@@ -359,7 +359,7 @@ def bwd_finalize(p: FaParams, dq, dk, dv, workspace, stream=None):
 
 
 def set_bwd_ctas(n: int) -> int:
-    """fa_set_bwd_ctas: cap on the persistent backward CTAs (0 = one per SM)."""
+    """fa_set_bwd_ctas: the CTAs per wave the backward plans its slices for (0 = one per SM)."""
     return int(load().fa_set_bwd_ctas(int(n)))
 
 

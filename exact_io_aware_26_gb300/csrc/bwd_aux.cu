@@ -5,9 +5,9 @@
 //               accumulator zeroed.  D_i equals sum_j P_ij dP_ij, the row term
 //               of dS = P * (dP - D), because O_i = sum_j P_ij v_j.
 //   finalize:   dQ = scale * accumulator, rounded to the 16-bit output type;
-//               and, after a persistent (stream-K) main kernel, dK and dV of
-//               every key tile that several CTAs shared: the sum of their fp32
-//               partial slots (bwd_sched.cuh).
+//               and, after a sliced main kernel, dK and dV of every key tile
+//               cut into several slices: the sum of their fp32 partial slots
+//               (bwd_sched.cuh).
 // Both are plain streaming kernels: 16-byte vector loads/stores, coalesced,
 // grid sized to a multiple of the SM count.
 #include "bwd_sched.cuh"
@@ -64,99 +64,28 @@ __global__ void __launch_bounds__(256) bwd_finalize_kernel(const float4* __restr
   }
 }
 
-// Block `boundary` looks at the boundary between CTA c = boundary and c + 1 of
-// the main kernel; if a key tile is shared there (sched_shared), the block
-// adds the partial slots of the CTAs that share it and writes its dK, dV.
-// Fixup blocks per CTA boundary: each adds one slice of the key tile's slots,
+// Fixup blocks per sliced key tile: each adds one part of the key tile's slots,
 // so that enough loads are in flight to hide their latency.
 constexpr int kFixupParts = 8;
 
-// Block `part` of boundary `boundary` (between CTA c = boundary and c + 1 of the
-// main kernel): if a key tile is shared there (sched_shared), the block adds
-// its slice of the partial slots of the CTAs that share it and writes that
-// slice of the key tile's dK, dV.
+// Block `part` of unit `unit` (a key tile of a sliced main kernel): if the unit
+// was cut into several slices, the block adds its part of their partial slots
+// and writes that part of the key tile's dV and dK (dK times the score scale).
 template <int D, bool F16>
-__device__ void fixup_key_tile(const BwdArgs& a, int boundary, int part) {
+__device__ void slices_key_tile(const BwdArgs& a, long long unit, int part) {
   const int BH = a.B * a.H;
-  const Sched s = make_sched((a.N + 127) / 128, BH, a.m.causal, a.G, a.u0);
-  const int c = boundary;
-  int bh, kt, c_last, fs;
-  if (!sched_shared(s, c, bh, kt, c_last, fs)) return;
+  const int n = (a.N + 127) / 128;
+  long long first;
+  int count;
+  unit_slots(unit, n, BH, a.m.causal, a.q_slice, a.qs_from, first, count);
+  if (count < 2) return;  // a whole key tile: written by its CTA
+  const int kt = (int)(unit / BH), bh = (int)(unit % BH);
   constexpr int PER = 2 * 128 * D / 4;  // float4 per slot ([dV | dK])
-  constexpr int SLICE = PER / kFixupParts;
-  const float4* first = reinterpret_cast<const float4*>(a.slots) + (size_t)fs * PER;
-  for (int e = part * SLICE + (int)threadIdx.x; e < (part + 1) * SLICE; e += blockDim.x) {
-    float4 acc = first[e];
-    // the other contributors' slots (2c'); usually one or two
-    int cc = c + 1;
-    for (; cc + 1 <= c_last; cc += 2) {
-      const float4 v0 = reinterpret_cast<const float4*>(a.slots)[(size_t)(2 * cc) * PER + e];
-      const float4 v1 = reinterpret_cast<const float4*>(a.slots)[(size_t)(2 * cc + 2) * PER + e];
-      acc.x += v0.x + v1.x;
-      acc.y += v0.y + v1.y;
-      acc.z += v0.z + v1.z;
-      acc.w += v0.w + v1.w;
-    }
-    if (cc <= c_last) {
-      const float4 v = reinterpret_cast<const float4*>(a.slots)[(size_t)(2 * cc) * PER + e];
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    const int f = e * 4;                 // first float of the four
-    const int which = f / (128 * D);     // 0: dV, 1: dK
-    const int row = (f / D) % 128;
-    const int col = f % D;
-    const int key = kt * 128 + row;
-    if (key >= a.N) continue;
-    const float mul = which == 0 ? 1.f : a.scale;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? a.dV : a.dK) + ((size_t)bh * a.N + key) * D + col;
-    uint2 o;
-    o.x = pack2<F16>(acc.x * mul, acc.y * mul);
-    o.y = pack2<F16>(acc.z * mul, acc.w * mul);
-    *reinterpret_cast<uint2*>(dst) = o;
-  }
-}
-
-// Blocks [0, dq_blocks) convert the dQ accumulator; blocks after them,
-// kFixupParts per CTA boundary of a persistent main kernel, finish the shared
-// key tiles.
-template <int D, bool F16>
-__global__ void __launch_bounds__(256) bwd_finalize_fixup_kernel(const BwdArgs a, int dq_blocks) {
-  if ((int)blockIdx.x >= dq_blocks) {
-    const int k = (int)blockIdx.x - dq_blocks;
-    fixup_key_tile<D, F16>(a, k / kFixupParts, k % kFixupParts);
-    return;
-  }
-  const long long n8 = (long long)a.B * a.H * a.N * D / 8;
-  const float4* acc = reinterpret_cast<const float4*>(a.dQacc);
-  uint4* dQ = reinterpret_cast<uint4*>(a.dQ);
-  const long long nthreads = (long long)dq_blocks * blockDim.x;
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += nthreads) {
-    const float4 x = acc[2 * t], y = acc[2 * t + 1];
-    uint4 o;
-    o.x = pack2<F16>(x.x * a.scale, x.y * a.scale);
-    o.y = pack2<F16>(x.z * a.scale, x.w * a.scale);
-    o.z = pack2<F16>(y.x * a.scale, y.y * a.scale);
-    o.w = pack2<F16>(y.z * a.scale, y.w * a.scale);
-    dQ[t] = o;
-  }
-}
-
-// Query-split backward (qsplit > 1): block `part` of key tile `unit` adds its
-// slice of the unit's qsplit partial slots and writes that slice of dV and
-// dK (dK times the score scale).
-template <int D, bool F16>
-__device__ void qsplit_key_tile(const BwdArgs& a, int unit, int part) {
-  const int BH = a.B * a.H;
-  const int kt = unit / BH, bh = unit % BH;
-  constexpr int PER = 2 * 128 * D / 4;  // float4 per slot ([dV | dK])
-  constexpr int SLICE = PER / kFixupParts;
-  const float4* base = reinterpret_cast<const float4*>(a.slots) + (size_t)(unit - a.qs_from) * a.qsplit * PER;
-  for (int e = part * SLICE + (int)threadIdx.x; e < (part + 1) * SLICE; e += blockDim.x) {
+  constexpr int PART = PER / kFixupParts;
+  const float4* base = reinterpret_cast<const float4*>(a.slots) + (size_t)first * PER;
+  for (int e = part * PART + (int)threadIdx.x; e < (part + 1) * PART; e += blockDim.x) {
     float4 acc = base[e];
-    for (int sp = 1; sp < a.qsplit; ++sp) {
+    for (int sp = 1; sp < count; ++sp) {
       const float4 v = base[(size_t)sp * PER + e];
       acc.x += v.x;
       acc.y += v.y;
@@ -179,13 +108,13 @@ __device__ void qsplit_key_tile(const BwdArgs& a, int unit, int part) {
 }
 
 // Blocks [0, dq_blocks) convert the dQ accumulator; blocks after them,
-// kFixupParts per split key tile (units qs_from on), add up a query-split
-// backward's partial dK, dV.
+// kFixupParts per unit from qs_from on, add up the sliced key tiles' partial
+// dK, dV.
 template <int D, bool F16>
-__global__ void __launch_bounds__(256) bwd_finalize_qsplit_kernel(const BwdArgs a, int dq_blocks) {
+__global__ void __launch_bounds__(256) bwd_finalize_slices_kernel(const BwdArgs a, int dq_blocks) {
   if ((int)blockIdx.x >= dq_blocks) {
-    const int k = (int)blockIdx.x - dq_blocks;
-    qsplit_key_tile<D, F16>(a, a.qs_from + k / kFixupParts, k % kFixupParts);
+    const long long k = (long long)blockIdx.x - dq_blocks;
+    slices_key_tile<D, F16>(a, a.qs_from + k / kFixupParts, (int)(k % kFixupParts));
     return;
   }
   const long long n8 = (long long)a.B * a.H * a.N * D / 8;
@@ -239,16 +168,10 @@ cudaError_t pre_t(const BwdArgs& a, cudaStream_t s) {
 }
 
 template <int D, bool F16>
-cudaError_t fin_qsplit_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
-  const int units = a.B * a.H * ((a.N + 127) / 128);  // the split ones: [qs_from, units)
-  bwd_finalize_qsplit_kernel<D, F16><<<dq_blocks + (units - a.qs_from) * kFixupParts, 256, 0, s>>>(
+cudaError_t fin_slices_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
+  const long long units = (long long)a.B * a.H * ((a.N + 127) / 128);  // sliced: [qs_from, units)
+  bwd_finalize_slices_kernel<D, F16><<<(unsigned)(dq_blocks + (units - a.qs_from) * kFixupParts), 256, 0, s>>>(
       a, dq_blocks);
-  return cudaGetLastError();
-}
-
-template <int D, bool F16>
-cudaError_t fin_fixup_t(const BwdArgs& a, int dq_blocks, cudaStream_t s) {
-  bwd_finalize_fixup_kernel<D, F16><<<dq_blocks + (a.G - 1) * kFixupParts, 256, 0, s>>>(a, dq_blocks);
   return cudaGetLastError();
 }
 
@@ -262,15 +185,10 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_
 cudaError_t launch_bwd_finalize(const BwdArgs& a, int d, bool f16, cudaStream_t s) {
   const long long n8 = (long long)a.B * a.H * a.N * d / 8;
   const int grid = grid_for(n8, 256);
-  if (a.qsplit > 1) {
-    // query-split main kernel: the same launch adds up the partial dK, dV
-    if (d == 64) return f16 ? fin_qsplit_t<64, true>(a, grid, s) : fin_qsplit_t<64, false>(a, grid, s);
-    return f16 ? fin_qsplit_t<128, true>(a, grid, s) : fin_qsplit_t<128, false>(a, grid, s);
-  }
-  if (a.G > 1) {
-    // persistent main kernel: the same launch also finishes the shared key tiles
-    if (d == 64) return f16 ? fin_fixup_t<64, true>(a, grid, s) : fin_fixup_t<64, false>(a, grid, s);
-    return f16 ? fin_fixup_t<128, true>(a, grid, s) : fin_fixup_t<128, false>(a, grid, s);
+  if (a.q_slice > 0) {
+    // sliced main kernel: the same launch adds up the sliced key tiles' partial dK, dV
+    if (d == 64) return f16 ? fin_slices_t<64, true>(a, grid, s) : fin_slices_t<64, false>(a, grid, s);
+    return f16 ? fin_slices_t<128, true>(a, grid, s) : fin_slices_t<128, false>(a, grid, s);
   }
   if (f16)
     bwd_finalize_kernel<true><<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(a.dQacc),

@@ -1,20 +1,18 @@
-// bwd_sched.cuh -- how the backward main kernel splits its work over CTAs, and
+// bwd_sched.cuh -- how the backward main kernel spreads its work over CTAs, and
 // the head-group grid order of the one-CTA-per-tile launches of both passes.
 //
 // A unit is one key tile of one head; the units are numbered key-tile-major,
-// u = kt * (B*H) + bh, and each unit's iterations are its visited query tiles
-// (causal: from the key tile's own index up).  The units from u0 on are split
-// "stream-K": their iterations, in that order, are cut into G contiguous
-// ranges of nearly equal length, one per persistent CTA (G about the SM
-// count).  A range may begin or end inside a unit: that key tile's dK, dV are
-// then written by each CTA that touched it as fp32 partial sums into a slot
-// of its own (slot 2c for CTA c's first range piece, 2c + 1 for its last), and
-// the finalize kernel adds the slots.  Units before u0 are whole-key-tile
-// CTAs of the one-CTA-per-key-tile kernel (so that only the last, ragged
-// wave is split), and with a block mask, whose kept query tiles are known on
-// the device only, every unit is.
+// u = kt * (B*H) + bh, and a unit visits query tiles base .. base + vis - 1
+// (causal: base = kt and vis = n - kt; else base = 0 and vis = n).  Units
+// before u0 each run as one CTA.  The units from u0 on are cut into slices of
+// at most P visited query tiles (slices_of(kt) = ceil(vis / P) of them), each
+// slice its own CTA: with fewer key tiles than SMs, so that every SM gets work
+// (u0 = 0, P chosen so that the slices about fill one wave), and for the key
+// tiles of a last, partly filled wave (non-causal only).  A unit cut into
+// several slices gets its dK, dV as fp32 partial sums, one slot per slice, that
+// the finalize kernel adds up.  With a block mask, whose kept query tiles are
+// known on the device only, every unit is one CTA.
 #pragma once
-#include <cmath>
 #include <cstdint>
 
 #ifndef __CUDACC__  // host-only compilers (the schedule is also checked on the CPU)
@@ -24,69 +22,115 @@
 
 namespace fa {
 
-struct Sched {
-  int n;         // tiles per sequence (ceil(N / 128))
-  int BH;        // heads (B * H)
-  int causal;    // query tiles before the key tile are skipped
-  int G;         // CTAs
-  long long P0;  // iterations of the units before u0
-  long long T;   // iterations of units u0 .. n*BH - 1
-};
-
-// Most CTAs a stream-K launch uses (and that the workspace holds slots for).
+// Most slices a launch may cut (the workspace holds a partial-sum slot for each).
 constexpr int kBwdMaxCtas = 160;
 
-// iterations of the key tiles before kt in one head
-__host__ __device__ inline long long sched_before(int kt, int n, int causal) {
-  return causal ? (long long)kt * n - (long long)kt * (kt - 1) / 2 : (long long)kt * n;
-}
 // query tiles key tile kt visits
 __host__ __device__ inline int sched_visited(int kt, int n, int causal) {
   return causal ? n - kt : n;
 }
-// iterations of the units before unit u
-__host__ __device__ inline long long sched_unit_start(long long u, int n, int BH, int causal) {
-  const int kt = (int)(u / BH), bh = (int)(u - (long long)kt * BH);
-  return (long long)BH * sched_before(kt, n, causal) + (long long)bh * sched_visited(kt, n, causal);
+// sum of ceil(m / P) over m = 1 .. M
+__host__ __device__ inline long long ceil_sum(long long M, int P) {
+  const long long q = M / P, r = M % P;
+  return (long long)P * q * (q + 1) / 2 + (q + 1) * r;
 }
-__host__ __device__ inline Sched make_sched(int n, int BH, int causal, int G, long long u0 = 0) {
-  Sched s;
-  s.n = n;
-  s.BH = BH;
-  s.causal = causal;
-  s.G = G;
-  s.P0 = sched_unit_start(u0, n, BH, causal);
-  s.T = (long long)BH * sched_before(n, n, causal) - s.P0;
-  return s;
+// slices of one unit of key tile kt
+__host__ __device__ inline int slices_of(int kt, int n, int causal, int P) {
+  return (sched_visited(kt, n, causal) + P - 1) / P;
 }
-// first iteration of CTA c (c = G gives T), counted from unit u0
-__host__ __device__ inline long long sched_start(const Sched& s, int c) {
-  return (long long)c * s.T / s.G;
+// slices of the units of key tiles 0 .. kt - 1 (all heads); every unit sliced
+__host__ __device__ inline long long slices_before(int kt, int n, int BH, int causal, int P) {
+  if (!causal) return (long long)BH * kt * ((n + P - 1) / P);
+  return (long long)BH * (ceil_sum(n, P) - ceil_sum(n - kt, P));
 }
-// head, key tile and index among the key tile's visited query tiles of iteration g
-__host__ __device__ inline void sched_locate(const Sched& s, long long g, int& bh, int& kt, int& j) {
-  const long long a = g + s.P0;  // from the first unit
-  // the key tile: the largest k with BH * sched_before(k) <= a, i.e. with
-  // sched_before(k) <= r
-  const long long r = a / s.BH;
-  int k;
-  if (!s.causal) {
-    k = (int)(r / s.n);
+
+// One sliced CTA's work: key tile kt of head bh, query tiles [q_first, q_end),
+// and its partial-sum slot (-1: the slice is the whole unit, whose dK, dV it
+// writes itself).
+struct Slice {
+  int kt, bh, q_first, q_end, slot;
+};
+
+// The work of sliced CTA j (0-based, counted from the first sliced unit u0).
+// A causal launch slices from u0 = 0 only.
+__host__ __device__ inline Slice slice_locate(long long j, int n, int BH, int causal, int P, int u0) {
+  int kt, bh, s, k;
+  if (!causal) {
+    k = (n + P - 1) / P;
+    const long long u = u0 + j / k;
+    kt = (int)(u / BH);
+    bh = (int)(u % BH);
+    s = (int)(j % k);
   } else {
-    // a root of k^2 - (2n+1) k + 2r, then corrected by exact integer comparisons
-    const double b2 = 2.0 * s.n + 1.0;
-    const double disc = b2 * b2 - 8.0 * (double)r;
-    k = (int)((b2 - sqrt(disc > 0.0 ? disc : 0.0)) * 0.5);
+    // the key tile: the largest kt with slices_before(kt) <= j (binary search)
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (slices_before(mid, n, BH, causal, P) <= j) lo = mid; else hi = mid - 1;
+    }
+    kt = lo;
+    k = slices_of(kt, n, causal, P);
+    const long long r = j - slices_before(kt, n, BH, causal, P);
+    bh = (int)(r / k);
+    s = (int)(r % k);
   }
-  if (k < 0) k = 0;
-  if (k > s.n - 1) k = s.n - 1;
-  while (k > 0 && sched_before(k, s.n, s.causal) > r) --k;
-  while (k + 1 < s.n && sched_before(k + 1, s.n, s.causal) <= r) ++k;
-  kt = k;
-  const long long rem = a - (long long)s.BH * sched_before(k, s.n, s.causal);
-  const int v = sched_visited(k, s.n, s.causal);
-  bh = (int)(rem / v);
-  j = (int)(rem - (long long)bh * v);
+  const int base = causal ? kt : 0, vis = sched_visited(kt, n, causal);
+  Slice sl;
+  sl.kt = kt;
+  sl.bh = bh;
+  sl.q_first = base + s * P;
+  sl.q_end = base + ((s + 1) * P < vis ? (s + 1) * P : vis);
+  sl.slot = k > 1 ? (int)j : -1;
+  return sl;
+}
+
+// Slots of unit u >= u0 (kt-major numbering): the first one and how many (one:
+// the unit ran whole and has none).
+__host__ __device__ inline void unit_slots(long long u, int n, int BH, int causal, int P, int u0,
+                                           long long& first, int& count) {
+  const int kt = (int)(u / BH), bh = (int)(u % BH);
+  count = slices_of(kt, n, causal, P);
+  first = causal ? slices_before(kt, n, BH, causal, P) + (long long)bh * count
+                 : (u - u0) * (long long)count;
+}
+
+// Sliced CTAs from unit u0 on.
+__host__ __device__ inline long long slice_total(int n, int BH, int causal, int P, int u0) {
+  if (!causal) return ((long long)n * BH - u0) * ((n + P - 1) / P);
+  return slices_before(n, n, BH, causal, P);
+}
+
+// The work split of an unmasked backward over G CTAs per wave (one per SM):
+// P = 0 when every key tile is one CTA; else the units from u0 on are sliced
+// with slice length P.  Returns the CTAs of the launch.
+//  - fewer key tiles than CTAs: every key tile is cut into slices of at most P
+//    visited query tiles, P the smallest whose slices fit in G CTAs;
+//  - non-causal, a grid that ends in a partly filled wave of r key tiles: those
+//    r tiles are cut into k slices of at least two query tiles over the SMs the
+//    wave leaves idle, so the launch ends about (k - 1) / k of a key tile sooner.
+__host__ __device__ inline long long plan_slices(int n, int BH, int causal, long long G, int& P, int& u0) {
+  const long long units = (long long)n * BH;
+  P = 0;
+  u0 = (int)units;
+  if (units < G) {
+    for (int p = 1; p < n; ++p) {
+      const long long total = slice_total(n, BH, causal, p, 0);
+      if (total <= G) {
+        P = p;
+        u0 = 0;
+        return total;
+      }
+    }
+  } else if (!causal && units % G != 0 && n >= 4) {
+    const long long r = units % G;
+    const long long k = (G / r < n / 2) ? G / r : n / 2;
+    if (k >= 2) {
+      P = (int)((n + k - 1) / k);
+      u0 = (int)(units - r);
+      return units - r + r * ((n + P - 1) / P);
+    }
+  }
+  return units;
 }
 
 // Grid order of a one-CTA-per-tile launch (both passes): CTA t of a grid over
@@ -113,53 +157,6 @@ __host__ __device__ inline void group_order(int t, int tiles, int BH, int group,
   const int r = t - g0 * tiles;
   ti = r / gh;
   bh = g0 + r % gh;
-}
-
-// One piece of a CTA's range: key tile kt of head bh, query tiles [q_first, q_end).
-struct Seg {
-  int bh, kt, q_first, q_end;
-  int slot;  // -1: the whole key tile (dK, dV written directly); else the partial-sum slot
-};
-
-// The next piece of CTA c's range [g, g_end); advances g.
-__host__ __device__ inline bool sched_next(const Sched& s, int c, long long& g, long long g_end,
-                                           bool& first, Seg& sg) {
-  if (g >= g_end) return false;
-  int bh, kt, j;
-  sched_locate(s, g, bh, kt, j);
-  const int vis = sched_visited(kt, s.n, s.causal);
-  const long long left = g_end - g;
-  const int j_end = (long long)(vis - j) <= left ? vis : j + (int)left;
-  const int qbase = s.causal ? kt : 0;
-  sg.bh = bh;
-  sg.kt = kt;
-  sg.q_first = qbase + j;
-  sg.q_end = qbase + j_end;
-  sg.slot = (j == 0 && j_end == vis) ? -1 : (first ? 2 * c : 2 * c + 1);
-  g += j_end - j;
-  first = false;
-  return true;
-}
-
-// The key tile that CTAs c and c + 1 share, if their boundary falls inside one
-// and is the first boundary inside it: its head and key tile, the last CTA that
-// shares it, and CTA c's slot for it (its last piece 2c + 1, or its first 2c
-// when its range starts at the key tile).  CTAs c + 1 .. c_last hold it in
-// their first slots, 2c'.
-__host__ __device__ inline bool sched_shared(const Sched& s, int c, int& bh, int& kt, int& c_last,
-                                             int& first_slot) {
-  const long long p = sched_start(s, c + 1);
-  int j;
-  sched_locate(s, p, bh, kt, j);
-  if (j == 0) return false;  // the boundary is at a key tile's start
-  const long long u_start = p - j;
-  const long long u_end = u_start + sched_visited(kt, s.n, s.causal);
-  const long long c_start = sched_start(s, c);
-  if (c_start > u_start) return false;  // an earlier boundary lies inside the key tile
-  c_last = c + 1;
-  while (c_last + 1 < s.G && sched_start(s, c_last + 1) < u_end) ++c_last;
-  first_slot = c_start < u_start ? 2 * c + 1 : 2 * c;
-  return true;
 }
 
 }  // namespace fa

@@ -127,24 +127,27 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
 
   const int BH = a.B * a.H;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  // QS (a query-split launch, qsplit > 1): from unit qs_from on, qsplit CTAs
-  // share each key tile, CTA part taking the part-th slice of its query tiles
-  int unit = (int)blockIdx.x, part = -1;
-  if (QS && unit >= a.qs_from) {
-    const int j = unit - a.qs_from;
-    unit = a.qs_from + j / a.qsplit;
-    part = j % a.qsplit;
+  // this CTA's key tile kt of head bh and its query tiles [qt_begin, q_end)
+  int kt, bh, qt_begin, q_end, slot = -1;
+  if (QS && (int)blockIdx.x >= a.qs_from) {
+    // a sliced launch (QS) from unit qs_from on: one slice of a key tile's
+    // visited query tiles; slot >= 0 when the key tile has several slices
+    const Slice sl = slice_locate((int)blockIdx.x - a.qs_from, n_tiles, BH, a.m.causal, a.q_slice,
+                                  a.qs_from);
+    kt = sl.kt;
+    bh = sl.bh;
+    qt_begin = sl.q_first;
+    q_end = sl.q_end;
+    slot = sl.slot;
+  } else {
+    // a whole key tile.  causal: low key tiles see the most queries, so they go
+    // first, within groups of head_group heads (a sliced launch keeps the
+    // key-tile-major unit numbering of its slices: one group)
+    group_order((int)blockIdx.x, n_tiles, BH, QS ? BH : a.head_group, QS ? 0 : a.head_tail, kt, bh);
+    qt_begin = a.m.causal ? kt : 0;
+    q_end = n_tiles;
   }
-  // causal: low key tiles see the most queries, so they go first, within groups
-  // of head_group heads (a query-split launch keeps the unit numbering of its
-  // workspace slots: one group)
-  int kt, bh;
-  group_order(unit, n_tiles, BH, QS ? BH : a.head_group, QS ? 0 : a.head_tail, kt, bh);
   const int b = bh / a.H, h = bh % a.H;
-  // this CTA's query tiles: [qt_begin, q_end) (all of them for a whole key tile)
-  const int q_per = QS ? (n_tiles + a.qsplit - 1) / a.qsplit : n_tiles;
-  const int qt_begin = part >= 0 ? part * q_per : (a.m.causal ? kt : 0);
-  const int q_end = part >= 0 ? min(n_tiles, qt_begin + q_per) : n_tiles;
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
   const uint32_t bar_kv = bar(0), bar_s_full = bar(1), bar_dp_full = bar(2), bar_dp_free = bar(3),
@@ -658,13 +661,14 @@ __global__ void __launch_bounds__(BwdLayout<D, NG>::NT, 1)
     }
     // tcgen05.ld is .sync.aligned: every lane of the warp loads (the condition
     // `ok`/`have` is warp-uniform); only the stores are predicated on the row
-    if (QS && part >= 0) {
+    if (QS && slot >= 0) {
       if (ok) {
-        // a slice of the key tile's query tiles: fp32 partial sums, dK unscaled
-        float* slot = a.slots + ((size_t)(unit - a.qs_from) * a.qsplit + part) * (2 * kTile * D);
+        // one of several slices of the key tile's query tiles: fp32 partial
+        // sums, dK unscaled
+        float* slotp = a.slots + (size_t)slot * (2 * kTile * D);
         for (int which = 0; which < 2; ++which) {
           const uint32_t col = (which == 0 ? L::T_DV : L::T_DK) + g * L::DQG;
-          float* dst = slot + (size_t)which * (kTile * D) + (size_t)r * D + g * L::DQG;
+          float* dst = slotp + (size_t)which * (kTile * D) + (size_t)r * D + g * L::DQG;
           constexpr int EC = L::DQG < 32 ? L::DQG : 32;
 #pragma unroll
           for (int c0 = 0; c0 < L::DQG; c0 += EC) {
@@ -731,22 +735,15 @@ cudaError_t launch_t(const BwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   // enough); with four they would fall into other warps' boxes
   constexpr int NG = (D == 64) ? 4 : 2;
   using L = BwdLayout<D, NG>;
-  // query-split launches (several CTAs per key tile) exist at d = 64 only
-  if constexpr (D == 128) {
-    if (a.qsplit > 1) return cudaErrorInvalidValue;
-  }
-  constexpr bool kQs = (D == 64);
-  // query-split launches have no block mask
-  auto kern = a.qsplit > 1 ? (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, kQs, false>
-                                        : bwd_tc_kernel<D, F16, NG, false, kQs, false>)
+  // sliced launches (their own instantiation, QS) have no block mask
+  auto kern = a.q_slice > 0 ? (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, true, false>
+                                         : bwd_tc_kernel<D, F16, NG, false, true, false>)
               : a.m.mask ? (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, false, true>
                                       : bwd_tc_kernel<D, F16, NG, false, false, true>)
                          : (a.drop.on ? bwd_tc_kernel<D, F16, NG, true, false, false>
                                       : bwd_tc_kernel<D, F16, NG, false, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
-  // the first a.direct key tiles, one CTA each (the rest, if any, go to the
-  // persistent kernel)
   // the dQ accumulator map whose box matches the staging: {32, 32} with the
   // 128-byte swizzle (tm[4]) or {16, 32} with the 64-byte swizzle (tm[5])
   kern<<<(unsigned)a.direct, L::NT, L::BYTES, s>>>(tm[0], tm[1], tm[2], tm[3], tm[L::DQC == 32 ? 4 : 5], a);

@@ -55,7 +55,7 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<uint32_t> g_epoch{0};
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
-std::atomic<int> g_bwd_ctas{0};  // cap on persistent backward CTAs; 0 = one per SM
+std::atomic<int> g_bwd_ctas{0};  // backward CTAs per wave; 0 = one per SM
 
 constexpr int kMaxDev = 64;
 struct DevState {
@@ -304,65 +304,26 @@ BwdArgs bwd_args(const fa_params* p, void* ws) {
   const int n = (p->N + 127) / 128;
   const long long units = (long long)p->B * p->H * n;
   a.direct = (int)units;  // one CTA per key tile ...
-  a.G = 0;
-  a.u0 = (int)units;
-  a.qsplit = 1;
   a.qs_from = (int)units;
+  a.q_slice = 0;
   if (!p->block_mask) {
-    // ... unless that leaves SMs idle, with fewer key tiles than CTAs (one per
-    // SM, at most kBwdMaxCtas, or the cap set by fa_set_bwd_ctas):
+    // ... unless that leaves SMs idle (plan_slices; G: CTAs per wave, one per
+    // SM, at most kBwdMaxCtas, or the count set by fa_set_bwd_ctas)
     long long G = device_sms();
     if (G > kBwdMaxCtas) G = kBwdMaxCtas;
     const int cap = g_bwd_ctas.load();
     if (cap > 0 && cap < G) G = cap;
-    if (p->d == 64 && !p->causal && 2 * units <= G && n >= 4) {
-      // - d = 64, non-causal, at most half as many key tiles as CTAs: two CTAs
-      //   per key tile, each with half of its query tiles, the partial dK, dV
-      //   added up by the finalize kernel (cheaper per (key tile, query tile)
-      //   pair than the persistent CTAs, which pay for their piece changes);
-      a.qsplit = 2;
-      a.qs_from = 0;
-      a.direct = (int)(2 * units);
-      return a;
-    }
-    const long long r = units % G;
-    if (p->d == 64 && !p->causal && cap == 0 && units > G && r > 0 && n >= 4) {
-      // - d = 64, non-causal, a grid that ends in a partly filled wave of r key
-      //   tiles: those r tiles are split k ways over the SMs the wave leaves
-      //   idle, so the launch ends about (k - 1) / k of a key tile sooner; k
-      //   slices of at least two query tiles each, every slice non-empty, and
-      //   r k partial-sum slots within the workspace's two per persistent CTA
-      const long long slots = 2 * (long long)kBwdMaxCtas;
-      long long k = std::min<long long>(G / r, n / 2);
-      while (k > 1 && (r * k > slots || (k - 1) * ((n + k - 1) / k) >= n)) --k;
-      if (k >= 2) {
-        a.qsplit = (int)k;
-        a.qs_from = (int)(units - r);
-        a.direct = (int)(units - r + r * k);
-        return a;
-      }
-    }
-    // - otherwise persistent stream-K CTAs take them all.  A cap also hands the
-    //   last one to two waves' worth of a non-causal grid that would end in a
-    //   partly filled wave to persistent CTAs (off by default: on GB300 the
-    //   persistent kernel's slower tiles cancel what the fuller last wave gains).
-    long long u0 = -1;
-    if (units < G) {
-      u0 = 0;
-    } else if (cap > 0 && !p->causal && units % G != 0) {
-      u0 = (units / G - 1) * G;
-    }
-    if (u0 >= 0) {
-      const Sched s0 = make_sched(n, p->B * p->H, p->causal ? 1 : 0, 1, u0);
-      if (G > s0.T) G = s0.T;
-      a.direct = (int)u0;
-      a.u0 = (int)u0;
-      a.G = (int)G;
+    int P = 0, u0 = 0;
+    const long long ctas = plan_slices(n, p->B * p->H, p->causal ? 1 : 0, G, P, u0);
+    if (P > 0) {
+      a.q_slice = P;
+      a.qs_from = u0;
+      a.direct = (int)ctas;
     }
   }
   // every key tile its own CTA: in groups of heads whose streamed operands fit
   // in L2 together
-  if (a.G == 0 && a.direct == units && a.qsplit == 1) {
+  if (a.q_slice == 0) {
     const HeadOrder ho = head_order(p, true);
     a.head_group = ho.group;
     a.head_tail = ho.tail;
@@ -762,10 +723,12 @@ size_t fa_bwd_workspace_size(const fa_params* p) {
   const size_t rows = (size_t)p->B * p->H * p->N;
   size_t slots = 0;
   if (!p->block_mask) {
-    // two fp32 [dV | dK] partial-sum slots of 128 x d each per persistent CTA
-    const Sched s0 = make_sched((p->N + 127) / 128, p->B * p->H, p->causal ? 1 : 0, 1);
-    const long long G = s0.T < kBwdMaxCtas ? s0.T : kBwdMaxCtas;
-    slots = align256((size_t)G * 2 * 2 * 128 * (size_t)p->d * 4);
+    // an fp32 [dV | dK] partial-sum slot of 128 x d each per slice CTA: at most
+    // kBwdMaxCtas, and at most one per visited (key tile, query tile) pair
+    const int n = (p->N + 127) / 128;
+    const long long T = (long long)p->B * p->H * (p->causal ? (long long)n * (n + 1) / 2 : (long long)n * n);
+    const long long G = T < kBwdMaxCtas ? T : kBwdMaxCtas;
+    slots = align256((size_t)G * 2 * 128 * (size_t)p->d * 4);
   }
   return align256(rows * 4) + align256(rows * (size_t)p->d * 4) + slots;
 }
@@ -823,8 +786,6 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
   FA_TRY(encode_dqacc(&tm[5], a.dQacc, p, 16));
   cudaError_t e = cudaSuccess;
   if (a.direct > 0) e = launch_bwd_tc(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess && a.G > 0)
-    e = launch_bwd_persist(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) {
     set_err("backward main kernel not available in this build");
     return FA_ERR_UNSUPPORTED;

@@ -101,23 +101,17 @@ struct BwdArgs {
   void* dQ;
   float* Dsum;   // [B*H*N]  rowsum(dO * O)
   float* dQacc;  // [B*H*N*d] fp32 accumulator of dQ / scale
-  // Work split: key tiles (units, numbered u = kt * B*H + bh) [0, direct) run
-  // one CTA each; units [u0, B*H*ceil(N/128)) are split "stream-K" over G
-  // persistent CTAs (G = 0: none), each with two slots of fp32 partial
-  // [dV | dK] sums [128][d] for key tiles it shares
+  // Work split (bwd_sched.cuh): units (key tiles, u = kt * B*H + bh) before
+  // qs_from run one CTA each; with q_slice = P > 0 the units from qs_from on are
+  // cut into slices of at most P visited query tiles, one CTA each, and a unit
+  // of several slices writes fp32 partial [dV | dK] sums (dK unscaled) to the
+  // slots of its slices, which the finalize kernel adds up.  direct: the CTAs
+  // of the launch.
   int direct;
-  int G;
-  int u0;
-  float* slots;
-  // qsplit > 1 (d = 64, non-causal, no block mask, direct CTAs only): key tiles
-  // (units) [0, qs_from) run one CTA each; each unit u >= qs_from runs qsplit
-  // CTAs, CTA qs_from + (u - qs_from) qsplit + s taking the s-th of qsplit equal
-  // slices of the query tiles and writing fp32 [dV | dK] partial sums (dK
-  // unscaled) to slot (u - qs_from) qsplit + s; the finalize kernel adds them
-  // up.  qsplit = 1: one CTA per key tile.
-  int qsplit;
   int qs_from;
-  // grid order of a launch whose every unit is its own CTA (qsplit = 1, G = 0):
+  int q_slice;
+  float* slots;
+  // grid order of a launch whose every unit is its own CTA (q_slice = 0):
   // the heads in groups of head_group, key-tile-major within a group (the
   // heaviest causal key tiles of the group's heads first); B*H is one group.  A
   // smaller group keeps the Q, dO and dQ accumulator the running CTAs stream
@@ -138,8 +132,6 @@ cudaError_t launch_fwd_merge(const FwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);
-cudaError_t launch_bwd_persist(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
-                               cudaStream_t s);
 cudaError_t launch_bwd_finalize(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_wait_selftest(const Report& rep, cudaStream_t s);
 

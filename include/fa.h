@@ -172,10 +172,9 @@ int fa_fwd_num_splits(const fa_params* p, int num_sms);
  * what it needs besides is linear in N ("Análise de Complexidade", reading
  * guide: O(N) extra memory): fp32
  * D = rowsum(dO * O) [B*H*N], the fp32 dQ accumulator [B*H*N*d] and, without a
- * block mask, the fp32 partial-sum slots of the persistent main kernel
- * (2 x 2 x 128 x d values for each of up to min(160, iterations) CTAs, where
- * iterations = B*H*T^2 or B*H*T(T+1)/2 causal, T = ceil(N / 128)).  0 on
- * invalid p. */
+ * block mask, the fp32 partial-sum slots of a sliced main kernel (2 x 128 x d
+ * values for each of up to min(160, pairs) slices, where pairs = B*H*T^2 or
+ * B*H*T(T+1)/2 causal, T = ceil(N / 128)).  0 on invalid p. */
 size_t fa_bwd_workspace_size(const fa_params* p);
 
 /*
@@ -201,15 +200,12 @@ fa_status fa_bwd(const fa_params* p, const void* Q, const void* K, const void* V
  * preprocess: D = rowsum(dO * O) into the workspace, dQ accumulator zeroed.
  * main: recompute P tile by tile, accumulate dK, dV per key tile and add
  *       scale-free dQ contributions into the accumulator.  One CTA per key
- *       tile, whose dK, dV it writes.  Without a block mask and with fewer key
- *       tiles than SMs: at d = 64, non-causal, with at most half as many key
- *       tiles as SMs, two CTAs per key tile, each with half of its query tiles
- *       and fp32 partial dK, dV in the workspace; otherwise persistent CTAs
- *       (about one per SM) that split the (key tile, query tile) iterations
- *       evenly, a key tile whose iterations several CTAs share getting fp32
- *       partial sums in the workspace.  At d = 64, non-causal, unmasked, with
- *       more key tiles than SMs and no cap set: the key tiles of a last, partly
- *       filled wave are split the same way over the SMs it leaves idle.
+ *       tile, whose dK, dV it writes.  Without a block mask, when that would
+ *       leave SMs idle, key tiles are cut into slices of their query tiles,
+ *       one CTA each, a key tile of several slices getting fp32 partial dK, dV
+ *       in the workspace: with fewer key tiles than SMs every key tile (slices
+ *       as short as fill one wave), and, non-causal, the key tiles of a last,
+ *       partly filled wave (over the SMs that wave leaves idle).
  * finalize: dQ = scale * accumulator, converted to `dtype`, and dK, dV of the
  *       shared key tiles from their partial sums.  Must follow the main stage
  *       of the same call sequence (same p, workspace and fa_set_bwd_ctas). */
@@ -221,12 +217,11 @@ fa_status fa_bwd_main(const fa_params* p, const void* Q, const void* K, const vo
 fa_status fa_bwd_finalize(const fa_params* p, void* dQ, void* dK, void* dV, void* workspace,
                           size_t workspace_bytes, void* stream);
 
-/* Upper bound on the CTAs of the persistent backward main kernel (0, the
- * default: one per SM, at most 160).  A cap n > 0 also hands the last one to
- * two waves' worth of a non-causal, unmasked problem to n persistent CTAs.
- * Applies to backward calls made after it; do not change it between the main
- * and finalize stages of one backward pass.  Returns the previous value.  The
- * tests use it to make key tiles shared between CTAs on small problems. */
+/* The CTAs per wave that the backward main kernel plans its slices for (0, the
+ * default: one per SM, at most 160; n > 0: min(n, that)).  Applies to backward
+ * calls made after it; do not change it between the main and finalize stages
+ * of one backward pass.  Returns the previous value.  The tests use it to make
+ * small problems cut their key tiles into slices. */
 int fa_set_bwd_ctas(int n);
 
 /*

@@ -1,10 +1,13 @@
-// Brute-force check of the backward kernel's work split (bwd_sched.cuh) on the
-// CPU: every (head, key tile, query tile) iteration of the units from u0 on is
-// taken by exactly one CTA (and none before u0), pieces that cover a whole key
-// tile have no slot, every other piece has a slot of its own, and the shared
-// key tiles that sched_shared reports (one boundary each) name exactly the
-// CTAs and slots that hold their partial sums.
-// Usage: sched_check n BH causal G u0   (exit status 0 when every check holds)
+// Brute-force check of the backward main kernel's work split (bwd_sched.cuh)
+// on the CPU: for an unmasked problem of n tiles per sequence and BH heads
+// spread over G CTAs per wave, plan_slices cuts the units from u0 on into
+// slices; every visited (head, key tile, query tile) of those units belongs to
+// exactly one slice CTA (and of the units before u0 to none), every slice is
+// non-empty and at most P long, the slices of a unit of several slices have
+// slots of their own that unit_slots names exactly, a unit of one slice has no
+// slot, and the slices fill at most one wave (with fewer key tiles than CTAs)
+// or the idle SMs of the last wave.
+// Usage: sched_check slices n BH causal G   (exit status 0 when every check holds)
 //        sched_check group tiles BH group tail   (the head-group grid order)
 #include <cstdio>
 #include <cstdlib>
@@ -59,74 +62,73 @@ static int check_group(int tiles, int BH, int group, int tail) {
   return 0;
 }
 
-int main(int argc, char** argv) {
-  if (argc == 6 && std::string(argv[1]) == "group")
-    return check_group(std::atoi(argv[2]), std::atoi(argv[3]), std::atoi(argv[4]), std::atoi(argv[5]));
-  if (argc != 6) return 2;
-  const int n = std::atoi(argv[1]), BH = std::atoi(argv[2]), causal = std::atoi(argv[3]),
-            G = std::atoi(argv[4]), u0 = std::atoi(argv[5]);
-  const Sched s = make_sched(n, BH, causal, G, u0);
-  // iteration order: key tile, then head (unit u = kt * BH + bh), then query tile
-  long long g = 0;
-  for (int u = u0; u < n * BH; ++u) {
-    const int kt = u / BH, bh = u % BH;
-    CHECK(sched_unit_start(u, n, BH, causal) == s.P0 + g);
-    for (int q = causal ? kt : 0; q < n; ++q, ++g) {
-      int b2, k2, j2;
-      sched_locate(s, g, b2, k2, j2);
-      CHECK(b2 == bh && k2 == kt && j2 == q - (causal ? kt : 0));
-    }
+static int check_slices(int n, int BH, int causal, long long G) {
+  int P = -1, u0 = -1;
+  const long long units = (long long)n * BH;
+  const long long ctas = plan_slices(n, BH, causal, G, P, u0);
+  if (P == 0) {  // every key tile one CTA
+    CHECK(ctas == units && u0 == units);
+    // slicing would not have shortened the launch: no P < n fits one wave, or
+    // the last wave is full, causal, too full to split, or n < 4
+    if (units < G) CHECK(slice_total(n, BH, causal, n - 1 > 0 ? n - 1 : 1, 0) > G || n == 1);
+    std::printf("ok n=%d BH=%d causal=%d G=%lld: whole key tiles\n", n, BH, causal, G);
+    return 0;
   }
-  CHECK(g == s.T);
-  CHECK(sched_start(s, 0) == 0 && sched_start(s, G) == s.T);
+  CHECK(P >= 1 && P < n && u0 >= 0 && u0 < units);
+  CHECK(!causal || u0 == 0);  // a causal launch slices from the first unit only
+  const long long total = slice_total(n, BH, causal, P, u0);
+  CHECK(ctas == u0 + total);
+  if (units < G) {
+    CHECK(u0 == 0 && total <= G);
+    if (P > 1) CHECK(slice_total(n, BH, causal, P - 1, 0) > G);  // P is the smallest that fits
+  } else {
+    CHECK(!causal && u0 == units - units % G && total <= G && P >= 2);
+  }
   std::vector<int> seen((size_t)BH * n * n, 0);
-  // key tile -> {(cta, slot)} of its partial pieces
-  std::map<std::pair<int, int>, std::set<std::pair<int, int>>> parts;
-  std::set<int> slots;
-  for (int c = 0; c < G; ++c) {
-    long long gg = sched_start(s, c);
-    const long long ge = sched_start(s, c + 1);
-    CHECK(ge > gg);  // no CTA without work
-    bool first = true;
-    Seg sg;
-    int pieces = 0;
-    std::vector<Seg> mine;
-    while (sched_next(s, c, gg, ge, first, sg)) {
-      mine.push_back(sg);
-      ++pieces;
-      CHECK(sg.bh >= 0 && sg.bh < BH && sg.kt >= 0 && sg.kt < n);
-      CHECK(sg.q_first >= (causal ? sg.kt : 0) && sg.q_first < sg.q_end && sg.q_end <= n);
-      for (int q = sg.q_first; q < sg.q_end; ++q) ++seen[((size_t)sg.bh * n + sg.kt) * n + q];
-      const bool whole = sg.q_first == (causal ? sg.kt : 0) && sg.q_end == n;
-      CHECK(whole == (sg.slot < 0));
-      if (sg.slot >= 0) {
-        CHECK(slots.insert(sg.slot).second);
-        parts[{sg.bh, sg.kt}].insert({c, sg.slot});
-      }
-    }
-    CHECK(gg == ge && pieces >= 1);
-    for (size_t k = 0; k < mine.size(); ++k) {
-      if (mine[k].slot < 0) continue;
-      if (k == 0) CHECK(mine[k].slot == 2 * c);
-      else CHECK(k + 1 == mine.size() && mine[k].slot == 2 * c + 1);
+  std::map<long long, std::vector<int>> unit_slot_list;  // unit -> slots of its slices
+  std::map<long long, int> unit_count;                   // unit -> slices
+  std::set<int> used;
+  for (long long j = 0; j < total; ++j) {
+    const Slice sl = slice_locate(j, n, BH, causal, P, u0);
+    CHECK(sl.bh >= 0 && sl.bh < BH && sl.kt >= 0 && sl.kt < n);
+    const long long u = (long long)sl.kt * BH + sl.bh;
+    CHECK(u >= u0);
+    const int base = causal ? sl.kt : 0;
+    CHECK(sl.q_first >= base && sl.q_first < sl.q_end && sl.q_end <= n && sl.q_end - sl.q_first <= P);
+    for (int q = sl.q_first; q < sl.q_end; ++q) ++seen[((size_t)sl.bh * n + sl.kt) * n + q];
+    ++unit_count[u];
+    if (sl.slot >= 0) {
+      CHECK(sl.slot < total && used.insert(sl.slot).second);
+      unit_slot_list[u].push_back(sl.slot);
     }
   }
   for (int bh = 0; bh < BH; ++bh)
     for (int kt = 0; kt < n; ++kt)
       for (int q = 0; q < n; ++q)
         CHECK(seen[((size_t)bh * n + kt) * n + q] ==
-              ((kt * BH + bh >= u0 && (!causal || q >= kt)) ? 1 : 0));
-  // the finalize stage's view of the shared key tiles
-  std::map<std::pair<int, int>, std::set<std::pair<int, int>>> fixed;
-  for (int c = 0; c + 1 < G; ++c) {
-    int bh, kt, c_last, fs;
-    if (!sched_shared(s, c, bh, kt, c_last, fs)) continue;
-    std::set<std::pair<int, int>> want{{c, fs}};
-    for (int cc = c + 1; cc <= c_last; ++cc) want.insert({cc, 2 * cc});
-    CHECK(fixed.emplace(std::make_pair(bh, kt), want).second);  // one boundary per key tile
+              (((long long)kt * BH + bh >= u0 && (!causal || q >= kt)) ? 1 : 0));
+  // the finalize stage's view: unit_slots names each unit's slots exactly
+  for (long long u = u0; u < units; ++u) {
+    long long first;
+    int count;
+    unit_slots(u, n, BH, causal, P, u0, first, count);
+    CHECK(count == unit_count[u]);
+    if (count == 1) {
+      CHECK(unit_slot_list.count(u) == 0);  // one slice: the whole unit, no slot
+    } else {
+      std::vector<int> want;
+      for (int i = 0; i < count; ++i) want.push_back((int)(first + i));
+      CHECK(unit_slot_list[u] == want);
+    }
   }
-  CHECK(fixed == parts);
-  std::printf("ok n=%d BH=%d causal=%d G=%d u0=%d T=%lld shared=%zu\n", n, BH, causal, G, u0, s.T,
-              parts.size());
+  std::printf("ok n=%d BH=%d causal=%d G=%lld: P=%d u0=%d slices=%lld\n", n, BH, causal, G, P, u0, total);
   return 0;
+}
+
+int main(int argc, char** argv) {
+  if (argc == 6 && std::string(argv[1]) == "group")
+    return check_group(std::atoi(argv[2]), std::atoi(argv[3]), std::atoi(argv[4]), std::atoi(argv[5]));
+  if (argc == 6 && std::string(argv[1]) == "slices")
+    return check_slices(std::atoi(argv[2]), std::atoi(argv[3]), std::atoi(argv[4]), std::atoll(argv[5]));
+  return 2;
 }

@@ -1,7 +1,7 @@
-"""Host-only check of how the backward main kernel splits its iterations over
-persistent CTAs (csrc/bwd_sched.cuh), and of the head-group grid order of the
-one-CTA-per-tile launches, by brute force over many shapes: built from the same
-header with the host compiler and run on the CPU."""
+"""Host-only check of how the backward main kernel spreads its work over CTAs
+(csrc/bwd_sched.cuh: whole key tiles, or slices of their query tiles), and of the
+head-group grid order of the one-CTA-per-tile launches, by brute force over many
+shapes: built from the same header with the host compiler and run on the CPU."""
 import os
 import subprocess
 
@@ -20,21 +20,22 @@ def checker(tmp_path_factory):
 
 
 CASES = [
-    # n, BH, causal, G, u0 (first split unit; the units before it run one CTA each)
-    (16, 48, 0, 152, 0), (16, 48, 1, 152, 0),
-    (16, 48, 0, 152, 456),                     # B=4 H=12 N=2048: the last 2 waves' worth split
-    (64, 12, 0, 152, 608), (183, 12, 1, 152, 0),
-    (64, 1, 0, 152, 0), (64, 1, 1, 152, 0),    # one head, N = 8192
-    (128, 32, 0, 152, 3800), (1, 1, 0, 1, 0), (1, 1, 1, 1, 0), (2, 1, 1, 3, 0),
-    (3, 1, 1, 6, 0), (8, 3, 0, 7, 0), (8, 3, 1, 7, 5), (5, 2, 1, 13, 0), (5, 2, 0, 50, 0),
-    (9, 5, 1, 160, 0), (16, 2, 0, 16, 16), (40, 1, 1, 17, 3), (7, 7, 0, 49, 0),
-    (7, 4, 0, 3, 24), (7, 4, 0, 5, 20), (7, 4, 0, 9, 18), (5, 3, 1, 4, 11),
+    # n, BH, causal, G (CTAs per wave)
+    (64, 1, 0, 152), (64, 1, 1, 152),            # one head, N = 8192
+    (16, 48, 0, 152), (16, 48, 1, 152),          # B=4 H=12 N=2048: a last wave of 8 key tiles
+    (183, 12, 1, 152), (183, 12, 0, 152),        # one trading day, 12 heads
+    (16, 10, 0, 152), (16, 11, 0, 152), (16, 14, 0, 152), (8, 20, 0, 152), (5, 31, 0, 152),
+    (16, 16, 0, 152), (128, 32, 0, 152), (32, 2, 0, 152), (32, 2, 1, 152),
+    (1, 1, 0, 152), (1, 1, 1, 152), (2, 1, 1, 3), (3, 1, 1, 6), (8, 3, 0, 7), (8, 3, 1, 7),
+    (5, 2, 1, 13), (5, 2, 0, 50), (9, 5, 1, 160), (16, 2, 0, 16), (40, 1, 1, 17), (7, 7, 0, 49),
+    (7, 4, 0, 3), (7, 4, 0, 5), (7, 4, 0, 9), (5, 3, 1, 4), (4, 7, 0, 9), (3, 2, 0, 160),
+    (28, 1, 0, 50), (7, 4, 1, 50), (27, 1, 1, 40), (4, 37, 0, 152), (100, 1, 1, 152),
 ]
 
 
-@pytest.mark.parametrize("n,BH,causal,G,u0", CASES)
-def test_schedule_covers_every_iteration_once(checker, n, BH, causal, G, u0):
-    r = subprocess.run([checker, str(n), str(BH), str(causal), str(G), str(u0)], capture_output=True,
+@pytest.mark.parametrize("n,BH,causal,G", CASES)
+def test_slices_cover_every_tile_pair_once(checker, n, BH, causal, G):
+    r = subprocess.run([checker, "slices", str(n), str(BH), str(causal), str(G)], capture_output=True,
                        text=True)
     assert r.returncode == 0, r.stderr + r.stdout
 

@@ -56,11 +56,12 @@ def test_bwd_small(cuda_lib, dtype, d, N, causal):
 @pytest.mark.parametrize("ctas", [1, 3, 5, 9, 50])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
-def test_bwd_persistent_ctas_share_key_tiles(cuda_lib, d, causal, ctas):
-    """28 key tiles (B=2, H=2, N=777) under a cap of `ctas` CTAs: 50 puts them all
-    on persistent CTAs; 3, 5 and 9 (non-causal) run most key tiles one CTA each
-    and split the last waves' worth over the persistent CTAs; 1 runs one CTA
-    per key tile.  Split key tiles get their dK, dV from the finalize stage."""
+def test_bwd_sliced_key_tiles(cuda_lib, d, causal, ctas):
+    """28 key tiles (B=2, H=2, N=777) planned for `ctas` CTAs per wave: 50 cuts
+    every key tile into query slices that fill one wave; 3, 5 and 9 (non-causal)
+    run most key tiles one CTA each and cut those of the last, partly filled
+    wave; 1 runs one CTA per key tile.  Key tiles of several slices get their
+    dK, dV from the finalize stage."""
     inp = synth.make_inputs(2, 2, 777, d, "bf16", seed=4200 + ctas + d)
     old = fa.set_bwd_ctas(ctas)
     try:
@@ -71,7 +72,7 @@ def test_bwd_persistent_ctas_share_key_tiles(cuda_lib, d, causal, ctas):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_persistent_and_single_key_tile_paths_agree(cuda_lib, causal):
+def test_bwd_sliced_and_whole_key_tile_paths_agree(cuda_lib, causal):
     """The same gradients (up to summation order) whatever the CTA count."""
     inp = synth.make_inputs(1, 3, 1100, 64, "f16", seed=4300)  # 27 key tiles
     outs = []
@@ -164,10 +165,10 @@ def test_bwd_workload_fp16_n8192_full_and_no_score_matrix(cuda_lib):
     torch.cuda.synchronize()
     peak = torch.cuda.max_memory_allocated() - base
     assert peak <= 1 << 20, f"backward allocated {peak} bytes"
-    # linear in N (D and the dQ accumulator) plus the persistent CTAs' partial-sum
-    # slots, whose size does not depend on N; the score matrix would be N^2 * 2 bytes
+    # linear in N (D and the dQ accumulator) plus the slices' partial-sum slots,
+    # whose size does not depend on N; the score matrix would be N^2 * 2 bytes
     linear = 8192 * 4 + 8192 * 64 * 4
-    slots = 160 * 2 * 2 * 128 * 64 * 4
+    slots = 160 * 2 * 128 * 64 * 4
     assert ws.numel() <= linear + slots + 3 * 256
     assert ws.numel() < 8192 * 8192 * 2 // 4
     assert fa.get_status() == fa.FA_OK

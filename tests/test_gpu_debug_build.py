@@ -1,8 +1,8 @@
 """The debug build of the library (FA_DEBUG, libfa_debug.so): its kernels check the
-tile coordinates they copy from, the schedule's pieces and the rows they store to,
+tile coordinates they copy from, the schedule's slices and the rows they store to,
 and record FA_ERR_BOUNDS instead of trapping when a check fails.  On a sweep of small
 shapes that reaches every launch kind (ragged tails, both head sizes, causal and not,
-block masks, split-KV, the query-split and the persistent backward) every check must
+block masks, split-KV, whole and sliced key tiles in the backward) every check must
 pass (status FA_OK), and the results must be those of the release build and agree with
 the fp64 oracle."""
 import math
@@ -43,9 +43,9 @@ CASES = [
     (1, 1, 1, 64, True, None, 0, 1),
     (2, 3, 63, 64, False, None, 0, 1),
     (1, 2, 129, 128, True, None, 0, 1),
-    (2, 2, 777, 64, True, None, 5, 1),      # persistent backward, shared key tiles
+    (2, 2, 777, 64, True, None, 50, 1),     # every key tile cut into query slices
     (2, 2, 777, 128, False, None, 9, 1),
-    (1, 1, 1000, 64, False, None, 0, 3),    # query-split backward (8 key tiles), split-KV forward
+    (1, 1, 1000, 64, False, None, 0, 3),    # sliced backward (8 key tiles), split-KV forward
     (1, 2, 900, 64, True, 0.4, 0, 1),       # block mask
     (1, 1, 1300, 128, False, 0.5, 0, 4),
 ]

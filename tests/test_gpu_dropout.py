@@ -88,7 +88,7 @@ def test_split_forward_applies_the_oracle_keep_decisions(cuda_lib):
     assert np.array_equal(got, _expect_keep(B, H, N, False, p, seed, off))
 
 
-@pytest.mark.parametrize("ctas", [0, 1])  # 0: persistent CTAs (few key tiles); 1: one CTA per key tile
+@pytest.mark.parametrize("ctas", [0, 1])  # 0: key tiles cut into query slices (few key tiles); 1: whole
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d,dtype", [(64, "f16"), (128, "bf16")])
 def test_backward_regenerates_the_oracle_keep_decisions(cuda_lib, d, dtype, causal, ctas):

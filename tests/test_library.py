@@ -72,16 +72,16 @@ def test_backward_limits(lib):
 
 def test_workspace_size(lib):
     up = lambda x: (x + 255) // 256 * 256
-    # D, the dQ accumulator and, without a block mask, two [dV | dK] fp32 slots
-    # of 128 x d per persistent CTA (at most 160, at most one per iteration)
-    slots = lambda ctas, d: up(ctas * 2 * 2 * 128 * d * 4)
+    # D, the dQ accumulator and, without a block mask, one [dV | dK] fp32 slot
+    # of 128 x d per slice CTA (at most 160, at most one per visited tile pair)
+    slots = lambda ctas, d: up(ctas * 2 * 128 * d * 4)
     p = _p(B=4, H=12, N=2048, d=64)
     rows = 4 * 12 * 2048
     assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4) + slots(160, 64)
     p = _p(N=23400, H=12, d=64, causal=1)
     rows = 12 * 23400
     assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(rows * 4) + up(rows * 64 * 4) + slots(160, 64)
-    p = _p(N=300, H=1, d=128, causal=1)  # 3 tiles: 6 causal iterations, so 6 CTAs at most
+    p = _p(N=300, H=1, d=128, causal=1)  # 3 tiles: 6 causal tile pairs, so 6 slices at most
     assert lib.fa_bwd_workspace_size(ctypes.byref(p)) == up(300 * 4) + up(300 * 128 * 4) + slots(6, 128)
     p = _p(B=2, H=3, N=700, d=64, block_mask=4096)  # one CTA per key tile: no slots
     rows = 2 * 3 * 700
@@ -91,7 +91,7 @@ def test_workspace_size(lib):
 
 def test_bwd_cta_cap_setter(lib):
     old = fa.set_bwd_ctas(7)
-    assert fa.set_bwd_ctas(-3) == 7   # negative clamps to 0 (one per SM)
+    assert fa.set_bwd_ctas(-3) == 7   # negative clamps to 0 (one CTA per SM per wave)
     assert fa.set_bwd_ctas(old) == 0
 
 
