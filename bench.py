@@ -317,7 +317,7 @@ def measured_traffic(workload: str, kind: str):
 def fwd(fa, r, q, k, v, o, lse, stream):
     """The forward of one run: fa_fwd, or fa_fwd_split when the run uses slices."""
     if r["splits"] > 1:
-        fa.fwd_split_raw(r["p"], q, k, v, o, lse, r["splits"], r["fws"], stream)
+        fa.fwd_split_raw(r["p"], q, k, v, o, lse, r["splits"], stream)
     else:
         fa.fwd_raw(r["p"], q, k, v, o, lse, stream)
 
@@ -668,10 +668,7 @@ def make_runs(fa, lib, w, inp, dev, fwd_splits=0, dropout=0.0):
         ws = torch.empty(int(lib.fa_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8,
                          device=dev)
         splits = fwd_splits if fwd_splits > 0 else fa.num_splits(p)
-        fws = None
-        if splits > 1:
-            fws = torch.empty(fa.split_workspace_bytes(p, splits), dtype=torch.uint8, device=dev)
-        runs.append(dict(causal=c, p=p, keep=keep, splits=splits, fws=fws, o=torch.empty_like(q),
+        runs.append(dict(causal=c, p=p, keep=keep, splits=splits, o=torch.empty_like(q),
                          lse=torch.empty(q.shape[:3], dtype=torch.float32, device=dev),
                          dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
                          ws=ws))
@@ -699,7 +696,9 @@ def run_one(fa, t, r, s, ev=None):
 
 
 def launches_per_pass(runs) -> int:
-    return sum(4 + (r["splits"] > 1) for r in runs)
+    """Kernels of one pass: the forward (split or not, one launch) and the backward's
+    three stages, per causal setting."""
+    return 4 * len(runs)
 
 
 def kernel_pass(fa, t, runs, stream, flush, iters: int):
@@ -765,7 +764,6 @@ def measure_workload(fa, lib, name, dev, stream, flush, peak, hbm_peak, iters=5,
     tensors = sum(x.numel() * x.element_size() for x in t.values())
     tensors += sum(r[k].numel() * r[k].element_size() for r in runs
                    for k in ("o", "lse", "dq", "dk", "dv", "ws"))
-    tensors += sum(r["fws"].numel() for r in runs if r["fws"] is not None)
     n2 = 2.0 * w.B * w.H * w.N * w.N
     if extra > (1 << 20):
         raise RuntimeError(f"{name}: {extra} bytes allocated while the path ran")

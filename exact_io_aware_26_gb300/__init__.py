@@ -85,8 +85,7 @@ def load() -> ctypes.CDLL:
     sigs = {
         "fa_check": (I, [PP, I]),
         "fa_fwd": (I, [PP, P, P, P, P, P, P]),
-        "fa_fwd_split": (I, [PP, P, P, P, P, P, I, P, S, P]),
-        "fa_fwd_split_workspace_size": (S, [PP, I]),
+        "fa_fwd_split": (I, [PP, P, P, P, P, P, I, P]),
         "fa_fwd_num_splits": (I, [PP, I]),
         "fa_bwd_workspace_size": (S, [PP]),
         "fa_bwd": (I, [PP, P, P, P, P, P, P, P, P, P, P, S, P]),
@@ -278,12 +277,8 @@ def num_splits(p: FaParams, num_sms: int = 0) -> int:
     return int(load().fa_fwd_num_splits(ctypes.byref(p), int(num_sms)))
 
 
-def split_workspace_bytes(p: FaParams, splits: int) -> int:
-    return int(load().fa_fwd_split_workspace_size(ctypes.byref(p), int(splits)))
-
-
 def attention_fwd_split(q, k, v, scale=None, causal=False, block_mask=None, mask_block=128,
-                        splits=None, out=None, lse=None, workspace=None, stream=None,
+                        splits=None, out=None, lse=None, stream=None,
                         dropout_p=0.0, seed=0, offset=0):
     """O, LSE = fa_fwd_split(Q, K, V): the key range cut into ``splits`` slices
     (None: fa_fwd_num_splits for the current device)."""
@@ -294,24 +289,19 @@ def attention_fwd_split(q, k, v, scale=None, causal=False, block_mask=None, mask
     lib = load()
     if splits is None:
         splits = int(lib.fa_fwd_num_splits(ctypes.byref(p), 0))
-    nbytes = int(lib.fa_fwd_split_workspace_size(ctypes.byref(p), int(splits)))
-    if workspace is None and nbytes > 0:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     _check(lib.fa_fwd_split(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                            int(splits), _ptr(workspace),
-                            0 if workspace is None else workspace.numel(), _stream(stream)),
+                            int(splits), _stream(stream)),
            "fa_fwd_split")
     return out, lse
 
 
-def fwd_split_raw(p: FaParams, q, k, v, o, lse, splits, workspace, stream=None):
+def fwd_split_raw(p: FaParams, q, k, v, o, lse, splits, stream=None):
     _check(load().fa_fwd_split(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                               int(splits), _ptr(workspace),
-                               0 if workspace is None else workspace.numel(), _stream(stream)),
+                               int(splits), _stream(stream)),
            "fa_fwd_split")
 
 

@@ -653,16 +653,8 @@ int fa_fwd_num_splits(const fa_params* p, int num_sms) {
   return best;
 }
 
-size_t fa_fwd_split_workspace_size(const fa_params* p, int num_splits) {
-  if (fa_check(p, 0) != FA_OK || check_splits(p, num_splits) != FA_OK) return 0;
-  if (num_splits == 1) return 0;
-  const size_t rows = (size_t)p->B * p->H * p->N;
-  return align256((size_t)num_splits * rows * (size_t)p->d * 4) + align256((size_t)num_splits * rows * 4);
-}
-
 fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
-                       float* LSE, int num_splits, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+                       float* LSE, int num_splits, void* stream) {
   NvtxRange nvtx_range("fa_fwd_split");
   FA_TRY(fa_check(p, 0));
   FA_TRY(check_splits(p, num_splits));
@@ -675,17 +667,11 @@ fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const v
     set_err("LSE is NULL or misaligned");
     return FA_ERR_INVALID;
   }
-  const size_t need = fa_fwd_split_workspace_size(p, num_splits);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) {
-    set_err("split workspace is NULL, not 256-byte aligned or too small");
-    return FA_ERR_WORKSPACE;
-  }
   DevStatus* st = nullptr;
   FA_TRY(device_ready(&st));
   const int n_tiles = (p->N + 127) / 128;
   int per = 0, used = 0;
   split_shape(n_tiles, num_splits, &per, &used);
-  const size_t rows = (size_t)p->B * p->H * p->N;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   a.B = p->B;
@@ -702,9 +688,6 @@ fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const v
   const HeadOrder ho = head_order(p, false);
   a.head_group = ho.group;
   a.head_tail = ho.tail;
-  a.Opart = static_cast<float*>(workspace);
-  a.LSEpart = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       align256((size_t)num_splits * rows * (size_t)p->d * 4));
   a.rep = make_report(st);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tm[3];
@@ -713,8 +696,6 @@ fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const v
   FA_TRY(encode_bhnd(&tm[2], V, p));
   cudaError_t e = launch_fwd_tc(a, p->d, p->dtype == FA_F16, tm, s);
   if (e != cudaSuccess) return cuda_fail(e, "split forward launch");
-  e = launch_fwd_merge(a, p->d, p->dtype == FA_F16, s);
-  if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
   return FA_OK;
 }
 

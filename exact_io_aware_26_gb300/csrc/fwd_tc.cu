@@ -45,6 +45,7 @@ namespace fa {
 namespace {
 
 constexpr float kRescaleThr = 8.f;  // move the running max only past 2^8
+constexpr int kMaxSplits = FA_MAX_SPLITS;  // key-range slices of a query tile: one cluster
 
 template <int D>
 struct FwdLayout {
@@ -60,7 +61,13 @@ struct FwdLayout {
   static constexpr uint32_t TSLOT = BAR + NBAR * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t KBITS = ABORT + 4;  // the key tiles this query tile sees (block mask)
-  static constexpr uint32_t BYTES = KBITS + kMaskBitBytes;
+  // split launches: each row's (running max, sum) for the cluster's merge
+  static constexpr uint32_t MST = (KBITS + kMaskBitBytes + 7) & ~7u;
+  static constexpr uint32_t BYTES = MST + kTile * 8;
+  // split launches: the weighted partial O, fp32 [128][D], over the K/V stages
+  // once every copy and product has completed
+  static constexpr uint32_t OBUF = K0;
+  static_assert(kTile * D * 4 <= 2 * NS * TILE, "merge buffer");
   // TMEM (256 columns): S at [0, 128), O at [128, 128 + D).  At d = 64 the 16-bit
   // P~ has columns of its own, [192, 256), so S_{j+1} can be computed while the
   // softmax of tile j runs; at d = 128 P~ is written over the first 64 columns of S
@@ -72,7 +79,7 @@ struct FwdLayout {
 
 
 
-template <int D, bool F16, bool DROP, bool MASKED>
+template <int D, bool F16, bool DROP, bool MASKED, bool SPLIT>
 __global__ void __launch_bounds__(192, 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -94,7 +101,7 @@ __global__ void __launch_bounds__(192, 2)
   const int b = bh / a.H, h = bh % a.H;
   // this CTA's key tiles: [kt_begin, kt_end)
   const int kt_begin = split * a.split_tiles;
-  const int kt_end = min(a.m.causal ? min(qt + 1, n_tiles) : n_tiles, kt_begin + a.split_tiles);
+  int kt_end = min(a.m.causal ? min(qt + 1, n_tiles) : n_tiles, kt_begin + a.split_tiles);
 
   auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
   const uint32_t bar_q = bar(0), bar_s = bar(1), bar_p = bar(2), bar_o = bar(3), bar_fin = bar(4),
@@ -110,10 +117,15 @@ __global__ void __launch_bounds__(192, 2)
     if (threadIdx.x == 0) raise_error(w, FA_ERR_CUDA);
     return;
   }
-  // debug build: the CTA's tile, head and key range lie inside the problem
-  if (!dbg_check(w, qt >= 0 && qt < n_tiles && bh >= 0 && bh < BH && kt_begin >= 0 &&
-                        kt_end <= n_tiles && split < a.n_splits))
-    return;
+  // debug build: the CTA's tile, head and key range lie inside the problem.  A
+  // CTA of a split launch must reach its cluster's barriers even then: it keeps
+  // an empty key range and writes nothing.
+  const bool cta_ok = dbg_check(w, qt >= 0 && qt < n_tiles && bh >= 0 && bh < BH && kt_begin >= 0 &&
+                                       kt_end <= n_tiles && split < a.n_splits);
+  if (!cta_ok) {
+    if (!SPLIT) return;
+    kt_end = kt_begin;
+  }
   // The producer lane sets up the barriers and, before the block-wide setup
   // barrier, already issues the copies that need no wait (Q and the first NS
   // K, V tiles), so that their latency overlaps the TMEM allocation.
@@ -175,6 +187,9 @@ __global__ void __launch_bounds__(192, 2)
   };
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
+  // split launches: what the softmax thread of row r hands to the cluster merge
+  float m_fin = -INFINITY, l_fin = 0.f;  // running max (exp2 domain) and sum
+  bool o_fin = false, ok_fin = false;    // O holds products; no wait gave up
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -427,10 +442,9 @@ __global__ void __launch_bounds__(192, 2)
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     const float lse = (l > 0.f) ? (m_use + __log2f(l)) * 0.693147180559945309f : -INFINITY;
-    // debug build: the row's outputs lie inside O and LSE (or the split partials)
-    if (row < a.N && ok)
-      ok = dbg_check(w, (size_t)(split + 1) * BH * a.N > (size_t)split * BH * a.N + (size_t)bh * a.N + row);
-    if (a.n_splits == 1) {
+    // debug build: the row's outputs lie inside O and LSE
+    if (row < a.N && ok) ok = dbg_check(w, (size_t)bh * a.N + row < (size_t)BH * a.N);
+    if constexpr (!SPLIT) {
       if (row < a.N && ok) a.LSE[(size_t)bh * a.N + row] = lse;
       uint16_t* Orow = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D;
 #pragma unroll
@@ -455,29 +469,91 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
     } else {
-      // a slice of the key range: normalised fp32 partial O and its LSE (an
-      // empty slice gives O = 0, LSE = -inf and weighs nothing in the merge)
-      const size_t prow = (size_t)split * BH * a.N + (size_t)bh * a.N + row;
-      if (row < a.N && ok) a.LSEpart[prow] = lse;
-      float* Prow = a.Opart + prow * D;
+      // a slice of the key range: the cluster merges the slices below
+      m_fin = m_use;
+      l_fin = l;
+      o_fin = have_o;
+      ok_fin = ok;
+    }
+  }
+
+  if constexpr (SPLIT) {
+    // The n_splits CTAs of a query tile form one cluster and merge their slices
+    // with the running-statistics merge of "Rastreamento Incremental do Softmax"
+    // (FlashAttention reading guide): with M = max_s m_s and L = sum_s l_s 2^(m_s - M),
+    // O = sum_s 2^(m_s - M) O_s / L and LSE = (M + log2 L) ln 2 (an empty slice has
+    // l_s = 0 and weighs nothing).  Every thread of the cluster reaches the three
+    // cluster barriers, after waits that are bounded, and none leaves early.
+    const uint32_t rank = cluster_rank();
+    const int ks = a.n_splits;
+    const int r = (int)threadIdx.x;
+    constexpr int CPR = D / 4;  // 16-byte chunks of an O row
+    if (warp < 4) reinterpret_cast<float2*>(smem + L::MST)[r] = make_float2(m_fin, l_fin);
+    cluster_sync();  // every slice's statistics are visible
+    if (warp < 4) {
+      float2 st[kMaxSplits];
+      float M = -INFINITY, Ls = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp) {
+        st[sp] = make_float2(-INFINITY, 0.f);
+        if (sp < ks) st[sp] = ld_cluster_f32x2(cluster_map(sb + L::MST + 8u * (uint32_t)r, (uint32_t)sp));
+        if (st[sp].y > 0.f) M = fmaxf(M, st[sp].x);
+      }
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp)
+        if (st[sp].y > 0.f) Ls += st[sp].y * ex2(st[sp].x - M);
+      const float wgt = (l_fin > 0.f && Ls > 0.f) ? ex2(m_fin - M) / Ls : 0.f;
+      const int row = qt * kTile + r;
+      if (rank == 0 && row < a.N && cta_ok)
+        a.LSE[(size_t)bh * a.N + row] = Ls > 0.f ? (M + __log2f(Ls)) * 0.693147180559945309f : -INFINITY;
+      // this slice's weighted O row into the merge buffer (16-byte chunks XOR-
+      // swizzled by row, so that a warp's stores spread over the banks)
+      const uint32_t tO = tmem + L::T_O + ((uint32_t)(warp * 32) << 16);
+      float* ob = reinterpret_cast<float*>(smem + L::OBUF) + (size_t)r * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        if (have_o) {
+        if (o_fin) {
           tmem_ld32(tO + c0, o);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
-        if (row < a.N && ok) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<float4*>(Prow + c0 + v * 4) =
-                make_float4(__uint_as_float(o[v * 4 + 0]) * inv_l, __uint_as_float(o[v * 4 + 1]) * inv_l,
-                            __uint_as_float(o[v * 4 + 2]) * inv_l, __uint_as_float(o[v * 4 + 3]) * inv_l);
+        for (int v = 0; v < 8; ++v) {
+          const int c = c0 / 4 + v;
+          *reinterpret_cast<float4*>(ob + 4 * (c ^ (r & (CPR - 1)))) =
+              make_float4(__uint_as_float(o[4 * v]) * wgt, __uint_as_float(o[4 * v + 1]) * wgt,
+                          __uint_as_float(o[4 * v + 2]) * wgt, __uint_as_float(o[4 * v + 3]) * wgt);
         }
       }
     }
+    cluster_sync();  // every slice's weighted O is visible
+    if (warp < 4) {
+      // CTA `rank` sums its share of the rows over the cluster and writes them
+      const int per = (kTile + ks - 1) / ks;
+      const int r0 = (int)rank * per, r1 = min(kTile, r0 + per);
+      uint16_t* Ob = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + (size_t)qt * kTile) * D;
+      for (int e = r; e < (r1 - r0) * CPR; e += kTile) {
+        const int rr = r0 + e / CPR, c = e % CPR;
+        const uint32_t off = L::OBUF + 4u * (uint32_t)(rr * D + 4 * (c ^ (rr & (CPR - 1))));
+        float4 acc = ld_cluster_f32x4(cluster_map(sb + off, 0));
+        for (int sp = 1; sp < ks; ++sp) {
+          const float4 v = ld_cluster_f32x4(cluster_map(sb + off, (uint32_t)sp));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        if (qt * kTile + rr < a.N && cta_ok) {
+          uint2 pk;
+          pk.x = pack2<F16>(acc.x, acc.y);
+          pk.y = pack2<F16>(acc.z, acc.w);
+          *reinterpret_cast<uint2*>(Ob + (size_t)rr * D + 4 * c) = pk;
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while another reads its shared memory
   }
 
   tc_fence_before();
@@ -488,80 +564,46 @@ __global__ void __launch_bounds__(192, 2)
   }
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool SPLIT>
 cudaError_t launch_t(const FwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   using L = FwdLayout<D>;
-  auto kern = a.m.mask ? (a.drop.on ? fwd_tc_kernel<D, F16, true, true> : fwd_tc_kernel<D, F16, false, true>)
-                       : (a.drop.on ? fwd_tc_kernel<D, F16, true, false> : fwd_tc_kernel<D, F16, false, false>);
+  auto kern = a.m.mask ? (a.drop.on ? fwd_tc_kernel<D, F16, true, true, SPLIT> : fwd_tc_kernel<D, F16, false, true, SPLIT>)
+                       : (a.drop.on ? fwd_tc_kernel<D, F16, true, false, SPLIT> : fwd_tc_kernel<D, F16, false, false, SPLIT>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const unsigned grid = (unsigned)(n_tiles * a.B * a.H * a.n_splits);
-  kern<<<grid, 192, L::BYTES, s>>>(tm[0], tm[1], tm[2], a);
-  return cudaGetLastError();
-}
-
-// Merge of the key-range slices of every query row with the running-statistics
-// merge of "Rastreamento Incremental do Softmax" (FlashAttention reading guide),
-// in log-sum-exp form: LSE = log sum_s exp(LSE_s) and O = sum_s exp(LSE_s - LSE) O_s,
-// each O_s normalised by its own slice's sum.  One warp per row; lane j holds
-// columns [j * D/32, (j + 1) * D/32).
-template <int D, bool F16>
-__global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
-  constexpr int C = D / 32;
-  const long long rows = (long long)a.B * a.H * a.N;
-  const int lane = threadIdx.x & 31;
-  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long r = warp0; r < rows; r += nwarps) {
-    float m = -INFINITY;
-    for (int sp = 0; sp < a.n_splits; ++sp) m = fmaxf(m, a.LSEpart[(size_t)sp * rows + r]);
-    float acc[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) acc[c] = 0.f;
-    float sum = 0.f;
-    if (m != -INFINITY) {
-      for (int sp = 0; sp < a.n_splits; ++sp) {
-        const float lse = a.LSEpart[(size_t)sp * rows + r];
-        const float wgt = ex2((lse - m) * 1.4426950408889634f);  // 0 for an empty slice
-        sum += wgt;
-        const float* src = a.Opart + ((size_t)sp * rows + r) * D + lane * C;
-#pragma unroll
-        for (int c = 0; c < C; ++c) acc[c] = fmaf(wgt, src[c], acc[c]);
-      }
-    }
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(a.O) + r * D + lane * C;
-#pragma unroll
-    for (int c = 0; c < C; c += 2) {
-      const uint32_t pk = pack2<F16>(acc[c] * inv, acc[c + 1] * inv);
-      *reinterpret_cast<uint32_t*>(dst + c) = pk;
-    }
-    if (lane == 0) a.LSE[r] = sum > 0.f ? m + __logf(sum) : -INFINITY;
+  if constexpr (!SPLIT) {
+    kern<<<grid, 192, L::BYTES, s>>>(tm[0], tm[1], tm[2], a);
+    return cudaGetLastError();
   }
+  // the key-range slices of a query tile (consecutive CTAs) form one cluster
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = L::BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.n_splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm[0], tm[1], tm[2], a);
 }
 
 template <int D, bool F16>
-cudaError_t merge_t(const FwdArgs& a, cudaStream_t s) {
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long rows = (long long)a.B * a.H * a.N;
-  long long blocks = (rows + 7) / 8;  // 8 warps per block
-  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
-  fwd_merge_kernel<D, F16><<<(unsigned)blocks, 256, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_d(const FwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
+  // split launches (clusters that merge their slices) are their own instantiation
+  return a.n_splits > 1 ? launch_t<D, F16, true>(a, tm, s) : launch_t<D, F16, false>(a, tm, s);
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_merge(const FwdArgs& a, int d, bool f16, cudaStream_t s) {
-  if (d == 64) return f16 ? merge_t<64, true>(a, s) : merge_t<64, false>(a, s);
-  return f16 ? merge_t<128, true>(a, s) : merge_t<128, false>(a, s);
-}
-
 cudaError_t launch_fwd_tc(const FwdArgs& a, int d, bool f16, const CUtensorMap* tm, cudaStream_t s) {
-  if (d == 64) return f16 ? launch_t<64, true>(a, tm, s) : launch_t<64, false>(a, tm, s);
-  return f16 ? launch_t<128, true>(a, tm, s) : launch_t<128, false>(a, tm, s);
+  if (d == 64) return f16 ? launch_d<64, true>(a, tm, s) : launch_d<64, false>(a, tm, s);
+  return f16 ? launch_d<128, true>(a, tm, s) : launch_d<128, false>(a, tm, s);
 }
 
 }  // namespace fa

@@ -71,12 +71,10 @@ struct FwdArgs {
   void* O;
   float* LSE;
   // split key range: with n_splits > 1, CTA split s covers key tiles
-  // [s * split_tiles, (s + 1) * split_tiles) and writes its normalised fp32
-  // partial O and its LSE to Opart / LSEpart [s] instead of O / LSE
+  // [s * split_tiles, (s + 1) * split_tiles) of its query tile, and the
+  // n_splits CTAs of a query tile (one cluster) merge their slices into O, LSE
   int n_splits;
   int split_tiles;
-  float* Opart;    // [n_splits][B*H*N][d]
-  float* LSEpart;  // [n_splits][B*H*N]
   // grid order: the heads are taken in groups of head_group (the last group may
   // be smaller); within a group the CTAs run query-tile-major, the heaviest
   // causal tiles of the group's heads first.  head_group = B*H is one group; a
@@ -128,7 +126,6 @@ cudaError_t launch_fwd_f32(const FwdArgs& a, int d, const float* Q, const float*
                            const float* V, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);
-cudaError_t launch_fwd_merge(const FwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, bool f16, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, int d, bool f16, const CUtensorMap* tmaps,
                           cudaStream_t s);

@@ -124,40 +124,33 @@ fa_status fa_check(const fa_params* p, int for_backward);
 fa_status fa_fwd(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
                  float* LSE, void* stream);
 
-/* Largest split count fa_fwd_split accepts. */
-#define FA_MAX_SPLITS 64
+/* Largest split count fa_fwd_split accepts (the slices of a query tile run as
+ * one thread-block cluster, at most 8 CTAs in a portable cluster). */
+#define FA_MAX_SPLITS 8
 
 /*
  * Split-KV forward: the same O and LSE as fa_fwd, computed with the key range
  * of every 128-row query tile cut into `num_splits` slices of
  * ceil(ceil(N / 128) / num_splits) key tiles, one CTA per (query tile, slice),
  * so that a problem with few query tiles (one long sequence, few heads) still
- * fills the GPU.  Each slice keeps its own running max and sum and writes its
- * normalised fp32 partial output and its LSE to `workspace`; a second kernel
- * merges the slices of each row with the statistics merge of "Rastreamento
- * Incremental do Softmax" (the reading guide to the FlashAttention paper):
- * m = max_s m_s and l = sum_s exp(m_s - m) l_s, i.e. in log-sum-exp form
- * LSE = log sum_s exp(LSE_s) and O = sum_s exp(LSE_s - LSE) O_s.
- * The key-scan parallelism of the decode kernels mentioned in "Что это
- * изменило на практике" ("Почему Flash Attention быстрее") is the same idea.
+ * fills the GPU.  Each slice keeps its own running max m_s and sum l_s; the
+ * slices of a query tile run as one thread-block cluster and merge in shared
+ * memory with the statistics merge of "Rastreamento Incremental do Softmax"
+ * (the reading guide to the FlashAttention paper): m = max_s m_s,
+ * l = sum_s exp(m_s - m) l_s, O = sum_s exp(m_s - m) O_s / l and
+ * LSE = m + log l, each slice's O_s unnormalised.  Nothing goes through device
+ * memory but Q, K, V, O and LSE.  The key-scan parallelism of the decode
+ * kernels mentioned in "Что это изменило на практике" ("Почему Flash Attention
+ * быстрее") is the same idea.
  *
  * num_splits in [1, min(FA_MAX_SPLITS, ceil(N / 128))], else FA_ERR_INVALID;
  * a count that would leave trailing slices empty runs with the non-empty ones
- * only.  num_splits = 1 is fa_fwd (workspace unused, may be NULL).  fp16/bf16
- * only for num_splits > 1 (FA_F32 -> FA_ERR_UNSUPPORTED).  `workspace` is a
- * device buffer owned by the caller, 256-byte aligned, of at least
- * fa_fwd_split_workspace_size(p, num_splits) bytes (else FA_ERR_WORKSPACE);
- * its contents on entry do not matter.  Results match fa_fwd up to rounding
- * order (the fp32 partials are rounded to `dtype` once, after the merge).
+ * only.  num_splits = 1 is fa_fwd.  fp16/bf16 only for num_splits > 1 (FA_F32
+ * -> FA_ERR_UNSUPPORTED).  Results match fa_fwd up to rounding order (the
+ * fp32 slices are rounded to `dtype` once, after the merge).
  */
 fa_status fa_fwd_split(const fa_params* p, const void* Q, const void* K, const void* V, void* O,
-                       float* LSE, int num_splits, void* workspace, size_t workspace_bytes,
-                       void* stream);
-
-/* Bytes of workspace fa_fwd_split needs: fp32 partial O [num_splits][B*H*N][d]
- * and partial LSE [num_splits][B*H*N], each 256-byte aligned; 0 when
- * num_splits == 1 or the arguments are invalid. */
-size_t fa_fwd_split_workspace_size(const fa_params* p, int num_splits);
+                       float* LSE, int num_splits, void* stream);
 
 /* Split count for fa_fwd_split on a GPU with `num_sms` SMs (<= 0: ask the
  * current device; 1 if that fails).  1 when the unsplit grid of B*H*ceil(N/128)
@@ -226,7 +219,7 @@ int fa_set_bwd_ctas(int n);
 
 /*
  * Maximum workspace, in bytes, that fa_bwd_noalloc can serve (64 MiB); e.g.
- * B=4, H=12, N=2048, d=64 needs about 47 MiB (fa_bwd_workspace_size).
+ * B=4, H=12, N=2048, d=64 needs about 34 MiB (fa_bwd_workspace_size).
  */
 #define FA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 

@@ -141,32 +141,17 @@ def test_split_count_model(lib):
         assert -(-t // per) == s
 
 
-def test_split_workspace_size(lib):
-    up = lambda x: (x + 255) // 256 * 256
-    p = _p(B=1, H=1, N=8192, d=64)
-    rows = 8192
-    assert fa.split_workspace_bytes(p, 1) == 0
-    assert fa.split_workspace_bytes(p, 4) == up(4 * rows * 64 * 4) + up(4 * rows * 4)
-    assert fa.split_workspace_bytes(p, 64) > 0
-    assert fa.split_workspace_bytes(p, 65) == 0    # above FA_MAX_SPLITS
-    assert fa.split_workspace_bytes(p, 0) == 0
-    assert fa.split_workspace_bytes(_p(N=300), 4) == 0   # more slices than key tiles
-
-
 def test_split_invalid_calls_return_before_any_launch(lib):
-    p = _p(N=1024)
     ok_ptr = 1 << 20  # never dereferenced: every call below fails validation first
-    need = fa.split_workspace_bytes(p, 4)
     args = [ok_ptr] * 5
-    call = lambda q, s, ws, n: lib.fa_fwd_split(ctypes.byref(q), *args, s, ws, n, None)
-    assert call(p, 0, ok_ptr, need) == fa.FA_ERR_INVALID
-    assert call(p, 9, ok_ptr, need) == fa.FA_ERR_INVALID       # 8 key tiles
-    assert call(p, 4, ok_ptr, need - 1) == fa.FA_ERR_WORKSPACE
-    assert call(p, 4, None, need) == fa.FA_ERR_WORKSPACE
-    assert call(p, 4, ok_ptr + 16, need) == fa.FA_ERR_WORKSPACE
-    assert call(_p(N=1024, dtype=fa.FA_F32), 4, ok_ptr, need) == fa.FA_ERR_UNSUPPORTED
-    assert lib.fa_fwd_split(ctypes.byref(p), ok_ptr + 2, ok_ptr, ok_ptr, ok_ptr, ok_ptr, 4,
-                            ok_ptr, need, None) == fa.FA_ERR_INVALID
+    call = lambda q, s: lib.fa_fwd_split(ctypes.byref(q), *args, s, None)
+    assert call(_p(N=1024), 0) == fa.FA_ERR_INVALID
+    assert call(_p(N=1024), 9) == fa.FA_ERR_INVALID       # 8 key tiles
+    assert call(_p(N=2048), 9) == fa.FA_ERR_INVALID       # above FA_MAX_SPLITS = 8
+    assert call(_p(N=300), 4) == fa.FA_ERR_INVALID        # more slices than key tiles
+    assert call(_p(N=1024, dtype=fa.FA_F32), 4) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_split(ctypes.byref(_p(N=1024)), ok_ptr + 2, ok_ptr, ok_ptr, ok_ptr, ok_ptr, 4,
+                            None) == fa.FA_ERR_INVALID
 
 
 def test_fp8_calls_validate_before_any_launch(lib):
