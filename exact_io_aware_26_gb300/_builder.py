@@ -22,7 +22,7 @@ LIB = os.path.join(HERE, "libfa.so")
 BUILD_DEBUG = os.path.join(HERE, "_build_debug")
 LIB_DEBUG = os.path.join(HERE, "libfa_debug.so")
 SOURCES = ["fa_api.cu", "fwd_tc.cu", "fwd_f32.cu", "bwd_tc.cu", "bwd_aux.cu", "fa_noalloc.cu", "fwd_fp8.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "bwd_sched.cuh", "fp8.h", "tiles.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "bwd_sched.cuh", "fp8.h", "tiles.cuh", "fwd_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

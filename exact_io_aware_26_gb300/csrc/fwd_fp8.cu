@@ -30,13 +30,12 @@
 // swizzle).  P~ has TMEM columns of its own at d = 64; at d = 128 it overwrites
 // S and the schedule is serial, as in the 16-bit kernel.
 #include "fp8.h"
-#include "ptx.cuh"
-#include "tiles.cuh"
+#include "fwd_common.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kT = 128;  // rows per block = query rows per CTA = keys per key tile
+constexpr int kT = kTile;  // rows per block = query rows per CTA = keys per key tile
 
 // ---------------------------------------------------------------- helpers
 
@@ -254,11 +253,8 @@ struct F8Layout {
   static constexpr uint32_t Q = 0;
   static constexpr uint32_t K0 = Q + TQ;
   static constexpr uint32_t V0 = K0 + NS * TQ;
-  static constexpr uint32_t BAR = V0 + NS * TV;
-  // barriers: 0 q_full, 1 s_full, 2 p_full, 3 o_done, 4 fin, 5 s_free,
-  //           6.. k_full[NS], v_full[NS], k_empty[NS], v_empty[NS]
-  static constexpr uint32_t NBAR = 6 + 4 * NS;
-  static constexpr uint32_t TSLOT = BAR + NBAR * 8;
+  static constexpr uint32_t BAR = V0 + NS * TV;  // FwdBars<NS>
+  static constexpr uint32_t TSLOT = BAR + FwdBars<NS>::kCount * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t BYTES = ABORT + 4;
   // TMEM (256 columns): S [0, 128), O [128, 128 + D); the e4m3 P~ (128 keys, four
@@ -285,13 +281,7 @@ __global__ void __launch_bounds__(192, 2)
   const int b = bh / a.H, h = bh % a.H;
   const int kt_end = a.m.causal ? min(qt + 1, n_tiles) : n_tiles;
 
-  auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
-  const uint32_t bar_q = bar(0), bar_s = bar(1), bar_p = bar(2), bar_o = bar(3), bar_fin = bar(4),
-                 bar_sfree = bar(5);
-  auto bar_kf = [&](int s) { return bar(6 + s); };
-  auto bar_vf = [&](int s) { return bar(6 + NS + s); };
-  auto bar_ke = [&](int s) { return bar(6 + 2 * NS + s); };
-  auto bar_ve = [&](int s) { return bar(6 + 3 * NS + s); };
+  const FwdBars<NS> bars{sb + L::BAR};
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -300,38 +290,28 @@ __global__ void __launch_bounds__(192, 2)
     return;
   }
   const bool producer = (warp == 4 && lane == 0);
-  int nk = 0, nv = 0;
-  int kt_next = kt_end;
+  int nk = 0, nv = 0;  // producer lane: K and V copies issued
+  int kt_next = kt_end;  // producer lane: the next key tile to copy
+  auto next = [&](int kt) { return next_kept(a.m, b, h, qt, kt, kt_end); };
+  // K8_j (128 keys x D bytes) and Vt8_j (D rows x 128 keys) of key tile kt into stage st
+  auto load_k = [&](int st, int kt) {
+    mbar_arrive_expect_tx(bars.kf(st), L::TQ);
+    tma_load_3d(sb + L::K0 + st * L::TQ, &tmK, bars.kf(st), 0, kt * kT, bh);
+  };
+  auto load_v = [&](int st, int kt) {
+    mbar_arrive_expect_tx(bars.vf(st), L::TV);
+    tma_load_3d(sb + L::V0 + st * L::TV, &tmV, bars.vf(st), kt * kT, 0, bh);
+  };
   if (producer) {
-    mbar_init(bar_q, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, 4);
-    mbar_init(bar_o, 1);
-    mbar_init(bar_fin, 1);
-    mbar_init(bar_sfree, 4);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_kf(s), 1);
-      mbar_init(bar_vf(s), 1);
-      mbar_init(bar_ke(s), 1);
-      mbar_init(bar_ve(s), 1);
-    }
+    bars.init();
     *abort_cta = 0;
     fence_barrier_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    mbar_arrive_expect_tx(bar_q, L::TQ);
-    tma_load_3d(sb + L::Q, &tmQ, bar_q, 0, qt * kT, bh);
-    kt_next = next_kept(a.m, b, h, qt, 0, kt_end);
-    for (; kt_next < kt_end && nk < NS; kt_next = next_kept(a.m, b, h, qt, kt_next + 1, kt_end)) {
-      const int s = nk;
-      mbar_arrive_expect_tx(bar_kf(s), L::TQ);
-      tma_load_3d(sb + L::K0 + s * L::TQ, &tmK, bar_kf(s), 0, kt_next * kT, bh);
-      ++nk;
-      mbar_arrive_expect_tx(bar_vf(s), L::TV);
-      tma_load_3d(sb + L::V0 + s * L::TV, &tmV, bar_vf(s), kt_next * kT, 0, bh);
-      ++nv;
-    }
+    mbar_arrive_expect_tx(bars.q(), L::TQ);
+    tma_load_3d(sb + L::Q, &tmQ, bars.q(), 0, qt * kT, bh);
+    kt_next = fwd_produce(w, bars, next(0), kt_end, a.N, NS, nk, nv, next, load_k, load_v);
   }
   if (warp == 5) {
     tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
@@ -345,73 +325,32 @@ __global__ void __launch_bounds__(192, 2)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int kt = kt_next; kt < kt_end; kt = next_kept(a.m, b, h, qt, kt + 1, kt_end)) {
-        const int s = nk % NS;
-        const uint32_t ph = ((nk / NS) - 1) & 1;
-        if (nk >= NS && !mbar_wait(w, bar_ke(s), ph)) break;
-        mbar_arrive_expect_tx(bar_kf(s), L::TQ);
-        tma_load_3d(sb + L::K0 + s * L::TQ, &tmK, bar_kf(s), 0, kt * kT, bh);
-        ++nk;
-        if (nv >= NS && !mbar_wait(w, bar_ve(s), ph)) break;
-        mbar_arrive_expect_tx(bar_vf(s), L::TV);
-        tma_load_3d(sb + L::V0 + s * L::TV, &tmV, bar_vf(s), kt * kT, 0, bh);
-        ++nv;
-      }
-      mbar_drain(w, bar_q, 0);
-      for (int s = 0; s < NS; ++s) {
-        const int ck = (nk - s + NS - 1) / NS, cv = (nv - s + NS - 1) / NS;
-        if (ck > 0) mbar_drain(w, bar_kf(s), (ck - 1) & 1);
-        if (cv > 0) mbar_drain(w, bar_vf(s), (cv - 1) & 1);
-      }
+      if (kt_next >= 0) fwd_produce(w, bars, kt_next, kt_end, a.N, 1 << 30, nk, nv, next, load_k, load_v);
+      fwd_drain_copies(w, bars, nk, nv);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    {
-      constexpr uint32_t idS = idesc_e4m3(kT, kT);
-      constexpr uint32_t idO = idesc_e4m3(kT, D);
-      const uint32_t tS = tmem + L::T_S, tO = tmem + L::T_O;
-      const uint64_t dQ = desc_k<D>(sb + L::Q);
-      const uint64_t dK0 = desc_k<D>(sb + L::K0);
-      const uint64_t dV0 = desc_k<128>(sb + L::V0);
-      auto issue_s = [&](int it) -> bool {
-        const int s = it % NS;
-        if (!warp_wait(w, bar_kf(s), (it / NS) & 1)) return false;
-        tc_fence_after();
-        const uint64_t dK = dK0 + (uint64_t)((s * L::TQ) >> 4);
+    constexpr uint32_t idS = idesc_e4m3(kT, kT);
+    constexpr uint32_t idO = idesc_e4m3(kT, D);
+    const uint32_t tS = tmem + L::T_S, tO = tmem + L::T_O;
+    const uint64_t dQ = desc_k<D>(sb + L::Q);
+    const uint64_t dK0 = desc_k<D>(sb + L::K0);
+    const uint64_t dV0 = desc_k<128>(sb + L::V0);
+    fwd_mma_schedule<NS, L::PSEP>(
+        w, bars, next(0), kt_end, next,
+        [&](int st) {  // S = Q8 K8^T: D / 32 products of K = 32 bytes
+          const uint64_t dK = dK0 + (uint64_t)((st * L::TQ) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk)
-          mma_f8_ss(tS, dQ + (uint64_t)(kk * 2), dK + (uint64_t)(kk * 2), idS, kk > 0 ? 1u : 0u);
-        tc_commit_elect(bar_s);
-        tc_commit_elect(bar_ke(s));
-        return true;
-      };
-      bool ok = warp_wait(w, bar_q, 0);
-      int kt = next_kept(a.m, b, h, qt, 0, kt_end);
-      if (ok && kt < kt_end) ok = issue_s(0);
-      for (int it = 0; ok && kt < kt_end; ++it) {
-        const int s = it % NS;
-        const int kn = next_kept(a.m, b, h, qt, kt + 1, kt_end);
-        if (L::PSEP && kn < kt_end) {
-          if (!(ok = warp_wait(w, bar_sfree, it & 1))) break;
-          if (!(ok = issue_s(it + 1))) break;
-        }
-        if (!(ok = warp_wait(w, bar_p, it & 1))) break;
-        if (!(ok = warp_wait(w, bar_vf(s), (it / NS) & 1))) break;
-        tc_fence_after();
-        const uint64_t dV = dV0 + (uint64_t)((s * L::TV) >> 4);
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_f8_ss(tS, dQ + (uint64_t)(kk * 2), dK + (uint64_t)(kk * 2), idS, kk > 0 ? 1u : 0u);
+        },
+        [&](int st, int it) {  // O += Pq Vt8^T, Pq read from TMEM: 4 products of 32 keys
+          const uint64_t dV = dV0 + (uint64_t)((st * L::TV) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kT / 32; ++kk)
-          mma_f8_ts(tO, tmem + L::T_P + (uint32_t)kk * 8u, dV + (uint64_t)(kk * 2), idO,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit_elect(bar_o);
-        tc_commit_elect(bar_ve(s));
-        if (!L::PSEP && kn < kt_end && !(ok = issue_s(it + 1))) break;
-        kt = kn;
-      }
-      tc_commit_elect(bar_fin);
-      if (lane == 0) mbar_drain(w, bar_fin, 0);
-      __syncwarp();
-    }
+          for (int kk = 0; kk < kT / 32; ++kk)
+            mma_f8_ts(tO, tmem + L::T_P + (uint32_t)kk * 8u, dV + (uint64_t)(kk * 2), idO,
+                      (it > 0 || kk > 0) ? 1u : 0u);
+        });
   } else {
     // ------------------------------------------------------------ softmax
     const int r = threadIdx.x;
@@ -430,7 +369,7 @@ __global__ void __launch_bounds__(192, 2)
          kt = next_kept(a.m, b, h, qt, kt + 1, kt_end), ++it) {
       const float c2 = c2q * sk_h[kt];
       const float sv = sv_h[kt];
-      if (!(ok = warp_wait(w, bar_s, it & 1))) break;
+      if (!(ok = warp_wait(w, bars.s(), it & 1))) break;
       tc_fence_after();
       float s[kT];
       {
@@ -445,25 +384,14 @@ __global__ void __launch_bounds__(192, 2)
       if (L::PSEP) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree);
+        if (lane == 0) mbar_arrive(bars.sfree());
       }
-      const int k0 = kt * kT;
-      if (k0 + kT > a.N || (a.m.causal && kt == qt)) {
-        int lim = a.N - k0;
-        if (a.m.causal && kt == qt) lim = min(lim, row - k0 + 1);
+      mask_score_row(s, kt, qt, row, a.N, a.m.causal);
+      float m8[8];
 #pragma unroll
-        for (int c = 0; c < kT; ++c)
-          if (c >= lim) s[c] = -INFINITY;
-      }
-      float m4[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float mj = fmax3(s[32 * j], s[32 * j + 1], s[32 * j + 2]);
-#pragma unroll
-        for (int c = 3; c + 1 < 32; c += 2) mj = fmax3(mj, s[32 * j + c], s[32 * j + c + 1]);
-        m4[j] = fmaxf(mj, s[32 * j + 31]);
-      }
-      const float m_tile = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
+      for (int j = 0; j < 8; ++j) m8[j] = max16(s, j);
+      const float m_tile =
+          fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c2;
       const float m_new = fmaxf(m_use, m_tile);
       const float alpha = (m_new > m_use) ? ex2(m_use - m_new) : 1.f;  // 0 when m_use = -inf
       m_use = m_new;
@@ -483,70 +411,30 @@ __global__ void __launch_bounds__(192, 2)
         acc[(c >> 2) & 3] = fadd2(acc[(c >> 2) & 3], fadd2(f2pack(p0, p1), f2pack(p2, p3)));
         pc[c / 4] = pack4_e4m3(p0 * 256.f, p1 * 256.f, p2 * 256.f, p3 * 256.f);
       }
-      float sum0, sum1, sum2, sum3, sum4, sum5, sum6, sum7;
-      f2unpack(acc[0], sum0, sum1);
-      f2unpack(acc[1], sum2, sum3);
-      f2unpack(acc[2], sum4, sum5);
-      f2unpack(acc[3], sum6, sum7);
-      l = l * alpha + (((sum0 + sum1) + (sum2 + sum3)) + ((sum4 + sum5) + (sum6 + sum7)));
+      l = l * alpha + sum_packed4(acc);
       if (L::PSEP && it > 0) {
-        if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
+        if (!(ok = warp_wait(w, bars.o(), (it - 1) & 1))) break;
         tc_fence_after();
       }
       tmem_st32(tmem + L::T_P + lane_off, pc);
-      if (it > 0 && __any_sync(0xffffffffu, f != 1.f)) {
-        const uint64_t fp = f2pack(f, f);
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c0, o);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float y0, y1;
-            f2unpack(fmul2(f2pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), fp), y0, y1);
-            o[i] = __float_as_uint(y0);
-            o[i + 1] = __float_as_uint(y1);
-          }
-          tmem_st32(tO + c0, o);
-        }
-      }
+      if (it > 0 && __any_sync(0xffffffffu, f != 1.f)) scale_o_row<D>(tO, f);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
+      if (lane == 0) mbar_arrive(bars.p());
     }
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
     if (ok && it > 0) {
-      ok = warp_wait(w, bar_o, (it - 1) & 1);
+      ok = warp_wait(w, bars.o(), (it - 1) & 1);
       tc_fence_after();
       have_o = ok;
     }
     const float inv = (l > 0.f) ? unit / (256.f * l) : 0.f;
     const float lse = (l > 0.f) ? (m_use + __log2f(l)) * 0.693147180559945309f : -INFINITY;
     if (row < a.N && ok) a.LSE[(size_t)bh * a.N + row] = lse;
-    uint16_t* Orow = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      if (have_o) {
-        tmem_ld32(tO + c0, o);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
-      }
-      if (row < a.N && ok) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 q;
-          q.x = pack2<F16>(__uint_as_float(o[v * 8 + 0]) * inv, __uint_as_float(o[v * 8 + 1]) * inv);
-          q.y = pack2<F16>(__uint_as_float(o[v * 8 + 2]) * inv, __uint_as_float(o[v * 8 + 3]) * inv);
-          q.z = pack2<F16>(__uint_as_float(o[v * 8 + 4]) * inv, __uint_as_float(o[v * 8 + 5]) * inv);
-          q.w = pack2<F16>(__uint_as_float(o[v * 8 + 6]) * inv, __uint_as_float(o[v * 8 + 7]) * inv);
-          *reinterpret_cast<uint4*>(Orow + c0 + v * 8) = q;
-        }
-      }
-    }
+    store_o_row<D, F16>(tO, have_o, inv, row < a.N && ok,
+                        reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D);
   }
 
   tc_fence_before();

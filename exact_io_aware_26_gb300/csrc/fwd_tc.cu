@@ -38,8 +38,7 @@
 // issuer.  Tiles hidden by the causal rule or the block mask are never
 // loaded ("Le masquage causal ...": "jamais chargée et jamais calculée").
 #include "bwd_sched.cuh"
-#include "ptx.cuh"
-#include "tiles.cuh"
+#include "fwd_common.cuh"
 
 namespace fa {
 namespace {
@@ -54,11 +53,8 @@ struct FwdLayout {
   static constexpr uint32_t Q = 0;
   static constexpr uint32_t K0 = Q + TILE;          // K stage s at K0 + s * TILE
   static constexpr uint32_t V0 = K0 + NS * TILE;    // V stage s at V0 + s * TILE
-  static constexpr uint32_t BAR = V0 + NS * TILE;
-  // barriers: 0 q_full, 1 s_full, 2 p_full, 3 o_done, 4 fin, 5 s_free,
-  //           6.. k_full[NS], v_full[NS], k_empty[NS], v_empty[NS]
-  static constexpr uint32_t NBAR = 6 + 4 * NS;
-  static constexpr uint32_t TSLOT = BAR + NBAR * 8;
+  static constexpr uint32_t BAR = V0 + NS * TILE;  // FwdBars<NS>
+  static constexpr uint32_t TSLOT = BAR + FwdBars<NS>::kCount * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
   static constexpr uint32_t KBITS = ABORT + 4;  // the key tiles this query tile sees (block mask)
   // split launches: each row's (running max, sum) for the cluster's merge
@@ -103,13 +99,7 @@ __global__ void __launch_bounds__(192, 2)
   const int kt_begin = split * a.split_tiles;
   int kt_end = min(a.m.causal ? min(qt + 1, n_tiles) : n_tiles, kt_begin + a.split_tiles);
 
-  auto bar = [&](int i) { return sb + L::BAR + 8u * (uint32_t)i; };
-  const uint32_t bar_q = bar(0), bar_s = bar(1), bar_p = bar(2), bar_o = bar(3), bar_fin = bar(4),
-                 bar_sfree = bar(5);
-  auto bar_kf = [&](int s) { return bar(6 + s); };
-  auto bar_vf = [&](int s) { return bar(6 + NS + s); };
-  auto bar_ke = [&](int s) { return bar(6 + 2 * NS + s); };
-  auto bar_ve = [&](int s) { return bar(6 + 3 * NS + s); };
+  const FwdBars<NS> bars{sb + L::BAR};
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + L::ABORT);
   const WaitCtx w{abort_cta, a.rep.st, a.rep.epoch, a.rep.wait_ns};
 
@@ -132,42 +122,29 @@ __global__ void __launch_bounds__(192, 2)
   const bool producer = (warp == 4 && lane == 0);
   int nk = 0, nv = 0;  // producer lane: K and V copies issued
   int kt_next = kt_end;  // producer lane: the next key tile to copy
+  // K_j, V_j of key tile kt into ring stage st: D / 64 boxes of 64 columns each
+  auto load_k = [&](int st, int kt) {
+    mbar_arrive_expect_tx(bars.kf(st), L::TILE);
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_3d(sb + L::K0 + st * L::TILE + c * (kTile * 128), &tmK, bars.kf(st), c * 64, kt * kTile, bh);
+  };
+  auto load_v = [&](int st, int kt) {
+    mbar_arrive_expect_tx(bars.vf(st), L::TILE);
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_3d(sb + L::V0 + st * L::TILE + c * (kTile * 128), &tmV, bars.vf(st), c * 64, kt * kTile, bh);
+  };
   if (producer) {
-    mbar_init(bar_q, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, 4);
-    mbar_init(bar_o, 1);
-    mbar_init(bar_fin, 1);
-    mbar_init(bar_sfree, 4);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_kf(s), 1);
-      mbar_init(bar_vf(s), 1);
-      mbar_init(bar_ke(s), 1);
-      mbar_init(bar_ve(s), 1);
-    }
+    bars.init();
     *abort_cta = 0;
     fence_barrier_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    mbar_arrive_expect_tx(bar_q, L::TILE);
+    mbar_arrive_expect_tx(bars.q(), L::TILE);
     for (int c = 0; c < D / 64; ++c)
-      tma_load_3d(sb + L::Q + c * (kTile * 128), &tmQ, bar_q, c * 64, qt * kTile, bh);
-    kt_next = next_kept(a.m, b, h, qt, kt_begin, kt_end);
-    for (; kt_next < kt_end && nk < NS; kt_next = next_kept(a.m, b, h, qt, kt_next + 1, kt_end)) {
-      if (!dbg_check(w, kt_next >= 0 && kt_next * kTile < a.N)) break;
-      const int s = nk;
-      mbar_arrive_expect_tx(bar_kf(s), L::TILE);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sb + L::K0 + s * L::TILE + c * (kTile * 128), &tmK, bar_kf(s), c * 64,
-                    kt_next * kTile, bh);
-      ++nk;
-      mbar_arrive_expect_tx(bar_vf(s), L::TILE);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sb + L::V0 + s * L::TILE + c * (kTile * 128), &tmV, bar_vf(s), c * 64,
-                    kt_next * kTile, bh);
-      ++nv;
-    }
+      tma_load_3d(sb + L::Q + c * (kTile * 128), &tmQ, bars.q(), c * 64, qt * kTile, bh);
+    kt_next = fwd_produce(w, bars, next_kept(a.m, b, h, qt, kt_begin, kt_end), kt_end, a.N, NS, nk, nv,
+                          [&](int kt) { return next_kept(a.m, b, h, qt, kt, kt_end); }, load_k, load_v);
   }
   // block mask (its own instantiation, MASKED, so that launches without one run
   // unchanged code): this query tile's row of kept key tiles as bits in shared memory
@@ -195,87 +172,33 @@ __global__ void __launch_bounds__(192, 2)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       // the rest of the K, V tiles, each into a stage once it is released
-      for (int kt = kt_next; kt < kt_end; kt = next_k(kt + 1)) {
-        if (!dbg_check(w, kt >= 0 && kt * kTile < a.N)) break;
-        const int s = nk % NS;
-        const uint32_t ph = ((nk / NS) - 1) & 1;
-        if (nk >= NS && !mbar_wait(w, bar_ke(s), ph)) break;
-        mbar_arrive_expect_tx(bar_kf(s), L::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sb + L::K0 + s * L::TILE + c * (kTile * 128), &tmK, bar_kf(s), c * 64,
-                      kt * kTile, bh);
-        ++nk;
-        if (nv >= NS && !mbar_wait(w, bar_ve(s), ph)) break;
-        mbar_arrive_expect_tx(bar_vf(s), L::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sb + L::V0 + s * L::TILE + c * (kTile * 128), &tmV, bar_vf(s), c * 64,
-                      kt * kTile, bh);
-        ++nv;
-      }
-      // every copy issued must have landed before the CTA may exit
-      mbar_drain(w, bar_q, 0);
-      for (int s = 0; s < NS; ++s) {
-        const int ck = (nk - s + NS - 1) / NS, cv = (nv - s + NS - 1) / NS;  // copies into stage s
-        if (ck > 0) mbar_drain(w, bar_kf(s), (ck - 1) & 1);
-        if (cv > 0) mbar_drain(w, bar_vf(s), (cv - 1) & 1);
-      }
+      if (kt_next >= 0) fwd_produce(w, bars, kt_next, kt_end, a.N, 1 << 30, nk, nv, next_k, load_k, load_v);
+      fwd_drain_copies(w, bars, nk, nv);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop converged (waits are warp-uniform); one
-    // elected lane issues each MMA and commit.
-    {
-      constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);
-      constexpr uint32_t idO = idesc_f16(F16, kTile, D, false, true);
-      const uint32_t tS = tmem + L::T_S, tO = tmem + L::T_O;
-      const uint64_t dQ = desc_kmajor_base(sb + L::Q);
-      const uint64_t dK0 = desc_kmajor_base(sb + L::K0);
-      const uint64_t dV0 = desc_mnmajor_base(sb + L::V0, kTile);
-      auto issue_s = [&](int it) -> bool {
-        const int s = it % NS;
-        if (!warp_wait(w, bar_kf(s), (it / NS) & 1)) return false;
-        tc_fence_after();
-        const uint64_t dK = desc_add(dK0, (uint32_t)s * L::TILE);
+    constexpr uint32_t idS = idesc_f16(F16, kTile, kTile, false, false);
+    constexpr uint32_t idO = idesc_f16(F16, kTile, D, false, true);
+    const uint32_t tS = tmem + L::T_S, tO = tmem + L::T_O;
+    const uint64_t dQ = desc_kmajor_base(sb + L::Q);
+    const uint64_t dK0 = desc_kmajor_base(sb + L::K0);
+    const uint64_t dV0 = desc_mnmajor_base(sb + L::V0, kTile);
+    fwd_mma_schedule<NS, L::PSEP>(
+        w, bars, next_k(kt_begin), kt_end, next_k,
+        [&](int st) {  // S = Q K^T: D / 16 products of K = 16
+          const uint64_t dK = desc_add(dK0, (uint32_t)st * L::TILE);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_elect(tS, dQ + kmajor_step(kk, kTile), dK + kmajor_step(kk, kTile), idS,
-                          kk > 0 ? 1u : 0u);
-        tc_commit_elect(bar_s);
-        tc_commit_elect(bar_ke(s));
-        return true;
-      };
-      bool ok = warp_wait(w, bar_q, 0);
-      int kt = next_k(kt_begin);
-      if (ok && kt < kt_end) ok = issue_s(0);
-      for (int it = 0; ok && kt < kt_end; ++it) {
-        const int s = it % NS;
-        const int kn = next_k(kt + 1);
-        // d = 64: S_{j+1} as soon as the softmax has copied S_j out of TMEM
-        if (L::PSEP && kn < kt_end) {
-          if (!(ok = warp_wait(w, bar_sfree, it & 1))) break;
-          if (!(ok = issue_s(it + 1))) break;
-        }
-        // P~ V_j, with P~ read from TMEM
-        if (!(ok = warp_wait(w, bar_p, it & 1))) break;
-        if (!(ok = warp_wait(w, bar_vf(s), (it / NS) & 1))) break;
-        tc_fence_after();
-        const uint64_t dV = desc_add(dV0, (uint32_t)s * L::TILE);
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss_elect(tS, dQ + kmajor_step(kk, kTile), dK + kmajor_step(kk, kTile), idS,
+                            kk > 0 ? 1u : 0u);
+        },
+        [&](int st, int it) {  // O += P~ V, P~ read from TMEM: 8 products of K = 16 keys
+          const uint64_t dV = desc_add(dV0, (uint32_t)st * L::TILE);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ts_elect(tO, tmem + L::T_P + (uint32_t)kk * 8u, dV + mnmajor_step(kk), idO,
-                          (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit_elect(bar_o);
-        tc_commit_elect(bar_ve(s));
-        // d = 128: the next score tile goes into the columns P~ V_j reads; MMAs
-        // of one thread execute in issue order, so it lands after they are read
-        if (!L::PSEP && kn < kt_end && !(ok = issue_s(it + 1))) break;
-        kt = kn;
-      }
-      // every MMA issued must have completed before TMEM is released
-      tc_commit_elect(bar_fin);
-      if (lane == 0) mbar_drain(w, bar_fin, 0);
-      __syncwarp();
-    }
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            tc_mma_ts_elect(tO, tmem + L::T_P + (uint32_t)kk * 8u, dV + mnmajor_step(kk), idO,
+                            (it > 0 || kk > 0) ? 1u : 0u);
+        });
   } else {
     // ------------------------------------------------------------ softmax
     const int r = threadIdx.x;  // query row in the tile = TMEM lane
@@ -305,7 +228,7 @@ __global__ void __launch_bounds__(192, 2)
           for (int i = 0; i < 4; ++i) kb[i] = (w4 == i) ? bits : kb[i];
         }
       }
-      if (!(ok = warp_wait(w, bar_s, it & 1))) break;
+      if (!(ok = warp_wait(w, bars.s(), it & 1))) break;
       tc_fence_after();
       float s[kTile];
       float m8[8];
@@ -316,12 +239,7 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
         for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // maxima of the first half while the second half arrives
-          float mj = fmax3(s[16 * j], s[16 * j + 1], s[16 * j + 2]);
-#pragma unroll
-          for (int c = 3; c + 1 < 16; c += 2) mj = fmax3(mj, s[16 * j + c], s[16 * j + c + 1]);
-          m8[j] = fmaxf(mj, s[16 * j + 15]);
-        }
+        for (int j = 0; j < 4; ++j) m8[j] = max16(s, j);  // the first half's maxima while the second half arrives
         tmem_wait_ld64(v);
 #pragma unroll
         for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(v[c]);
@@ -329,39 +247,18 @@ __global__ void __launch_bounds__(192, 2)
       if (L::PSEP) {  // S_j is in registers: the MMA warp may compute S_{j+1}
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree);
-      }
-      // hide keys past the end of the sequence and, on the diagonal tile,
-      // keys after the query ("Le masquage causal")
-      const int k0 = kt * kTile;
-      if (k0 + kTile > a.N || (a.m.causal && kt == qt)) {
-        int lim = a.N - k0;
-        if (a.m.causal && kt == qt) lim = min(lim, row - k0 + 1);
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (c >= lim) s[c] = -INFINITY;
+        if (lane == 0) mbar_arrive(bars.sfree());
       }
       // the rest of the row max as four more independent chains of sixteen (eight
       // chains keep the dependent-max latency short: only two softmax warps share
       // an SM sub-partition); on a tile that masks keys the first four are redone
       // on the masked values
-      const bool masked_tile = kt * kTile + kTile > a.N || (a.m.causal && kt == qt);
-      if (masked_tile) {
+      if (mask_score_row(s, kt, qt, row, a.N, a.m.causal)) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float mj = fmax3(s[16 * j], s[16 * j + 1], s[16 * j + 2]);
-#pragma unroll
-          for (int c = 3; c + 1 < 16; c += 2) mj = fmax3(mj, s[16 * j + c], s[16 * j + c + 1]);
-          m8[j] = fmaxf(mj, s[16 * j + 15]);
-        }
+        for (int j = 0; j < 4; ++j) m8[j] = max16(s, j);
       }
 #pragma unroll
-      for (int j = 4; j < 8; ++j) {
-        float mj = fmax3(s[16 * j], s[16 * j + 1], s[16 * j + 2]);
-#pragma unroll
-        for (int c = 3; c + 1 < 16; c += 2) mj = fmax3(mj, s[16 * j + c], s[16 * j + c + 1]);
-        m8[j] = fmaxf(mj, s[16 * j + 15]);
-      }
+      for (int j = 4; j < 8; ++j) m8[j] = max16(s, j);
       const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float m_tile = mx * c2;
       float alpha = 1.f;
@@ -394,7 +291,7 @@ __global__ void __launch_bounds__(192, 2)
         }
         if (!o_ready) {
           // P~ V_{j-1} must be done: it reads the P~ columns and writes O
-          if (!(ok = warp_wait(w, bar_o, (it - 1) & 1))) break;
+          if (!(ok = warp_wait(w, bars.o(), (it - 1) & 1))) break;
           tc_fence_after();
           o_ready = true;
         }
@@ -403,32 +300,12 @@ __global__ void __launch_bounds__(192, 2)
         tmem_st16(tmem + L::T_P + lane_off + 16 * ch, pk);
       }
       if (!ok) break;
-      float sum0, sum1, sum2, sum3, sum4, sum5, sum6, sum7;
-      f2unpack(acc[0], sum0, sum1);
-      f2unpack(acc[1], sum2, sum3);
-      f2unpack(acc[2], sum4, sum5);
-      f2unpack(acc[3], sum6, sum7);
-      l = l * alpha + (((sum0 + sum1) + (sum2 + sum3)) + ((sum4 + sum5) + (sum6 + sum7)));
-      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const uint64_t ap = f2pack(alpha, alpha);
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c0, o);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float y0, y1;
-            f2unpack(fmul2(f2pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ap), y0, y1);
-            o[i] = __float_as_uint(y0);
-            o[i + 1] = __float_as_uint(y1);
-          }
-          tmem_st32(tO + c0, o);
-        }
-      }
+      l = l * alpha + sum_packed4(acc);
+      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) scale_o_row<D>(tO, alpha);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
+      if (lane == 0) mbar_arrive(bars.p());
     }
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
@@ -436,7 +313,7 @@ __global__ void __launch_bounds__(192, 2)
       // the o_done barrier is at most one phase behind the last P~ V: at d = 64
       // the loop waited every earlier phase, at d = 128 each earlier P~ V
       // completed before the next S did
-      ok = warp_wait(w, bar_o, (it - 1) & 1);
+      ok = warp_wait(w, bars.o(), (it - 1) & 1);
       tc_fence_after();
       have_o = ok;
     }
@@ -446,28 +323,8 @@ __global__ void __launch_bounds__(192, 2)
     if (row < a.N && ok) ok = dbg_check(w, (size_t)bh * a.N + row < (size_t)BH * a.N);
     if constexpr (!SPLIT) {
       if (row < a.N && ok) a.LSE[(size_t)bh * a.N + row] = lse;
-      uint16_t* Orow = reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        if (have_o) {
-          tmem_ld32(tO + c0, o);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        if (row < a.N && ok) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 q;
-            q.x = pack2<F16>(__uint_as_float(o[v * 8 + 0]) * inv_l, __uint_as_float(o[v * 8 + 1]) * inv_l);
-            q.y = pack2<F16>(__uint_as_float(o[v * 8 + 2]) * inv_l, __uint_as_float(o[v * 8 + 3]) * inv_l);
-            q.z = pack2<F16>(__uint_as_float(o[v * 8 + 4]) * inv_l, __uint_as_float(o[v * 8 + 5]) * inv_l);
-            q.w = pack2<F16>(__uint_as_float(o[v * 8 + 6]) * inv_l, __uint_as_float(o[v * 8 + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(Orow + c0 + v * 8) = q;
-          }
-        }
-      }
+      store_o_row<D, F16>(tO, have_o, inv_l, row < a.N && ok,
+                          reinterpret_cast<uint16_t*>(a.O) + ((size_t)bh * a.N + row) * D);
     } else {
       // a slice of the key range: the cluster merges the slices below
       m_fin = m_use;
