@@ -284,7 +284,8 @@ def run_reference(args, w, rank):
 
 KERNEL_SOURCES = {"bwd_main": ("bwd_tc.cu", "ptx.cuh", "internal.h", "bwd_sched.cuh", "tiles.cuh"),
                   "fwd": ("fwd_tc.cu", "fwd_common.cuh", "ptx.cuh", "internal.h", "bwd_sched.cuh", "tiles.cuh"),
-                  "fwd_fp8": ("fwd_fp8.cu", "fwd_common.cuh", "fp8.h", "ptx.cuh", "internal.h", "tiles.cuh")}
+                  "fwd_fp8": ("fwd_fp8.cu", "fwd_common.cuh", "fp8.h", "ptx.cuh", "internal.h", "bwd_sched.cuh",
+                              "tiles.cuh")}
 TRAFFIC_KEY = {"main": "bwd_main", "fwd": "fwd", "fwd_fp8": "fwd_fp8", "bwd_main": "bwd_main"}
 
 

@@ -139,9 +139,9 @@ long long device_l2_bytes() {
 struct HeadOrder {
   int group, tail;
 };
-HeadOrder head_order(const fa_params* p, bool backward) {
-  const long long e = p->dtype == FA_F32 ? 4 : 2;
-  const long long per_head = backward ? (long long)p->N * p->d * (2 * e + 4) : (long long)p->N * p->d * 2 * e;
+// per_head: the streamed bytes of one head (forward: K and V; backward: Q, dO and
+// the fp32 dQ accumulator)
+HeadOrder head_order_bytes(const fa_params* p, long long per_head, bool backward) {
   const long long bh = (long long)p->B * p->H;
   const long long l2 = device_l2_bytes();
   const long long budget = backward ? l2 / 2 : l2 * 3 / 4;
@@ -149,6 +149,11 @@ HeadOrder head_order(const fa_params* p, bool backward) {
   long long tail = p->causal ? budget / per_head : 0;
   if (tail < 2) tail = 0;
   return {1, (int)tail};
+}
+HeadOrder head_order(const fa_params* p, bool backward) {
+  const long long e = p->dtype == FA_F32 ? 4 : 2;
+  const long long nd = (long long)p->N * p->d;
+  return head_order_bytes(p, backward ? nd * (2 * e + 4) : nd * 2 * e, backward);
 }
 
 Report make_report(DevStatus* st) {
@@ -470,6 +475,10 @@ fa_status fa_fwd_fp8(const fa_params* p, const void* q8, const void* k8, const v
   a.sv = sv;
   a.O = O;
   a.LSE = LSE;
+  // the FP8 K and V: one byte per element
+  const HeadOrder ho = head_order_bytes(p, 2LL * p->N * p->d, false);
+  a.head_group = ho.group;
+  a.head_tail = ho.tail;
   a.rep = make_report(st);
   const cudaError_t e = launch_fwd_fp8(a, p->d, p->dtype == FA_F16, tm, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "FP8 forward launch");

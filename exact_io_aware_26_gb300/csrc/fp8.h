@@ -33,6 +33,10 @@ struct Fp8FwdArgs {
   const float* sv;
   void* O;     // [B*H][N][d], 16-bit
   float* LSE;  // [B*H][N]
+  // grid order, as in the 16-bit forward: heads in groups of head_group, query-
+  // tile-major within a group, the last head_tail heads one more group
+  int head_group;
+  int head_tail;
   Report rep;
 };
 

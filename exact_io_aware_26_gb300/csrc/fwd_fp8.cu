@@ -16,7 +16,8 @@
 //
 // fwd_fp8_kernel: the schedule of the 16-bit forward (warps 0-3 softmax, one
 // query row per thread; warp 4 TMA producer with a two-stage K/V ring; warp 5
-// TMEM owner and MMA issuer; two CTAs per SM), with
+// TMEM owner and MMA issuer; two CTAs per SM; the same grid order over heads and
+// the same block-mask bitmask), with
 //   S   = Q8 K8^T              tcgen05.mma kind::f8f6f4 (e4m3 x e4m3, f32 in TMEM)
 //   s   = S * scale * sigma_q * sigma_k,j   (powers of two: exact)
 //   P~  = exp(s - m) against the exact running max m, so that P~ <= 1,
@@ -29,6 +30,7 @@
 // rows are 64 bytes (64-byte swizzle); with d = 128 they are 128 bytes (128-byte
 // swizzle).  P~ has TMEM columns of its own at d = 64; at d = 128 it overwrites
 // S and the schedule is serial, as in the 16-bit kernel.
+#include "bwd_sched.cuh"
 #include "fp8.h"
 #include "fwd_common.cuh"
 
@@ -256,7 +258,8 @@ struct F8Layout {
   static constexpr uint32_t BAR = V0 + NS * TV;  // FwdBars<NS>
   static constexpr uint32_t TSLOT = BAR + FwdBars<NS>::kCount * 8;
   static constexpr uint32_t ABORT = TSLOT + 4;
-  static constexpr uint32_t BYTES = ABORT + 4;
+  static constexpr uint32_t KBITS = ABORT + 4;  // the key tiles this query tile sees (block mask)
+  static constexpr uint32_t BYTES = KBITS + kMaskBitBytes;
   // TMEM (256 columns): S [0, 128), O [128, 128 + D); the e4m3 P~ (128 keys, four
   // per column) at [192, 224) for d = 64, over the first 32 columns of S for d = 128
   static constexpr uint32_t TMEM_COLS = 256;
@@ -264,7 +267,7 @@ struct F8Layout {
   static constexpr uint32_t T_S = 0, T_O = 128, T_P = PSEP ? 192 : 0;
 };
 
-template <int D, bool F16>
+template <int D, bool F16, bool MASKED>
 __global__ void __launch_bounds__(192, 2)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Fp8FwdArgs a) {
@@ -276,8 +279,11 @@ __global__ void __launch_bounds__(192, 2)
 
   const int BH = a.B * a.H;
   const int n_tiles = a.T;
-  const int qt = n_tiles - 1 - (int)blockIdx.x / BH;  // heaviest (causal) tiles first
-  const int bh = (int)blockIdx.x % BH;
+  // heads in groups of head_group; within a group the heaviest (causal) query
+  // tiles of all its heads first
+  int qt, bh;
+  group_order((int)blockIdx.x, n_tiles, BH, a.head_group, a.head_tail, qt, bh);
+  qt = n_tiles - 1 - qt;
   const int b = bh / a.H, h = bh % a.H;
   const int kt_end = a.m.causal ? min(qt + 1, n_tiles) : n_tiles;
 
@@ -292,7 +298,9 @@ __global__ void __launch_bounds__(192, 2)
   const bool producer = (warp == 4 && lane == 0);
   int nk = 0, nv = 0;  // producer lane: K and V copies issued
   int kt_next = kt_end;  // producer lane: the next key tile to copy
-  auto next = [&](int kt) { return next_kept(a.m, b, h, qt, kt, kt_end); };
+  // the next kept key tile at or after kt, from the mask in device memory (the
+  // producer's first copies, before the setup barrier) ...
+  auto next_mem = [&](int kt) { return next_kept(a.m, b, h, qt, kt, kt_end); };
   // K8_j (128 keys x D bytes) and Vt8_j (D rows x 128 keys) of key tile kt into stage st
   auto load_k = [&](int st, int kt) {
     mbar_arrive_expect_tx(bars.kf(st), L::TQ);
@@ -311,14 +319,22 @@ __global__ void __launch_bounds__(192, 2)
     prefetch_tmap(&tmV);
     mbar_arrive_expect_tx(bars.q(), L::TQ);
     tma_load_3d(sb + L::Q, &tmQ, bars.q(), 0, qt * kT, bh);
-    kt_next = fwd_produce(w, bars, next(0), kt_end, a.N, NS, nk, nv, next, load_k, load_v);
+    kt_next = fwd_produce(w, bars, next_mem(0), kt_end, a.N, NS, nk, nv, next_mem, load_k, load_v);
   }
+  // block mask (its own instantiation, MASKED): this query tile's row of kept key
+  // tiles as bits in shared memory
+  uint32_t* kbits = reinterpret_cast<uint32_t*>(smem + L::KBITS);
+  const bool use_bits = MASKED && n_tiles <= kMaskBits;
+  if (use_bits)
+    build_tile_bits(kbits, n_tiles, warp, 6, lane, [&](int t) { return tile_kept(a.m, b, h, qt, t); });
   if (warp == 5) {
     tmem_alloc(sb + L::TSLOT, L::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
+  // ... and from the bitmask after the setup barrier
+  auto next = [&](int kt) { return use_bits ? next_bit(kbits, kt, kt_end) : next_mem(kt); };
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
 
@@ -365,8 +381,7 @@ __global__ void __launch_bounds__(192, 2)
     float unit = 0.f;         // O is held in units of this V scale
     bool ok = true;
     int it = 0;
-    for (int kt = next_kept(a.m, b, h, qt, 0, kt_end); kt < kt_end;
-         kt = next_kept(a.m, b, h, qt, kt + 1, kt_end), ++it) {
+    for (int kt = next(0); kt < kt_end; kt = next(kt + 1), ++it) {
       const float c2 = c2q * sk_h[kt];
       const float sv = sv_h[kt];
       if (!(ok = warp_wait(w, bars.s(), it & 1))) break;
@@ -455,7 +470,8 @@ cudaError_t quant_t(const Fp8QuantArgs& a, cudaStream_t s) {
 template <int D, bool F16>
 cudaError_t fwd_t(const Fp8FwdArgs& a, const CUtensorMap* tm, cudaStream_t s) {
   using L = F8Layout<D>;
-  auto kern = fwd_fp8_kernel<D, F16>;
+  // the block-mask bitmask is its own instantiation
+  auto kern = a.m.mask ? fwd_fp8_kernel<D, F16, true> : fwd_fp8_kernel<D, F16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(a.T * a.B * a.H);

@@ -199,3 +199,29 @@ def test_full_size_workload_two_heads(cuda_lib, causal):
         _compare_quantized(t_head, t_ref, ref, sg64, w.N, w.d)
         O_ref, L_ref = oracle.fp8_attention_fwd(t_ref, w.scale, causal=causal)
         check_fwd(O[b:b + 1, h:h + 1], L[b:b + 1, h:h + 1], O_ref, L_ref, "bf16")
+
+
+@pytest.mark.parametrize("causal,masked", [(True, False), (False, True)])
+def test_head_order_of_a_problem_larger_than_l2(cuda_lib, causal, masked):
+    """B2 H16 N16384 d128 (the block-sparse workload's shape): its FP8 K and V (134 MB)
+    exceed three quarters of L2, so the launch runs head by head (causal: its last heads
+    as one more group).  Every (query tile, head) must be computed once, with its own
+    coordinates: O and LSE equal, bit for bit, those of the same kernel run one head at a
+    time (whose K, V fit)."""
+    B, H, N, d = 2, 16, 16384, 128
+    g = torch.Generator().manual_seed(2024)
+    q, k, v = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).cuda() for _ in range(3))
+    t = fa.fp8_quantize(q, k, v, synth.rotation_signs(d, 3).cuda())
+    m = None
+    if masked:
+        m = torch.from_numpy(synth.block_mask(np.random.Generator(np.random.PCG64(5)), N, 128, 0.25)).cuda()
+    scale = 1.0 / math.sqrt(d)
+    O, L = fa.attention_fwd_fp8_codes(t, scale, causal=causal, block_mask=m, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fa.get_status() == fa.FA_OK
+    for b, h in ((0, 0), (0, 9), (1, 4), (1, 15)):
+        th = {n: t[n][b:b + 1, h:h + 1].contiguous() for n in t}
+        Oh, Lh = fa.attention_fwd_fp8_codes(th, scale, causal=causal, block_mask=m, dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        assert fa.get_status() == fa.FA_OK
+        assert torch.equal(O[b, h], Oh[0, 0]) and torch.equal(L[b, h], Lh[0, 0]), (b, h)
