@@ -87,16 +87,17 @@ def test_bwd_sliced_and_whole_key_tile_paths_agree(cuda_lib, causal):
             assert rel_fro(g, g0) <= 2e-3
 
 
-@pytest.mark.parametrize("n_tiles,extra", [(16, 8), (16, 24), (16, 72), (8, 8), (5, 3), (16, 100)])
-def test_bwd_last_partial_wave_split(cuda_lib, n_tiles, extra):
-    """Non-causal d = 64 grids of SMs + `extra` key tiles (one partly filled last
-    wave): the leftover key tiles are split over the idle SMs (2 to 8 slices of
-    their query tiles, fp32 partial dK, dV added up by the finalize stage; with
-    100 left over no split fits).  The last query tile is ragged."""
+@pytest.mark.parametrize("d,n_tiles,extra", [(64, 16, 8), (64, 16, 24), (64, 16, 72), (64, 8, 8), (64, 5, 3),
+                                             (64, 16, 100), (128, 16, 8), (128, 6, 20)])
+def test_bwd_last_partial_wave_split(cuda_lib, d, n_tiles, extra):
+    """Non-causal grids of SMs + `extra` key tiles (one partly filled last wave): the
+    leftover key tiles are split over the idle SMs (2 to 8 slices of their query
+    tiles, fp32 partial dK, dV added up by the finalize stage; with 100 left over no
+    split fits).  The last query tile is ragged."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     H = -(-(sms + extra) // n_tiles)  # key tiles = H * n_tiles, just past sms + extra
     N = 128 * n_tiles - 37
-    inp = synth.make_inputs(1, H, N, 64, "bf16", seed=4500 + n_tiles + extra)
+    inp = synth.make_inputs(1, H, N, d, "bf16", seed=4500 + n_tiles + extra + d)
     got = _run(inp, False, guard=True)
     check_grads(got, _ref(inp, False), "bf16")
 
