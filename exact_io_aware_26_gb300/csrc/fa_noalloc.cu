@@ -74,7 +74,7 @@ extern "C" fa_status fa_bwd_noalloc(const fa_params* p, const void* Q, const voi
   if ((s = scratch_address(&scratch)) != FA_OK) return s;
   // fa_bwd's first stage rewrites D and zeroes the dQ accumulator before the
   // main kernel reads either, and the main stage stores every partial-sum slot
-  // of a shared key tile in full before the finalize stage reads it (no slot is
+  // of a sliced key tile in full before the finalize stage reads it (no slot is
   // accumulated into), so the array's previous contents never matter
   return fa_bwd(p, Q, K, V, O, dO, LSE, dQ, dK, dV, scratch, (size_t)FA_NOALLOC_SCRATCH_BYTES,
                 stream);

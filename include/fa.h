@@ -249,7 +249,7 @@ int fa_set_bwd_ctas(int n);
  * Every call, on every stream, shares the one array: calls that can overlap on
  * the GPU race on it and must be serialised by the caller.  Each call rewrites
  * all the scratch it reads: D and the dQ accumulator (zeroed first) in the first
- * stage, and the fp32 partial-sum slots of key tiles that several CTAs share,
+ * stage, and the fp32 partial-sum slots of key tiles cut into several slices,
  * each stored in full by the main stage before the finalize stage reads it.  So
  * nothing left by an earlier call affects a call's results.
  */
