@@ -28,6 +28,10 @@
 // read dQ_i out of TMEM and reduce it into the fp32 accumulator.  More compute warps per SM
 // sub-partition hide more of the TMEM, shared-memory and barrier latencies of
 // the elementwise steps, which (with one CTA per SM) bound the loop.
+//
+// Grids that would leave SMs idle run the same kernel on slices of key tiles'
+// query ranges (a separate instantiation, QS; bwd_sched.cuh): a key tile of
+// several slices gets fp32 partial dK, dV sums that the finalize kernel adds up.
 #include "bwd_sched.cuh"
 #include "ptx.cuh"
 #include "tiles.cuh"

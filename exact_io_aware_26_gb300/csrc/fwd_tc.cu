@@ -22,9 +22,13 @@
 // At d = 64 P~ has TMEM columns of its own, so S_{j+1} is computed while the
 // softmax of tile j runs; at d = 128 P~ overwrites S and the schedule is
 // serial (S_j, softmax, P~V_j, S_{j+1}).  Two CTAs share each SM (256 TMEM
-// columns and at most 97 KiB of shared memory each), so one CTA's
+// columns and at most 100 KiB of shared memory each), so one CTA's
 // exponentials run on the CUDA cores while the other's MMAs run on the tensor
 // core ("FA3 : Mécanique de la trémie", point 2, realised across CTAs).
+//
+// Split-KV (a separate instantiation, SPLIT): the key range of a query tile is
+// cut into slices run by the CTAs of one thread-block cluster, which merge
+// their running statistics and partial O through distributed shared memory.
 //
 // Dropout (a separate instantiation): after the exponentials of a tile, each
 // weight whose 16-bit Philox4x32-10 draw is below the threshold is replaced by 0 and
