@@ -289,12 +289,37 @@ KERNEL_SOURCES = {"bwd_main": ("bwd_tc.cu", "ptx.cuh", "internal.h", "bwd_sched.
 TRAFFIC_KEY = {"main": "bwd_main", "fwd": "fwd", "fwd_fp8": "fwd_fp8", "bwd_main": "bwd_main"}
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank space (string and character
+    literals kept as they are): what the compiler sees of the code."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":  # a literal: copy it up to its closing quote
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest(kernel: str = "bwd_main") -> str:
-    """Digest of the sources a kernel is built from."""
+    """Digest of the code a kernel is built from (its sources without comments, so
+    that a change to the notes alone keeps the recorded counters)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "exact_io_aware_26_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "exact_io_aware_26_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
