@@ -7,6 +7,7 @@ pass (status FA_OK), and the results must be those of the release build and agre
 the fp64 oracle."""
 import math
 
+import numpy as np
 import pytest
 import torch
 
@@ -70,6 +71,28 @@ def test_debug_build_checks_pass_and_results_match(debug_lib, B, H, N, d, causal
     O, L, g = _ref(inp, causal, inp["mask"])
     check_fwd(o, lse, O, L, "bf16")
     check_grads(grads, g, "bf16")
+
+
+@pytest.mark.parametrize("d,causal,mask_p", [(64, True, None), (128, False, 0.4)])
+def test_debug_build_fp8_forward(debug_lib, d, causal, mask_p):
+    """The FP8 quantiser and forward (head order, block-mask bitmask) under the debug
+    build: every check passes and the result agrees with the oracle's FP8 forward on
+    the oracle's own codes."""
+    B, H, N = 1, 2, 700
+    inp = synth.make_inputs(B, H, N, d, "bf16", seed=7300 + d, mask_p=mask_p, backward=False)
+    o = oracle_inputs(inp)
+    signs = synth.rotation_signs(d, 4)
+    t_ref = oracle.fp8_quantize(o["q"], o["k"], o["v"], signs.double().numpy())
+    t = {n: torch.from_numpy(np.ascontiguousarray(t_ref[n])).cuda() for n in ("q8", "k8", "vt8")}
+    t.update({n: torch.from_numpy(np.ascontiguousarray(t_ref[n])).to("cuda", torch.float32)
+              for n in ("sq", "sk", "sv")})
+    m = None if inp["mask"] is None else torch.as_tensor(inp["mask"]).cuda()
+    scale = 1.0 / math.sqrt(d)
+    O, L = fa.attention_fwd_fp8_codes(t, scale, causal=causal, block_mask=m, dtype=torch.bfloat16)
+    st = fa.get_status()
+    assert st == fa.FA_OK, fa.load().fa_status_string(st)
+    O_ref, L_ref = oracle.fp8_attention_fwd(t_ref, scale, causal=causal, mask=inp["mask"])
+    check_fwd(O, L, O_ref, L_ref, "bf16")
 
 
 def test_debug_build_reports_its_status_code(debug_lib):
