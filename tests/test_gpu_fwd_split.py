@@ -133,3 +133,37 @@ def test_split_fwd_workload_trading_day_sampled(cuda_lib):
         o = oracle_inputs({n: inp[n][0, h] for n in "qkv"})
         O_ref, L_ref = oracle.attention_fwd_rows(o["q"], o["k"], o["v"], rows, w.scale, causal=True)
         check_fwd(O[0, h, rows], L[0, h, rows], O_ref, L_ref, w.dtype)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_fwd_d128_block_mask(cuda_lib, causal):
+    """d = 128 with a block mask and 3 slices per query tile: the slices' cluster merge
+    against the oracle."""
+    inp = synth.make_inputs(1, 3, 1100, 128, "bf16", seed=5600, mask_p=0.5, backward=False)
+    O, L = _run(inp, 3, causal, inp["mask"], 128)
+    check_fwd(O, L, *_ref(inp, causal, inp["mask"], 128), "bf16")
+
+
+def test_split_fwd_concurrent_streams(cuda_lib):
+    """Two split forwards (different problems, different slice counts) on two streams
+    at once give the results they give one after the other."""
+    a = synth.make_inputs(1, 2, 2000, 64, "bf16", seed=5700, backward=False)
+    b = synth.make_inputs(2, 1, 1500, 128, "f16", seed=5701, backward=False)
+    ta = [a[n].cuda() for n in "qkv"]
+    tb = [b[n].cuda() for n in "qkv"]
+    Oa, La = fa.attention_fwd_split(*ta, causal=True, splits=5)
+    Ob, Lb = fa.attention_fwd_split(*tb, causal=False, splits=3)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            oa, la = fa.attention_fwd_split(*ta, causal=True, splits=5, stream=s1)
+        with torch.cuda.stream(s2):
+            ob, lb = fa.attention_fwd_split(*tb, causal=False, splits=3, stream=s2)
+        outs.append((oa, la, ob, lb))
+    torch.cuda.synchronize()
+    assert fa.get_status() == fa.FA_OK
+    for oa, la, ob, lb in outs:
+        assert torch.equal(oa, Oa) and torch.equal(la, La)
+        assert torch.equal(ob, Ob) and torch.equal(lb, Lb)
