@@ -210,3 +210,29 @@ def test_bwd_workload_block_sparse_n16384_sampled(cuda_lib):
     w = synth.WORKLOADS["bf16_sparse_n16384"]
     _sampled(w, [(0, 0), (1, 3), (1, 15)], 256, 256, 55,
              always=[*range(0, 128), *range(w.N - 128, w.N)])
+
+
+def test_bwd_concurrent_streams(cuda_lib):
+    """Two backward passes (one sliced, one with whole key tiles; separate workspaces) on
+    two streams at once give the gradients they give one after the other, up to the
+    order of the dQ accumulator's additions."""
+    a = synth.make_inputs(1, 2, 1500, 64, "bf16", seed=4700)   # 24 key tiles: sliced
+    b = synth.make_inputs(2, 12, 1024, 64, "bf16", seed=4701)  # 192 key tiles: whole
+    probs = []
+    for inp, causal in ((a, False), (b, True)):
+        q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+        o, lse = fa.attention_fwd(q, k, v, causal=causal)
+        probs.append((q, k, v, do, o, lse, causal))
+    ref = [fa.attention_bwd(q, k, v, o, do, lse, causal=c) for q, k, v, do, o, lse, c in probs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    got = []
+    for _ in range(3):
+        for (q, k, v, do, o, lse, c), st in zip(probs, streams):
+            with torch.cuda.stream(st):
+                got.append(fa.attention_bwd(q, k, v, o, do, lse, causal=c, stream=st))
+    torch.cuda.synchronize()
+    assert fa.get_status() == fa.FA_OK
+    for i, g in enumerate(got):
+        for x, x0 in zip(g, ref[i % 2]):
+            assert rel_fro(to_np64(x), to_np64(x0)) <= 1e-3
